@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 MoE layer: µs per layer and effective weight HBM GB/s.
+
+Default workload: Ling-shape decode, T=1, d=2560, 512 experts top-8 + 1 shared
+expert, SwiGLU I=768; 32 weight sets cycled so consecutive calls never hit L2
+(one cycle reads ~1.26 GB of distinct weights; L2 is 129 MB).
+
+One step = one replay of a CUDA graph holding one layer call per weight set
+(32 calls for the default workload). value = µs per layer call with inputs
+resident in HBM; e2e = the same through the C ABI with the step's activations
+copied from pinned host memory and y copied back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer does not shard across GPUs here); value is the job aggregate
+(max time over ranks / layer calls of all ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "µs per MoE layer and effective weight HBM GB/s (% of GB300 peak) at T=1"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ling_t1", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--sets", type=int, default=None, help="weight sets cycled (default: the workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for profilers: no clocks, e2e or CPU baseline")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas only)
+
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+
+def weight_bytes_per_call(w, D):
+    return wl.weight_bytes(w, D)
+
+
+def stage_bytes(w, stage, D, slots):
+    """Algorithmic HBM bytes of one launch of a stage (weights + activations moved)."""
+    T, d, I, E = w.T, w.d, w.I, w.E
+    per_gu = 2 * I * d // 2 + 2 * I * d // 32
+    per_dn = d * I // 2 + d * I // 32
+    return {
+        "act_split_x": T * d * 2 + T * (d // 32) * 130,
+        "router_shared_gateup": E * d * 2 + 2 * I * d * 2 + T * d * 2 + T * (E + I) * 4,
+        "topk": T * E * 4 + T * w.k * 8,
+        "sort": T * w.k * 4 * 4,
+        "routed_gateup": D * per_gu + slots * I * 4,
+        "act_split_h": slots * I * 4 + slots * (I // 32) * 130,
+        "routed_down": D * per_dn + slots * d * 4,
+        "combine": d * I * 2 + slots * d * 4 + T * d * 2,
+    }.get(stage, 0)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_src, kernel):
+    """dram bytes per launch from profiles/dram_traffic.txt if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    for ln in open(p):
+        f = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("src_sha") == sha:
+            return int(float(f["bytes_per_launch"]))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+
+def oracle_layer_sample(w, set_idx, token, device):
+    """Inputs for one oracle layer call: x row, router, shared, and the MXFP4
+    codes/scales of the experts the oracle's own routing selects (prepared
+    untimed, from the generator's fp32 weights)."""
+    from oracle import moe as omoe
+    from oracle import mxfp4
+    x = wl.gen_x(w, set_idx, "cpu" if device == "cpu" else device).cpu()[token:token + 1]
+    router = omoe.as_f64(wl.gen_router(w, set_idx, device))
+    shared = tuple(omoe.as_f64(t) for t in wl.gen_shared(w, set_idx, device))
+    bias = wl.gen_bias(w, set_idx, "cpu")
+    if bias is not None:
+        bias = bias.numpy()
+        if bias.ndim == 2:
+            bias = bias[token:token + 1]
+    xs = omoe.as_f64(x)
+    idx, _, _ = omoe.route_topk(omoe.router_logits(xs, router).astype(np.float32), w.k, bias)
+    packed = {}
+    for e in sorted(set(idx.ravel().tolist())):
+        gu, dn = wl.gen_expert(w, set_idx, e, device)
+        c1, s1, _ = mxfp4.quantize(gu.cpu().numpy())
+        c2, s2, _ = mxfp4.quantize(dn.cpu().numpy())
+        packed[e] = (c1, s1, c2, s2)
+    return xs, router, shared, bias, packed
+
+
+def oracle_layer_call(w, xs, router, shared, bias, packed):
+    """One timed layer call of the oracle: logits, top-k, dequantise the selected
+    experts from MXFP4, SwiGLU experts, shared expert."""
+    from oracle import moe as omoe
+    from oracle import mxfp4
+    logits = omoe.router_logits(xs, router)
+    idx, _, _ = omoe.route_topk(logits.astype(np.float32), w.k, bias)
+    experts = {}
+    for e in set(idx.ravel().tolist()):
+        c1, s1, c2, s2 = packed[e]
+        gu = mxfp4.dequantize(c1, s1)
+        experts[e] = omoe.Expert(gu[:w.I], gu[w.I:], mxfp4.dequantize(c2, s2))
+    return omoe.moe_layer(xs, router, experts, shared, w.k, bias=bias, idx=idx)["y"]
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count()
+
+
+def time_oracle(w, n_calls, device, budget_s=25.0):
+    samples = [oracle_layer_sample(w, s % max(1, w.sets), 0, device) for s in range(min(n_calls, 4))]
+    oracle_layer_call(w, *samples[0])     # warm caches / BLAS threads
+    t0 = time.perf_counter()
+    done = 0
+    while done < n_calls and (time.perf_counter() - t0) < budget_s:
+        oracle_layer_call(w, *samples[done % len(samples)])
+        done += 1
+    dt = time.perf_counter() - t0
+    return dt / done * 1e6, done, dt
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args, w):
+    rank, ws = dist_setup("gloo")
+    if rank != 0:
+        return
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    steps = args.steps or 20
+    from oracle import moe as omoe  # noqa: F401  (the oracle is the reference arm here)
+    samples = [oracle_layer_sample(w, s % max(1, w.sets), 0, device) for s in range(min(steps, 4))]
+    for i in range(args.warmup):
+        oracle_layer_call(w, *samples[i % len(samples)])
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle_layer_call(w, *samples[i % len(samples)])
+    dt = time.perf_counter() - t0
+    us = dt / steps * 1e6
+    D = w.k * min(w.T, 1)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/layer",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name} (one token per step)", "T": 1, "d": w.d, "E": w.E, "k": w.k,
+                   "I": w.I},
+        "effective_gbs": weight_bytes_per_call(w, D) / (us * 1e-6) / 1e9,
+        "cpu_baseline": {"value": us, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{steps} single-token layer calls of {w.name}, experts dequantised "
+                                   f"from MXFP4 inside each call"},
+        "e2e": {"value": us, "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    rank, ws = dist_setup("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import mxfp4_expert_gb300 as mx
+    from mxfp4_expert_gb300 import synthetic
+
+    n_sets = args.sets or w.sets
+    t_setup = time.perf_counter()
+    base = synthetic.build_layer(w, 0, device=dev)
+    layers = [base] + [synthetic.clone_rotated(base, w, s, device=dev) for s in range(1, n_sets)]
+    xs, biases = [], []
+    for s in range(n_sets):
+        x, b = synthetic.inputs(w, s, device=dev)
+        xs.append(x)
+        biases.append(b)
+    ys = [torch.empty_like(x) for x in xs]
+    wsb = mx.moe_workspace_bytes(base.shape, w.T)
+    work = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(n_sets)]
+    idxs = [torch.empty((w.T, w.k), dtype=torch.int32, device=dev) for _ in range(n_sets)]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    path = mx.moe_query_path(base.shape, w.T)
+    stages = mx.moe_stage_names(path)
+    n_ev = len(stages) + 1
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_sets)]
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_cycle(with_events, copies=None):
+        for s in range(n_sets):
+            if copies is not None:
+                xs[s].copy_(copies[0][s], non_blocking=True)
+            mx.moe_forward(layers[s], xs[s], biases[s], y=ys[s], workspace=work[s], idx_out=idxs[s],
+                           dev_status=status, stage_events=events[s] if with_events else None,
+                           stream=stream)
+            if copies is not None:
+                copies[1][s].copy_(ys[s], non_blocking=True)
+
+    # eager warm-up (also sets kernel attributes outside capture)
+    with torch.cuda.stream(stream):
+        one_cycle(False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    # distinct experts per set (for algorithmic bytes)
+    D_sets = [len(set(i.cpu().numpy().ravel().tolist())) for i in idxs]
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        one_cycle(True)
+    steps = args.steps or (10 if args.profile else max(50, int(2.0 / max(1e-6, 32 * 12e-6 * max(1, w.T / 4)))))
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    if not args.profile:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.stop() if not args.profile else None
+    ms = max_over_ranks(ms, ws, dev)
+    calls = steps * n_sets
+    us_per_layer = ms * 1e3 / (calls * ws)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # per-stage durations of the last replayed cycle (events recorded inside the graph)
+    stage_us = {n: [] for n in stages}
+    for s in range(n_sets):
+        for i, n in enumerate(stages):
+            stage_us[n].append(events[s][i].elapsed_time(events[s][i + 1]) * 1e3)
+    stage_mean = {n: float(np.mean(v)) for n, v in stage_us.items()}
+    dom = max(stage_mean, key=stage_mean.get)
+    D_mean = float(np.mean(D_sets))
+    slots = w.T * w.k
+    dom_bytes = float(np.mean([stage_bytes(w, dom, D, slots) for D in D_sets]))
+    peak, peak_kind = measured_peaks()
+    achieved = dom_bytes / (stage_mean[dom] * 1e-6) / 1e9
+    kernel_src = os.path.join(ROOT, "mxfp4_expert_gb300", "csrc",
+                              "experts.cu" if dom.startswith("routed") else "dense.cu")
+    traffic = profiled_traffic(kernel_src, dom)
+    algo_bytes = float(np.mean([weight_bytes_per_call(w, D) for D in D_sets]))
+    eff_gbs = algo_bytes * calls * ws / (ms * 1e-3) / 1e9     # whole-job weight bytes per second
+
+    # e2e through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e and not args.profile:
+        hx = [x.cpu().pin_memory() for x in xs]
+        hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            one_cycle(False, (hx, hy))
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g2, stream=stream):
+            one_cycle(False, (hx, hy))
+        for _ in range(args.warmup):
+            g2.replay()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g2.replay()
+            e1.record(stream)
+        e1.synchronize()
+        ms2 = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+        e2e = {"value": ms2 * 1e3 / (calls * ws), "unit": "us/layer",
+               "h2d_bytes_per_step": n_sets * w.T * w.d * 2, "d2h_bytes_per_step": n_sets * w.T * w.d * 2}
+
+    launches_per_call = {"act_split_x": 1, "router_shared_gateup": 1, "topk": 1, "sort": 3,
+                         "routed_gateup": 1, "act_split_h": 1, "routed_down": 1, "combine": 1}
+    per_call = sum(launches_per_call.get(n, 1) for n in stages)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and not args.profile:
+        us_cpu, n_done, dt = time_oracle(w, 64, dev, budget_s=20.0)
+        cpu = {"value": us_cpu, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n_done} single-token layer calls of {w.name} in {dt:.1f} s "
+                         f"(numpy fp64; experts dequantised from MXFP4 inside each call)"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": us_per_layer, "unit": "us/layer", "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1xe4m3->f32 (mma.sync), bf16 router/shared, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, E={w.E}, k={w.k}, I={w.I}, shared=1",
+                   "weight_sets_cycled": n_sets, "layers_per_step": n_sets,
+                   "l2": f"defeated by cycling {n_sets} weight sets "
+                         f"({n_sets * algo_bytes / 1e9:.2f} GB of weights read per step; L2 129 MB)",
+                   "distinct_experts_mean": D_mean, "path": stages, "setup_s": round(setup_s, 1)},
+        "effective_gbs": eff_gbs,
+        "pct_of_hbm_peak": 100.0 * eff_gbs / peak,
+        "algorithmic_bytes_per_layer": algo_bytes,
+        "stage_us": stage_mean,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": dom_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": per_call * calls,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = wl.get(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * moe_mxfp4.h — C ABI of a GB300 (sm_103a) mixture-of-experts layer with
+ * MXFP4 expert weights, for decode (T = 1 .. 64 tokens) and prefill.
+ *
+ * What is computed (page "3 ways to speed up MoE inference on NVIDIA DGX
+ * Spark", §2: every MoE layer sends each token to 8 of 512 routed experts plus
+ * one shared expert; §3: moe_intermediate_size 768; §1: at batch 1, decode is
+ * bound by reading weights). Per token t with activations x (bf16, width d):
+ *
+ *   l[e]   = sum_j x[j] * Wr[e][j]                      router logits (fp32)
+ *   key[e] = l[e] + bias[e]                             fp32 add; bias optional
+ *   S      = the k experts with the largest key; equal keys -> lower index
+ *   w[j]   = exp(key[S_j] - key[S_0]) / sum_i exp(key[S_i] - key[S_0])
+ *   h_e    = silu(Wg_e x) * (Wu_e x)                    SwiGLU, fp32
+ *   y      = sum_j w[j] * Wd_{S_j} h_{S_j}  +  Wd_sh (silu(Wg_sh x) * (Wu_sh x))
+ *
+ * Routed experts are stored in MXFP4 (OCP Microscaling v1.0): E2M1 codes
+ * (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, sign bit), one E8M0 scale
+ * 2^(s-127) per 32 consecutive elements along K. Router and shared expert
+ * are bf16. Accumulation is fp32; y is bf16.
+ *
+ * Conventions for every entry point
+ *   - Pointers ending in a device buffer are device pointers owned by the
+ *     caller; the library allocates no device memory and keeps no mutable
+ *     global state. Host pointers are marked "host".
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream). Nothing synchronises the host.
+ *   - Return value: MOE_OK (0) or a negative moe_status. Arguments are
+ *     checked before anything is enqueued; on error nothing is enqueued.
+ *   - Conditions only a kernel can see are OR-ed into *dev_status (a device
+ *     int the caller zeroes and reads after synchronising), as moe_dev_status
+ *     bits. dev_status may be NULL where noted.
+ *   - There is no CPU fallback and no alternate backend: an unsupported
+ *     shape is an error, never a silent slow path.
+ *   - Calls are reentrant; concurrent calls must not share output or
+ *     workspace buffers.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* == cudaStream_t */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* null pointer, negative size, bad enum */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* e.g. K % 32 != 0, N % 16 != 0, k > E */
+  MOE_ERR_BAD_DESCRIPTOR = -3,     /* packed-weight descriptor does not match */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_BUFFER_TOO_SMALL = -5,   /* packed buffer smaller than required */
+  MOE_ERR_CUDA = -6,               /* a CUDA runtime call failed */
+  MOE_ERR_NO_DEVICE = -7           /* current device is not sm_103 */
+} moe_status;
+
+/* Bits OR-ed into *dev_status by kernels. */
+typedef enum moe_dev_status {
+  MOE_DEV_NONFINITE_INPUT = 1,  /* pack: a block held inf/NaN (its scale byte is 255) */
+  MOE_DEV_SCALE_RANGE = 2,      /* pack: a scale byte above 248 (|w| >= 2^122); the
+                                   expert kernels cannot represent it */
+  MOE_DEV_INDEX_OOB = 4,        /* a routing index outside [0, E) reached a kernel */
+  MOE_DEV_TIMEOUT = 8           /* a bounded wait in a kernel gave up */
+} moe_dev_status;
+
+/* Packed layouts (byte formats of moe_pack_mxfp4's output).
+ *
+ * MOE_LAYOUT_MMA16: matrix W [N][K] (N % 16 == 0, K % 32 == 0) is cut into
+ *   row tiles of 16 rows. For tile r (rows 16r..16r+15) and K-block b
+ *   (columns 32b..32b+31) a 272-byte unit sits at byte (r*K/32 + b) * 272:
+ *     bytes [0, 256): the 512 E2M1 codes, 8 bytes per lane l = 4g + q
+ *       (g = l/4, q = l%4): word 0 holds rows g and g+8 at columns
+ *       32b + 4q + (0..3), word 1 the same rows at columns 32b + 16 + 4q + (0..3).
+ *       In byte j of a word, row g's code sits at bits {2: m, 3: e0, 4: e1,
+ *       7: sign} and row g+8's at bits {0: m, 1: e0, 6: e1, 5: sign}; masking
+ *       the first with 0x9C, or shifting the second into place, gives the
+ *       code as an E4M3 byte worth 2^-6 times the E2M1 value.
+ *     bytes [256, 272): scale bytes, row g at 256 + 2g, row g+8 at 257 + 2g.
+ *   Bytes per matrix: N*K/2 + N*K/32 (exactly the MXFP4 payload).
+ * MOE_LAYOUT_MMA16_GATEUP: the input matrix is a fused [2I][K] gate/up
+ *   projection (rows 0..I-1 gate, I..2I-1 up, I % 8 == 0). Packed tile r
+ *   holds gate rows 8r..8r+7 as its rows 0..7 and up rows 8r..8r+7 as its
+ *   rows 8..15; otherwise as MOE_LAYOUT_MMA16.
+ */
+typedef enum moe_layout {
+  MOE_LAYOUT_MMA16 = 1,
+  MOE_LAYOUT_MMA16_GATEUP = 2
+} moe_layout;
+
+#define MOE_PACK_MAGIC 0x3446584Du /* "MXF4" */
+#define MOE_PACK_VERSION 1u
+
+/* Host-side descriptor of a packed weight buffer. moe_pack_mxfp4 fills it;
+ * moe_forward refuses buffers whose descriptor does not match the layer
+ * shape (MOE_ERR_BAD_DESCRIPTOR) instead of reinterpreting them. */
+typedef struct moe_packed_desc {
+  uint32_t magic;        /* MOE_PACK_MAGIC */
+  uint32_t version;      /* MOE_PACK_VERSION */
+  int32_t layout;        /* moe_layout */
+  int32_t n_mat;         /* number of matrices (experts) */
+  int32_t N, K;          /* rows, reduction length of each matrix */
+  uint64_t bytes_per_mat;
+  uint64_t total_bytes;
+} moe_packed_desc;
+
+typedef struct moe_shape {
+  int32_t d_model;    /* d: hidden width (multiple of 256) */
+  int32_t d_ff;       /* I: expert intermediate width (multiple of 32) */
+  int32_t n_experts;  /* E: routed experts (1 .. 1024) */
+  int32_t top_k;      /* k: experts per token (1 .. min(E, 32)) */
+  int32_t has_shared; /* 1: one bf16 shared expert, 0: none */
+} moe_shape;
+
+/* A layer's weights (all device pointers, caller-owned, read-only). */
+typedef struct moe_layer {
+  moe_shape shape;
+  const void* router_w;        /* bf16 [E][d] row-major */
+  const void* gate_up;         /* packed, MOE_LAYOUT_MMA16_GATEUP, n_mat=E, N=2I, K=d */
+  moe_packed_desc gate_up_desc;
+  const void* down;            /* packed, MOE_LAYOUT_MMA16, n_mat=E, N=d, K=I */
+  moe_packed_desc down_desc;
+  const void* shared_gate;     /* bf16 [I][d]  (unused if has_shared == 0) */
+  const void* shared_up;       /* bf16 [I][d] */
+  const void* shared_down;     /* bf16 [d][I] */
+} moe_layer;
+
+/* Kernel paths moe_forward can take (moe_query_path). */
+typedef enum moe_path {
+  MOE_PATH_DECODE_MMA = 1   /* per-stage kernels: router GEMV, top-k + sort,
+                               MXFP4 expert GEMVs on e4m3 mma.sync, combine */
+} moe_path;
+
+/* ---- packing ------------------------------------------------------------ */
+
+/* Bytes of a packed buffer for n_mat matrices [N][K] in `layout`; 0 if the
+ * shape or layout is unsupported. */
+size_t moe_packed_bytes(int n_mat, int N, int K, int layout);
+
+/* Fill *out (host) with the descriptor of a packed buffer of that shape
+ * (for buffers packed earlier and stored). */
+int moe_describe_packed(int n_mat, int N, int K, int layout, moe_packed_desc* out);
+
+/* Quantise fp32 weights to MXFP4 and write them in `layout`.
+ *   w_dev       fp32 [n_mat][N][K] row-major (device)
+ *   packed_dev  output, packed_bytes >= moe_packed_bytes(...) (device, 16-B aligned)
+ *   desc_out    host, may be NULL
+ *   dev_status  device int, may be NULL; MOE_DEV_NONFINITE_INPUT,
+ *               MOE_DEV_SCALE_RANGE
+ * Rule (OCP MX v1.0, §6.3): per 32-block, s = clamp(floor(log2 amax) - 2 +
+ * 127, 0, 254) (amax = 0 -> 0); codes = RNE(v * 2^(127-s)) onto the E2M1
+ * grid, ties to even mantissa, saturating at 6, sign kept (-0 -> code 8).
+ * A block with inf/NaN gets scale 255, its non-finite elements code 0. */
+int moe_pack_mxfp4(const float* w_dev, int n_mat, int N, int K, int layout,
+                   void* packed_dev, size_t packed_bytes, moe_packed_desc* desc_out,
+                   int* dev_status, moe_stream_t stream);
+
+/* Inverse permutation of a packed buffer into the canonical MXFP4 layout
+ * (test aid): codes [n_mat][N][K/2] (element 2j in the low nibble of byte j),
+ * scales [n_mat][N][K/32], rows in the order of moe_pack_mxfp4's input. */
+int moe_unpack_mxfp4(const void* packed_dev, const moe_packed_desc* desc,
+                     uint8_t* codes_dev, uint8_t* scales_dev, moe_stream_t stream);
+
+/* ---- routing ------------------------------------------------------------ */
+
+/* Top-k selection and renormalised softmax weights from fp32 logits.
+ *   logits_dev      fp32 [T][E]
+ *   bias_dev        fp32, NULL for none; bias_row_stride 0: one row [E]
+ *                   for all tokens, >= E: row t at bias_dev + t*stride
+ *   idx_dev         int32 [T][k], slots in descending key order
+ *   w_dev           fp32 [T][k]
+ * Keys are logit + bias in fp32 (round-to-nearest-even); -0 ranks as +0, NaN
+ * ranks as -inf; equal keys go to the lower expert index. E <= 1024, k <= 32. */
+int moe_route_topk(const float* logits_dev, int T, int E, int k,
+                   const float* bias_dev, int bias_row_stride,
+                   int32_t* idx_dev, float* w_dev, moe_stream_t stream);
+
+/* Group (token, slot) pairs by expert, stable in p = t*k + j (page "MoE-SpeQ
+ * ...", §4.2: sort the verify tokens' expert assignments by expert id so each
+ * expert runs once over all its tokens).
+ *   idx_dev      int32 [T][k], values in [0, E)
+ *   counts_dev   int32 [E]; offsets_dev int32 [E+1] (exclusive scan)
+ *   perm_dev     int32 [T*k]: sorted position -> p;  inv_dev: p -> position
+ *   active_dev   int32 [E]: the D experts with count > 0, ascending
+ *   n_active_dev int32 [1]: D
+ *   workspace    >= moe_sort_workspace_bytes(T, k, E) bytes (device)
+ * An index outside [0, E) sets MOE_DEV_INDEX_OOB in dev_status (may be NULL);
+ * that pair is left out of every list (its inv entry is -1 and offsets[E]
+ * counts only the pairs kept). */
+size_t moe_sort_workspace_bytes(int T, int k, int E);
+int moe_sort_by_expert(const int32_t* idx_dev, int T, int k, int E,
+                       int32_t* counts_dev, int32_t* offsets_dev, int32_t* perm_dev,
+                       int32_t* inv_dev, int32_t* active_dev, int32_t* n_active_dev,
+                       void* workspace_dev, size_t workspace_bytes, int* dev_status,
+                       moe_stream_t stream);
+
+/* ---- the layer ---------------------------------------------------------- */
+
+/* Device workspace moe_forward needs for T tokens (256-B aligned base). */
+size_t moe_workspace_bytes(const moe_shape* shape, int T);
+
+/* Which moe_path moe_forward takes for this shape and T; negative status if
+ * unsupported. */
+int moe_query_path(const moe_shape* shape, int T);
+
+/* The layer over T tokens.
+ *   L             host struct with device weight pointers and descriptors
+ *   x_dev         bf16 [T][d];  y_dev bf16 [T][d] (may not alias x)
+ *   bias_dev      fp32 router bias as in moe_route_topk (NULL: none)
+ *   logits_out    fp32 [T][E] router logits before bias (NULL: not returned)
+ *   idx_out       int32 [T][k]; w_out fp32 [T][k] (NULL: not returned)
+ *   workspace_dev >= moe_workspace_bytes(&L->shape, T) bytes
+ *   dev_status    device int (may be NULL)
+ *   stage_events  NULL, or n_stage_events cudaEvent_t handles (host array,
+ *                 caller-created): event 0 is recorded on `stream` before the
+ *                 first kernel and event i after stage i (stages listed by
+ *                 moe_stage_names), for per-stage timing; extra events are
+ *                 left untouched.
+ * Activations must satisfy |x| < 2^100 and expert outputs stay finite. */
+int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                const float* bias_dev, int bias_row_stride,
+                float* logits_out, int32_t* idx_out, float* w_out,
+                void* workspace_dev, size_t workspace_bytes, int* dev_status,
+                void* const* stage_events, int n_stage_events,
+                moe_stream_t stream);
+
+/* Comma-separated names of the stages of `path` in launch order (the
+ * boundaries moe_forward's stage_events mark); NULL for an unknown path. */
+const char* moe_stage_names(int path);
+
+/* Static text for a moe_status value. */
+const char* moe_status_string(int status);
+
+/* Library version, e.g. "moe_mxfp4 1.0 sm_103a". */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXFP4_H */

@@ -1,0 +1,278 @@
+"""Python binding of libmoe_mxfp4 — the GB300 (sm_103a) MXFP4 mixture-of-experts layer.
+
+The functions here carry the C-ABI names (see include/moe_mxfp4.h) and only
+marshal arguments: every step of the layer runs in the library's CUDA
+kernels. PyTorch supplies device memory and streams. There is no CPU or
+PyTorch fallback: importing this package fails if the library has not been
+built, and every call raises ``MoeError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "MoeError", "LIB_PATH", "lib", "MOE_LAYOUT_MMA16", "MOE_LAYOUT_MMA16_GATEUP",
+    "MOE_PATH_DECODE_MMA", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
+    "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
+    "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
+    "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_status_string", "moe_version",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp4.so")
+
+MOE_LAYOUT_MMA16 = 1
+MOE_LAYOUT_MMA16_GATEUP = 2
+MOE_PATH_DECODE_MMA = 1
+DEV_NONFINITE_INPUT, DEV_SCALE_RANGE, DEV_INDEX_OOB, DEV_TIMEOUT = 1, 2, 4, 8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {moe_status_string(status)} (status {status})")
+        self.status = status
+
+
+class moe_packed_desc(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("layout", ctypes.c_int32),
+                ("n_mat", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("bytes_per_mat", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("has_shared", ctypes.c_int32)]
+
+
+class moe_layer(ctypes.Structure):
+    _fields_ = [("shape", moe_shape), ("router_w", ctypes.c_void_p),
+                ("gate_up", ctypes.c_void_p), ("gate_up_desc", moe_packed_desc),
+                ("down", ctypes.c_void_p), ("down_desc", moe_packed_desc),
+                ("shared_gate", ctypes.c_void_p), ("shared_up", ctypes.c_void_p),
+                ("shared_down", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing. Build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+            "(nvcc, sm_103a). This package has no CPU or PyTorch fallback.")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "moe_packed_bytes": (sz, [i32, i32, i32, i32]),
+        "moe_describe_packed": (i32, [i32, i32, i32, i32, ctypes.POINTER(moe_packed_desc)]),
+        "moe_pack_mxfp4": (i32, [vp, i32, i32, i32, i32, vp, sz, ctypes.POINTER(moe_packed_desc), vp, vp]),
+        "moe_unpack_mxfp4": (i32, [vp, ctypes.POINTER(moe_packed_desc), vp, vp, vp]),
+        "moe_route_topk": (i32, [vp, i32, i32, i32, vp, i32, vp, vp, vp]),
+        "moe_sort_workspace_bytes": (sz, [i32, i32, i32]),
+        "moe_sort_by_expert": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+        "moe_workspace_bytes": (sz, [ctypes.POINTER(moe_shape), i32]),
+        "moe_query_path": (i32, [ctypes.POINTER(moe_shape), i32]),
+        "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
+                                ctypes.POINTER(ctypes.c_void_p), i32, vp]),
+        "moe_stage_names": (ctypes.c_char_p, [i32]),
+        "moe_status_string": (ctypes.c_char_p, [i32]),
+        "moe_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    return L
+
+
+lib = _load()
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MoeError(what, status)
+
+
+def _cuda(t, dtype, name):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def moe_status_string(status: int) -> str:
+    return lib.moe_status_string(status).decode()
+
+
+def moe_version() -> str:
+    return lib.moe_version().decode()
+
+
+def moe_packed_bytes(n_mat: int, N: int, K: int, layout: int) -> int:
+    return int(lib.moe_packed_bytes(n_mat, N, K, layout))
+
+
+def moe_describe_packed(n_mat: int, N: int, K: int, layout: int) -> moe_packed_desc:
+    d = moe_packed_desc()
+    _check(lib.moe_describe_packed(n_mat, N, K, layout, ctypes.byref(d)), "moe_describe_packed")
+    return d
+
+
+def moe_pack_mxfp4(w: torch.Tensor, layout: int, out: torch.Tensor | None = None,
+                   dev_status: torch.Tensor | None = None, stream=None):
+    """fp32 [n_mat, N, K] (or [N, K]) -> (packed uint8 tensor, moe_packed_desc)."""
+    _cuda(w, torch.float32, "w")
+    n_mat, N, K = (1, *w.shape) if w.dim() == 2 else tuple(w.shape)
+    nbytes = moe_packed_bytes(n_mat, N, K, layout)
+    if nbytes == 0:
+        raise MoeError("moe_pack_mxfp4", -2)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    desc = moe_packed_desc()
+    _check(lib.moe_pack_mxfp4(_p(w), n_mat, N, K, layout, _p(out), out.numel(), ctypes.byref(desc),
+                              _p(dev_status), _s(stream)), "moe_pack_mxfp4")
+    return out, desc
+
+
+def moe_unpack_mxfp4(packed: torch.Tensor, desc: moe_packed_desc, stream=None):
+    """Packed buffer -> canonical (codes [n_mat, N, K/2], scales [n_mat, N, K/32]) uint8."""
+    codes = torch.empty((desc.n_mat, desc.N, desc.K // 2), dtype=torch.uint8, device=packed.device)
+    scales = torch.empty((desc.n_mat, desc.N, desc.K // 32), dtype=torch.uint8, device=packed.device)
+    _check(lib.moe_unpack_mxfp4(_p(packed), ctypes.byref(desc), _p(codes), _p(scales), _s(stream)),
+           "moe_unpack_mxfp4")
+    return codes, scales
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, bias: torch.Tensor | None = None,
+                   idx: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None):
+    """fp32 logits [T, E] -> (idx int32 [T, k], w fp32 [T, k]); bias [E] or [T, E]."""
+    _cuda(logits, torch.float32, "logits")
+    T, E = logits.shape
+    stride = 0
+    if bias is not None:
+        _cuda(bias, torch.float32, "bias")
+        stride = 0 if bias.dim() == 1 else bias.shape[1]
+    idx = torch.empty((T, k), dtype=torch.int32, device=logits.device) if idx is None else idx
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device) if w is None else w
+    _check(lib.moe_route_topk(_p(logits), T, E, k, _p(bias), stride, _p(idx), _p(w), _s(stream)),
+           "moe_route_topk")
+    return idx, w
+
+
+def moe_sort_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(lib.moe_sort_workspace_bytes(T, k, E))
+
+
+def moe_sort_by_expert(idx: torch.Tensor, E: int, dev_status: torch.Tensor | None = None, stream=None):
+    """int32 idx [T, k] -> dict(counts, offsets, perm, inv, active, n_active) device tensors."""
+    _cuda(idx, torch.int32, "idx")
+    T, k = idx.shape
+    dev = idx.device
+    out = {"counts": torch.empty(E, dtype=torch.int32, device=dev),
+           "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+           "perm": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "inv": torch.empty(T * k, dtype=torch.int32, device=dev),
+           "active": torch.empty(E, dtype=torch.int32, device=dev),
+           "n_active": torch.empty(1, dtype=torch.int32, device=dev)}
+    nws = moe_sort_workspace_bytes(T, k, E)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+    _check(lib.moe_sort_by_expert(_p(idx), T, k, E, _p(out["counts"]), _p(out["offsets"]), _p(out["perm"]),
+                                  _p(out["inv"]), _p(out["active"]), _p(out["n_active"]), _p(ws), ws.numel(),
+                                  _p(dev_status), _s(stream)), "moe_sort_by_expert")
+    return out
+
+
+def _shape(d, I, E, k, has_shared) -> moe_shape:
+    return moe_shape(d, I, E, k, 1 if has_shared else 0)
+
+
+def moe_workspace_bytes(shape: moe_shape, T: int) -> int:
+    return int(lib.moe_workspace_bytes(ctypes.byref(shape), T))
+
+
+def moe_query_path(shape: moe_shape, T: int) -> int:
+    return int(lib.moe_query_path(ctypes.byref(shape), T))
+
+
+def moe_stage_names(path: int) -> list[str]:
+    r = lib.moe_stage_names(path)
+    return [] if r is None else r.decode().split(",")
+
+
+class Layer:
+    """Device weights of one layer plus the moe_layer struct the C ABI takes.
+
+    router_w bf16 [E, d]; gate_up packed (layout MMA16_GATEUP, n_mat=E, N=2I,
+    K=d); down packed (layout MMA16, n_mat=E, N=d, K=I); shared_* bf16 or None.
+    """
+
+    def __init__(self, router_w, gate_up, gate_up_desc, down, down_desc,
+                 shared_gate=None, shared_up=None, shared_down=None, top_k=8):
+        E, d = router_w.shape
+        I = gate_up_desc.N // 2
+        self.router_w, self.gate_up, self.down = router_w, gate_up, down
+        self.shared = (shared_gate, shared_up, shared_down)
+        has_shared = shared_gate is not None
+        self.shape = _shape(d, I, E, top_k, has_shared)
+        self.struct = moe_layer(self.shape, router_w.data_ptr(), gate_up.data_ptr(), gate_up_desc,
+                                down.data_ptr(), down_desc,
+                                shared_gate.data_ptr() if has_shared else None,
+                                shared_up.data_ptr() if has_shared else None,
+                                shared_down.data_ptr() if has_shared else None)
+
+    @classmethod
+    def from_fp32(cls, router_w, gate_up_f32, down_f32, shared=None, top_k=8, stream=None):
+        """Pack fp32 expert weights (gate_up [E, 2I, d], down [E, d, I]) with moe_pack_mxfp4."""
+        gu, gud = moe_pack_mxfp4(gate_up_f32, MOE_LAYOUT_MMA16_GATEUP, stream=stream)
+        dn, dnd = moe_pack_mxfp4(down_f32, MOE_LAYOUT_MMA16, stream=stream)
+        sg, su, sd = shared if shared is not None else (None, None, None)
+        return cls(router_w, gu, gud, dn, dnd, sg, su, sd, top_k=top_k)
+
+    @property
+    def d(self):
+        return self.shape.d_model
+
+    def workspace_bytes(self, T: int) -> int:
+        return moe_workspace_bytes(self.shape, T)
+
+
+def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
+                y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
+                w_out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                stage_events=None, stream=None):
+    """y = layer(x) for bf16 x [T, d]; returns y (bf16 [T, d]).
+
+    stage_events: optional list of torch.cuda.Event (enable_timing=True); see
+    moe_stage_names for what each boundary marks.
+    """
+    _cuda(x, torch.bfloat16, "x")
+    T = x.shape[0]
+    stride = 0
+    if bias is not None:
+        _cuda(bias, torch.float32, "bias")
+        stride = 0 if bias.dim() == 1 else bias.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(layer.workspace_bytes(T), dtype=torch.uint8, device=x.device)
+    ev_arr, n_ev = None, 0
+    if stage_events:
+        n_ev = len(stage_events)
+        ev_arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in stage_events])
+    _check(lib.moe_forward(ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride, _p(logits_out),
+                           _p(idx_out), _p(w_out), _p(workspace), workspace.numel(), _p(dev_status),
+                           ev_arr, n_ev, _s(stream)),
+           "moe_forward")
+    return y

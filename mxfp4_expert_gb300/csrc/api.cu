@@ -1,0 +1,261 @@
+// C-ABI entry points for the layer: argument and descriptor checks, workspace
+// carving, and the kernel sequence of one forward call.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "kernels.h"
+
+namespace moe {
+
+int current_device(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& c = cache[dev];
+  if (c.device != dev) {
+    DeviceInfo d;
+    d.device = dev;
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev));
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev));
+    int optin = 0;
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+    d.smem_optin = size_t(optin);
+    c = d;
+  }
+  if (c.major != 10 || c.minor != 3) return MOE_ERR_NO_DEVICE;
+  *out = c;
+  return MOE_OK;
+}
+
+namespace {
+
+// Workspace sections of one forward call (byte offsets from the base).
+struct Workspace {
+  size_t logits, idx, w, sort_ws, counts, offsets, perm, inv, active, n_active, status;
+  size_t x_b, x_e, h_sh, h, h_b, h_e, part, total;
+};
+
+Workspace plan(const moe_shape& sh, int T) {
+  Workspace o{};
+  const size_t d = size_t(sh.d_model), I = size_t(sh.d_ff), E = size_t(sh.n_experts),
+               k = size_t(sh.top_k), slots = size_t(T) * k;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t here = at;
+    at += round_up(bytes, 256);
+    return here;
+  };
+  o.logits = take(size_t(T) * E * 4);
+  o.idx = take(slots * 4);
+  o.w = take(slots * 4);
+  o.sort_ws = take(sort_workspace_bytes(T, int(E)));
+  o.counts = take(E * 4);
+  o.offsets = take((E + 1) * 4);
+  o.perm = take(slots * 4);
+  o.inv = take(slots * 4);
+  o.active = take(E * 4);
+  o.n_active = take(4);
+  o.status = take(4);
+  o.x_b = take(size_t(T) * (d / 32) * kActRowKbBytes);
+  o.x_e = take(size_t(T) * (d / 32) * 2);
+  o.h_sh = take(size_t(T) * I * 4);
+  o.h = take(slots * I * 4);
+  o.h_b = take(slots * (I / 32) * kActRowKbBytes);
+  o.h_e = take(slots * (I / 32) * 2);
+  o.part = take(slots * d * 4);
+  o.total = at;
+  return o;
+}
+
+int check_shape(const moe_shape* sh, int T) {
+  if (!sh) return MOE_ERR_INVALID_ARG;
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (sh->d_model < 32 || sh->d_ff < 32 || sh->n_experts < 1 || sh->top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (sh->d_model % 32 || sh->d_ff % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (sh->n_experts > 1024 || sh->top_k > 32 || sh->top_k > sh->n_experts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (sh->has_shared != 0 && sh->has_shared != 1) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool desc_matches(const moe_packed_desc& d, int layout, int n_mat, int N, int K) {
+  return d.magic == MOE_PACK_MAGIC && d.version == MOE_PACK_VERSION && d.layout == layout &&
+         d.n_mat == n_mat && d.N == N && d.K == K &&
+         d.bytes_per_mat == (uint64_t)N * K / 2 + (uint64_t)N * K / 32 &&
+         d.total_bytes == d.bytes_per_mat * (uint64_t)n_mat;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_workspace_bytes(const moe_shape* shape, int T) {
+  if (check_shape(shape, T) != MOE_OK) return 0;
+  return plan(*shape, T).total;
+}
+
+extern "C" int moe_query_path(const moe_shape* shape, int T) {
+  const int st = check_shape(shape, T);
+  if (st != MOE_OK) return st;
+  return MOE_PATH_DECODE_MMA;
+}
+
+extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                           const float* bias_dev, int bias_row_stride, float* logits_out,
+                           int32_t* idx_out, float* w_out, void* workspace_dev,
+                           size_t workspace_bytes, int* dev_status, void* const* stage_events,
+                           int n_stage_events, moe_stream_t stream) {
+  MOE_CHECK_ARG(L && x_dev && y_dev && workspace_dev, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(n_stage_events >= 0 && (stage_events || n_stage_events == 0), MOE_ERR_INVALID_ARG);
+  int st = check_shape(&L->shape, T);
+  if (st != MOE_OK) return st;
+  const moe_shape& sh = L->shape;
+  const int d = sh.d_model, I = sh.d_ff, E = sh.n_experts, k = sh.top_k;
+  MOE_CHECK_ARG(L->router_w && L->gate_up && L->down, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(!sh.has_shared || (L->shared_gate && L->shared_up && L->shared_down), MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(bias_row_stride == 0 || bias_row_stride >= E, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(x_dev != y_dev, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(desc_matches(L->gate_up_desc, MOE_LAYOUT_MMA16_GATEUP, E, 2 * I, d), MOE_ERR_BAD_DESCRIPTOR);
+  MOE_CHECK_ARG(desc_matches(L->down_desc, MOE_LAYOUT_MMA16, E, d, I), MOE_ERR_BAD_DESCRIPTOR);
+  MOE_CHECK_ARG(aligned(L->gate_up, 16) && aligned(L->down, 16) && aligned(L->router_w, 16) &&
+                    aligned(x_dev, 16) && aligned(workspace_dev, 256),
+                MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(!sh.has_shared || (aligned(L->shared_gate, 16) && aligned(L->shared_up, 16) &&
+                                   aligned(L->shared_down, 16)),
+                MOE_ERR_INVALID_ARG);
+  const Workspace ws = plan(sh, T);
+  MOE_CHECK_ARG(workspace_bytes >= ws.total, MOE_ERR_WORKSPACE_TOO_SMALL);
+  DeviceInfo di;
+  st = current_device(&di);
+  if (st != MOE_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  void* B = workspace_dev;
+  float* logits = logits_out ? logits_out : at<float>(B, ws.logits);
+  int32_t* idx = idx_out ? idx_out : at<int32_t>(B, ws.idx);
+  float* w = w_out ? w_out : at<float>(B, ws.w);
+  int* status = dev_status ? dev_status : at<int>(B, ws.status);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(x_dev);
+  // Under stream capture an event record must be an external node to be
+  // timed on replay; outside capture the flag records as usual.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (n_stage_events > 0) MOE_CUDA_TRY(cudaStreamIsCapturing(s, &cap));
+  const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  int mark_i = 0;
+  auto mark = [&]() -> int {
+    if (mark_i < n_stage_events && stage_events[mark_i]) {
+      if (cudaEventRecordWithFlags((cudaEvent_t)stage_events[mark_i], s, ev_flags) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+    }
+    ++mark_i;
+    return MOE_OK;
+  };
+  if ((st = mark())) return st;
+
+  // 1. activations -> e4m3 B-operand terms
+  if ((st = launch_act_split(x, true, T, d, at<uint8_t>(B, ws.x_b), at<int16_t>(B, ws.x_e), di, s))) return st;
+  if ((st = mark())) return st;
+  // 2. router logits and shared gate/up (routing-independent)
+  FrontArgs fa{x, T, d, E, I, static_cast<const __nv_bfloat16*>(L->router_w),
+               sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_gate) : nullptr,
+               sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_up) : nullptr, logits,
+               at<float>(B, ws.h_sh)};
+  if ((st = launch_front(fa, di, s))) return st;
+  if ((st = mark())) return st;
+  // 3. top-k + weights, 4. sort by expert
+  if ((st = launch_topk(logits, T, E, k, bias_dev, bias_row_stride, idx, w, s))) return st;
+  if ((st = mark())) return st;
+  int32_t* offsets = at<int32_t>(B, ws.offsets);
+  int32_t* perm = at<int32_t>(B, ws.perm);
+  int32_t* inv = at<int32_t>(B, ws.inv);
+  int32_t* active = at<int32_t>(B, ws.active);
+  int32_t* n_active = at<int32_t>(B, ws.n_active);
+  if ((st = launch_sort(idx, T, k, E, at<int32_t>(B, ws.counts), offsets, perm, inv, active, n_active,
+                        at<void>(B, ws.sort_ws), status, s)))
+    return st;
+  if ((st = mark())) return st;
+  const int max_active = T * k < E ? T * k : E;
+  // 5. routed gate/up + SwiGLU -> h [slots][I]
+  RoutedArgs ra{};
+  ra.w = static_cast<const uint8_t*>(L->gate_up);
+  ra.mat_bytes = L->gate_up_desc.bytes_per_mat;
+  ra.n_tiles = 2 * I / kTileRows;
+  ra.KB = d / kMxBlock;
+  ra.active = active;
+  ra.n_active = n_active;
+  ra.offsets = offsets;
+  ra.perm = perm;
+  ra.k = k;
+  ra.act_b = at<uint8_t>(B, ws.x_b);
+  ra.act_e = at<int16_t>(B, ws.x_e);
+  ra.act_by_token = 1;
+  ra.max_items = max_active * ra.n_tiles;
+  ra.out = at<float>(B, ws.h);
+  ra.out_ld = I;
+  ra.status = status;
+  if ((st = launch_routed(kModeGateUp, ra, di, s))) return st;
+  if ((st = mark())) return st;
+  // 6. h -> e4m3 terms
+  const int slots = T * k;
+  if ((st = launch_act_split(at<float>(B, ws.h), false, slots, I, at<uint8_t>(B, ws.h_b),
+                             at<int16_t>(B, ws.h_e), di, s)))
+    return st;
+  if ((st = mark())) return st;
+  // 7. routed down -> part [slots][d]
+  RoutedArgs rd = ra;
+  rd.w = static_cast<const uint8_t*>(L->down);
+  rd.mat_bytes = L->down_desc.bytes_per_mat;
+  rd.n_tiles = d / kTileRows;
+  rd.KB = I / kMxBlock;
+  rd.act_b = at<uint8_t>(B, ws.h_b);
+  rd.act_e = at<int16_t>(B, ws.h_e);
+  rd.act_by_token = 0;
+  rd.max_items = max_active * rd.n_tiles;
+  rd.out = at<float>(B, ws.part);
+  rd.out_ld = d;
+  if ((st = launch_routed(kModeDown, rd, di, s))) return st;
+  if ((st = mark())) return st;
+  // 8. shared down + weighted combine -> y bf16
+  CombineArgs ca{T, d, I, k,
+                 sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_down) : nullptr,
+                 at<float>(B, ws.h_sh), w, inv, at<float>(B, ws.part),
+                 static_cast<__nv_bfloat16*>(y_dev)};
+  if ((st = launch_combine(ca, di, s))) return st;
+  return mark();
+}
+
+extern "C" const char* moe_stage_names(int path) {
+  if (path == MOE_PATH_DECODE_MMA)
+    return "act_split_x,router_shared_gateup,topk,sort,routed_gateup,act_split_h,routed_down,combine";
+  return nullptr;
+}
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_BAD_DESCRIPTOR: return "packed-weight descriptor does not match";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* moe_version(void) { return "moe_mxfp4 1.0 sm_103a"; }

@@ -1,0 +1,140 @@
+// Shared device helpers for the sm_103a MXFP4 MoE kernels: inline-PTX wrappers
+// (mbarrier, 1-D bulk copies, e4m3 warp MMA, fp8 conversions), bounded waits,
+// and the constants of the packed weight format (see include/moe_mxfp4.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_mxfp4.h"
+
+namespace moe {
+
+constexpr int kMxBlock = 32;        // elements per E8M0 scale (OCP MX)
+constexpr int kTileRows = 16;       // rows per packed tile = MMA M
+constexpr int kUnitCodeBytes = 256; // 16 rows x 32 codes x 4 bits
+constexpr int kUnitBytes = 272;     // codes + 16 scale bytes
+constexpr int kActTerms = 4;        // B-operand columns per activation row
+constexpr int kActRowKbBytes = 128; // 4 terms x 32 e4m3 bytes per (row, K-block)
+constexpr int16_t kActZeroExp = -32768;  // marks an all-zero activation block
+
+// Spin budget for any wait on another agent (clock64 cycles, ~1 s at 2 GHz).
+constexpr long long kSpinBudget = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: returns false (and sets MOE_DEV_TIMEOUT) if the phase never
+// completes within kSpinBudget cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kSpinBudget) {
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---- loads ----------------------------------------------------------------
+__device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_nc_stream_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// ---- e4m3 warp MMA: D[16x8] = A[16x32] * B[32x8], fp32 accumulate from 0 ----
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Packed code word -> two e4m3x4 registers (each byte = 2^-6 * E2M1 value).
+// Row-g codes sit at bits {2,3,4,7} of every byte, row-(g+8) codes at
+// {0,1,6,5} (m, e0, e1, sign); see the layout in moe_mxfp4.h.
+__device__ __forceinline__ uint32_t decode_rowlo(uint32_t w) { return w & 0x9C9C9C9Cu; }
+__device__ __forceinline__ uint32_t decode_rowhi(uint32_t w) {
+  return ((w << 2) & 0x8C8C8C8Cu) | ((w >> 2) & 0x10101010u);
+}
+
+// fp32 pair -> e4m3x2 (round to nearest even, saturating to +-448); low byte = lo.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Exact e4m3 -> fp32 (finite codes).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+  float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : float(m) * 0.001953125f;
+  return (c & 0x80u) ? -mag : mag;
+}
+
+// 2^ex as fp32 for an unbiased exponent, including the subnormal/overflow ends.
+__device__ __forceinline__ float exp2i(int ex) {
+  int f = ex + 127;
+  if (f >= 1 && f <= 254) return __uint_as_float(uint32_t(f) << 23);
+  return ldexpf(1.0f, ex);
+}
+
+// Combined factor of one (weight row, K-block) x (activation row, K-block):
+// weights were decoded as 2^-6 * value, activations stored as value * 2^-e.
+// factor = 2^(s - 127) * 2^6 * 2^e.
+__device__ __forceinline__ float block_factor(uint32_t s, int e) {
+  if (e == kActZeroExp) return 0.0f;
+  return exp2i(int(s) - 121 + e);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace moe

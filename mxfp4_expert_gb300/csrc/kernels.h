@@ -1,0 +1,72 @@
+// Launchers shared between the translation units of libmoe_mxfp4.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "host_util.h"
+
+namespace moe {
+
+// route.cu
+int launch_topk(const float* logits, int T, int E, int k, const float* bias, int bias_stride,
+                int32_t* idx, float* w, cudaStream_t s);
+size_t sort_workspace_bytes(int T, int E);
+int launch_sort(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* ws,
+                int* status, cudaStream_t s);
+
+// experts.cu
+// Activation rows [rows][K] (bf16 if src_bf16, else fp32) -> B-operand terms
+// act_b [rows][K/32][128] and block exponents act_e [rows][K/32].
+int launch_act_split(const void* src, bool src_bf16, int rows, int K, uint8_t* act_b,
+                     int16_t* act_e, const DeviceInfo& di, cudaStream_t s);
+
+enum RoutedMode { kModeGateUp = 0, kModeDown = 1 };
+
+struct RoutedArgs {
+  const uint8_t* w;         // packed matrices, expert e at w + e * mat_bytes
+  uint64_t mat_bytes;
+  int n_tiles;              // N / 16
+  int KB;                   // K / 32
+  const int32_t* active;    // [E] active experts (ascending)
+  const int32_t* n_active;  // [1]
+  const int32_t* offsets;   // [E+1] sorted-slot offsets per expert
+  const int32_t* perm;      // sorted slot -> p = t*k + j
+  int k;
+  const uint8_t* act_b;     // B-operand rows
+  const int16_t* act_e;
+  int act_by_token;         // 1: activation row = perm[slot] / k; 0: = slot
+  int max_items;            // upper bound on n_active * n_tiles (grid sizing)
+  float* out;               // gate/up: h [slots][N/2]; down: part [slots][N]
+  int out_ld;
+  int* status;
+};
+int launch_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+// dense.cu
+struct FrontArgs {
+  const __nv_bfloat16* x;   // [T][d]
+  int T, d, E, I;
+  const __nv_bfloat16* router_w;   // [E][d]
+  const __nv_bfloat16* sh_gate;    // [I][d] or null
+  const __nv_bfloat16* sh_up;      // [I][d]
+  float* logits;                   // [T][E]
+  float* h_sh;                     // [T][I]
+};
+int launch_front(const FrontArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+struct CombineArgs {
+  int T, d, I, k;
+  const __nv_bfloat16* sh_down;    // [d][I] or null
+  const float* h_sh;               // [T][I]
+  const float* w;                  // [T][k]
+  const int32_t* inv;              // [T*k] p -> sorted slot
+  const float* part;               // [slots][d]
+  __nv_bfloat16* y;                // [T][d]
+};
+int launch_combine(const CombineArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,177 @@
+"""moe_forward on the GPU vs. the fp64 oracle.
+
+Per call: (1) the GPU's router logits are within 1e-5 * sum_j |x_j Wr_j| of
+the oracle's fp64 logits; (2) the GPU's indices equal the oracle's ranking of
+the GPU's own fp32 logits (plus bias) and the weights agree to 2e-6;
+(3) y (bf16) against the oracle's fp64 layer output computed with those
+indices: relative L2 <= 5e-3 and max |err| <= 2e-2 * rms(y_ref).
+Full-size workloads are checked on every token where the oracle is cheap
+(T = 1, 4) and on sampled tokens otherwise (T = 64, 4096).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import moe as omoe
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+MAX_ABS = 2e-2
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import mxfp4_expert_gb300 as mx
+    return mx
+
+
+def run(mx, layer, x, bias, T, E, k):
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = mx.moe_forward(layer, x, bias, logits_out=logits, idx_out=idx, w_out=w, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return y, logits, idx, w
+
+
+def check_layer(w, set_idx, layer, x, bias, out, tokens=None, device="cuda"):
+    y, logits, idx, wts = out
+    tokens = list(range(w.T)) if tokens is None else list(tokens)
+    xs = x[tokens].cpu()
+    router = wl.gen_router(w, set_idx, device).cpu()
+    gl = logits.cpu().numpy()[tokens]
+    gi = idx.cpu().numpy()[tokens]
+    b = None
+    if bias is not None:
+        b = bias.cpu().numpy()
+        if b.ndim == 2:
+            b = b[tokens]
+    # (1) logits
+    ref_l = omoe.router_logits(xs, router)
+    bound = 1e-5 * (np.abs(omoe.as_f64(xs)) @ np.abs(omoe.as_f64(router)).T)
+    assert np.all(np.abs(gl - ref_l) <= bound + 1e-30)
+    # (2) routing from the GPU's own fp32 logits
+    ri, rw, _ = omoe.route_topk(gl, w.k, b)
+    assert np.array_equal(gi, ri)
+    assert np.all(np.abs(wts.cpu().numpy()[tokens] - rw) <= 2e-6)
+    # (3) y with the oracle's expert values at those indices
+    needed = sorted(set(gi.ravel().tolist()))
+    experts = {}
+    for e in needed:
+        gu, dn = wl.gen_expert(w, set_idx, e, device)
+        experts[e] = omoe.Expert.from_fp32(gu.cpu().numpy(), dn.cpu().numpy())
+    shared = tuple(t.cpu() for t in wl.gen_shared(w, set_idx, device))
+    ref = omoe.moe_layer(xs, router, experts, shared, w.k, bias=b, idx=gi)
+    yg = y.float().cpu().numpy().astype(np.float64)[tokens]
+    yr = ref["y"]
+    rel = np.linalg.norm(yg - yr) / np.linalg.norm(yr)
+    rms = np.sqrt(np.mean(yr ** 2))
+    mabs = np.max(np.abs(yg - yr))
+    assert rel <= REL_L2, rel
+    assert mabs <= MAX_ABS * rms, (mabs, rms)
+    return rel, mabs / rms
+
+
+def build(mx, w, set_idx=0):
+    from mxfp4_expert_gb300 import synthetic
+    layer = synthetic.build_layer(w, set_idx)
+    x, bias = synthetic.inputs(w, set_idx)
+    return layer, x, bias
+
+
+@pytest.mark.parametrize("name,T,d,I,E,k,routing", [
+    ("tiny", 1, 512, 128, 32, 4, "natural"),
+    ("ragged", 5, 256, 64, 16, 3, "natural"),
+    ("ragged", 17, 512, 96, 24, 5, "natural"),
+    ("onehot", 3, 64, 32, 1, 1, "natural"),
+    ("wide_k", 2, 128, 32, 40, 32, "natural"),
+])
+def test_small_layers(mx, name, T, d, I, E, k, routing):
+    w = wl.Workload(name, T=T, d=d, I=I, E=E, k=k, sets=1, routing=routing, seed=3)
+    layer, x, bias = build(mx, w)
+    out = run(mx, layer, x, bias, w.T, w.E, w.k)
+    check_layer(w, 0, layer, x, bias, out)
+
+
+def test_no_shared_expert(mx):
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.Workload("noshared", T=4, d=256, I=64, E=16, k=2, sets=1, routing="natural", seed=5)
+    full = synthetic.build_layer(w, 0)
+    layer = mx.Layer(full.router_w, full.gate_up, full.struct.gate_up_desc, full.down,
+                     full.struct.down_desc, top_k=w.k)
+    x, _ = synthetic.inputs(w, 0)
+    y, logits, idx, wts = run(mx, layer, x, None, w.T, w.E, w.k)
+    gi = idx.cpu().numpy()
+    experts = {e: omoe.Expert.from_fp32(*(t.cpu().numpy() for t in wl.gen_expert(w, 0, e, "cuda")))
+               for e in set(gi.ravel().tolist())}
+    ref = omoe.moe_layer(x.cpu(), full.router_w.cpu(), experts, None, w.k, idx=gi)
+    yg = y.float().cpu().numpy()
+    assert np.linalg.norm(yg - ref["y"]) / np.linalg.norm(ref["y"]) <= REL_L2
+
+
+def test_ling_t1(mx):
+    w = wl.get("ling_t1")
+    for s in (0, 1):
+        layer, x, bias = build(mx, w, s)
+        out = run(mx, layer, x, bias, w.T, w.E, w.k)
+        check_layer(w, s, layer, x, bias, out)
+        del layer
+        torch.cuda.empty_cache()
+
+
+def test_mtp_t4(mx):
+    w = wl.get("mtp_t4")
+    for s in (0, 5):
+        layer, x, bias = build(mx, w, s)
+        out = run(mx, layer, x, bias, w.T, w.E, w.k)
+        D, sets = wl.mtp_expert_sets(w, s)
+        assert len(set(out[2].cpu().numpy().ravel().tolist())) == D
+        check_layer(w, s, layer, x, bias, out)
+        del layer
+        torch.cuda.empty_cache()
+
+
+def test_zipf_t64_sampled(mx):
+    w = wl.get("zipf_t64")
+    layer, x, bias = build(mx, w, 0)
+    out = run(mx, layer, x, bias, w.T, w.E, w.k)
+    D = len(set(out[2].cpu().numpy().ravel().tolist()))
+    assert 100 <= D <= 220
+    check_layer(w, 0, layer, x, bias, out, tokens=[0, 17, 40, 63])
+
+
+@pytest.mark.slow
+def test_prefill_t4096_sampled(mx):
+    w = wl.get("prefill_t4096")
+    layer, x, bias = build(mx, w, 0)
+    out = run(mx, layer, x, bias, w.T, w.E, w.k)
+    check_layer(w, 0, layer, x, bias, out, tokens=[0, 1, 2047, 4095])
+
+
+def test_deterministic(mx):
+    w = wl.get("mtp_t4")
+    layer, x, bias = build(mx, w, 2)
+    y1 = run(mx, layer, x, bias, w.T, w.E, w.k)[0].clone()
+    y2 = run(mx, layer, x, bias, w.T, w.E, w.k)[0]
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_forward_rejects_bad_inputs(mx):
+    w = wl.get("tiny")
+    layer, x, bias = build(mx, w)
+    bad = mx.Layer(layer.router_w, layer.gate_up, layer.struct.down_desc, layer.down, layer.struct.down_desc,
+                   *layer.shared, top_k=w.k)
+    with pytest.raises(mx.MoeError) as e:
+        mx.moe_forward(bad, x)
+    assert e.value.status == -3
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.MoeError) as e:
+        mx.moe_forward(layer, x, workspace=small)
+    assert e.value.status == -4
+    with pytest.raises(mx.MoeError) as e:
+        mx.moe_forward(layer, x, y=x)
+    assert e.value.status == -1
