@@ -99,22 +99,18 @@ def round_to_e2m1(q: np.ndarray) -> np.ndarray:
     """Nearest E2M1 code for fp64 values q: ties to the even mantissa, saturating.
 
     The sign bit of q is kept (so small negatives give code 8, i.e. -0).
-    Written as the definition: distance to each of the 8 magnitudes, the
-    smallest wins, and on a tie the code with mantissa bit 0 wins. Magnitudes
+    Written as the definition: among the two grid magnitudes around |q| the
+    nearer wins, and on a tie the code with mantissa bit 0 wins. Magnitudes
     above 6 saturate to 6 (spec: conversion to E2M1 saturates).
     """
     q = np.asarray(q, dtype=np.float64)
-    a = np.abs(q)
-    dist = np.abs(a[..., None] - E2M1_MAGNITUDE)          # [..., 8]
-    best = np.min(dist, axis=-1, keepdims=True)
-    tied = dist == best
-    # among the tied (at most two, adjacent) prefer the even code
-    even = (np.arange(8) & 1) == 0
-    pick_even = tied & even
-    has_even = pick_even.any(axis=-1, keepdims=True)
-    cand = np.where(has_even, pick_even, tied)
-    mag = np.argmax(cand, axis=-1)
-    mag = np.where(a > 6.0, 7, mag)
+    a = np.minimum(np.abs(q), 6.0)
+    hi = np.clip(np.searchsorted(E2M1_MAGNITUDE, a), 1, 7)   # first magnitude >= a
+    lo = hi - 1
+    d_lo = a - E2M1_MAGNITUDE[lo]
+    d_hi = E2M1_MAGNITUDE[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((hi & 1) == 0))
+    mag = np.where(pick_hi, hi, lo)
     sign = np.signbit(q).astype(np.int64) << 3
     return (mag | sign).astype(np.uint8)
 
