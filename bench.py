@@ -157,6 +157,7 @@ def stage_bytes(w, stage, D, slots):
         "router_shared_gateup": E * d * 2 + 2 * I * d * 2 + T * d * 2 + T * (E + I) * 4,
         "topk": T * E * 4 + T * w.k * 8,
         "sort": T * w.k * 4 * 4,
+        "decode_fused": wl.weight_bytes(w, D) + T * d * 4,
         "routed_gateup": D * per_gu + slots * I * 4,
         "act_split_h": slots * I * 4 + slots * (I // 32) * 130,
         "routed_down": D * per_dn + slots * d * 4,
@@ -301,7 +302,7 @@ def run_ours(args, w):
         biases.append(b)
     ys = [torch.empty_like(x) for x in xs]
     wsb = mx.moe_workspace_bytes(base.shape, w.T)
-    work = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(n_sets)]
+    work = [torch.zeros(wsb, dtype=torch.uint8, device=dev) for _ in range(n_sets)]
     idxs = [torch.empty((w.T, w.k), dtype=torch.int32, device=dev) for _ in range(n_sets)]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     path = mx.moe_query_path(base.shape, w.T)
@@ -374,6 +375,7 @@ def run_ours(args, w):
     peak, peak_kind = measured_peaks()
     achieved = dom_bytes / (stage_mean[dom] * 1e-6) / 1e9
     kernel_src = os.path.join(ROOT, "mxfp4_expert_gb300", "csrc",
+                              "decode.cu" if dom == "decode_fused" else
                               "experts.cu" if dom.startswith("routed") else "dense.cu")
     traffic = profiled_traffic(kernel_src, dom)
     algo_bytes = float(np.mean([weight_bytes_per_call(w, D) for D in D_sets]))
@@ -403,7 +405,7 @@ def run_ours(args, w):
         e2e = {"value": ms2 * 1e3 / (calls * ws), "unit": "us/layer",
                "h2d_bytes_per_step": n_sets * w.T * w.d * 2, "d2h_bytes_per_step": n_sets * w.T * w.d * 2}
 
-    launches_per_call = {"act_split_x": 1, "router_shared_gateup": 1, "topk": 1, "sort": 3,
+    launches_per_call = {"decode_fused": 1, "act_split_x": 1, "router_shared_gateup": 1, "topk": 1, "sort": 3,
                          "routed_gateup": 1, "act_split_h": 1, "routed_down": 1, "combine": 1}
     per_call = sum(launches_per_call.get(n, 1) for n in stages)
 

@@ -130,8 +130,11 @@ typedef struct moe_layer {
 
 /* Kernel paths moe_forward can take (moe_query_path). */
 typedef enum moe_path {
-  MOE_PATH_DECODE_MMA = 1   /* per-stage kernels: router GEMV, top-k + sort,
-                               MXFP4 expert GEMVs on e4m3 mma.sync, combine */
+  MOE_PATH_DECODE_MMA = 1,   /* per-stage kernels: router GEMV, top-k + sort,
+                                MXFP4 expert GEMVs on e4m3 mma.sync, combine */
+  MOE_PATH_DECODE_FUSED = 2  /* T <= 4: one cooperative persistent kernel per
+                                call (router, top-k, shared and routed experts,
+                                combine), one CTA per SM */
 } moe_path;
 
 /* ---- packing ------------------------------------------------------------ */
@@ -199,11 +202,16 @@ int moe_sort_by_expert(const int32_t* idx_dev, int T, int k, int E,
 
 /* ---- the layer ---------------------------------------------------------- */
 
-/* Device workspace moe_forward needs for T tokens (256-B aligned base). */
+/* Device workspace moe_forward needs for T tokens (256-B aligned base).
+ * The first bytes hold synchronisation counters that carry over from one call
+ * to the next: zero-fill a workspace once before its first moe_forward, and
+ * do not share one workspace between calls that may run concurrently. After
+ * a call that reported MOE_DEV_TIMEOUT, zero it again. */
 size_t moe_workspace_bytes(const moe_shape* shape, int T);
 
-/* Which moe_path moe_forward takes for this shape and T; negative status if
- * unsupported. */
+/* Which moe_path moe_forward takes for this shape and T on the current
+ * device; negative status if unsupported (MOE_ERR_NO_DEVICE without an
+ * sm_103 device, since the choice depends on its SM count and shared memory). */
 int moe_query_path(const moe_shape* shape, int T);
 
 /* The layer over T tokens.
@@ -212,7 +220,8 @@ int moe_query_path(const moe_shape* shape, int T);
  *   bias_dev      fp32 router bias as in moe_route_topk (NULL: none)
  *   logits_out    fp32 [T][E] router logits before bias (NULL: not returned)
  *   idx_out       int32 [T][k]; w_out fp32 [T][k] (NULL: not returned)
- *   workspace_dev >= moe_workspace_bytes(&L->shape, T) bytes
+ *   workspace_dev >= moe_workspace_bytes(&L->shape, T) bytes, zero-filled
+ *                 before its first use (see moe_workspace_bytes)
  *   dev_status    device int (may be NULL)
  *   stage_events  NULL, or n_stage_events cudaEvent_t handles (host array,
  *                 caller-created): event 0 is recorded on `stream` before the
@@ -230,6 +239,14 @@ int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
 /* Comma-separated names of the stages of `path` in launch order (the
  * boundaries moe_forward's stage_events mark); NULL for an unknown path. */
 const char* moe_stage_names(int path);
+
+/* Failure-detection self-test: one GPU thread waits for *flag_dev == want with
+ * the bounded spin the kernels use for every cross-CTA wait (acquire loads,
+ * clock64 budget of budget_cycles, at most the kernels' own budget). If the
+ * flag never takes that value, MOE_DEV_TIMEOUT is OR-ed into *dev_status and
+ * the kernel returns; nothing hangs or faults. flag_dev: device uint32. */
+int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want, long long budget_cycles,
+                              int* dev_status, moe_stream_t stream);
 
 /* Static text for a moe_status value. */
 const char* moe_status_string(int status);

@@ -15,11 +15,11 @@ import torch
 
 __all__ = [
     "MoeError", "LIB_PATH", "lib", "MOE_LAYOUT_MMA16", "MOE_LAYOUT_MMA16_GATEUP",
-    "MOE_PATH_DECODE_MMA", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
+    "MOE_PATH_DECODE_MMA", "MOE_PATH_DECODE_FUSED", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
-    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_status_string", "moe_version",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp4.so")
@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp
 MOE_LAYOUT_MMA16 = 1
 MOE_LAYOUT_MMA16_GATEUP = 2
 MOE_PATH_DECODE_MMA = 1
+MOE_PATH_DECODE_FUSED = 2
 DEV_NONFINITE_INPUT, DEV_SCALE_RANGE, DEV_INDEX_OOB, DEV_TIMEOUT = 1, 2, 4, 8
 
 
@@ -75,6 +76,7 @@ def _load():
         "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
                                 ctypes.POINTER(ctypes.c_void_p), i32, vp]),
         "moe_stage_names": (ctypes.c_char_p, [i32]),
+        "moe_selftest_bounded_wait": (i32, [vp, ctypes.c_uint32, ctypes.c_longlong, vp, vp]),
         "moe_status_string": (ctypes.c_char_p, [i32]),
         "moe_version": (ctypes.c_char_p, []),
     }
@@ -109,6 +111,13 @@ def _cuda(t, dtype, name):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def moe_selftest_bounded_wait(flag: torch.Tensor, want: int, budget_cycles: int,
+                              dev_status: torch.Tensor, stream=None):
+    """Run the kernels' bounded wait on flag (uint32 as int32 tensor) == want."""
+    _check(lib.moe_selftest_bounded_wait(_p(flag), want, budget_cycles, _p(dev_status), _s(stream)),
+           "moe_selftest_bounded_wait")
 
 
 def moe_status_string(status: int) -> str:
@@ -254,6 +263,10 @@ def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
                 stage_events=None, stream=None):
     """y = layer(x) for bf16 x [T, d]; returns y (bf16 [T, d]).
 
+    workspace: uint8 device tensor of layer.workspace_bytes(T) bytes, zero-filled
+    before its first use (it carries synchronisation counters between calls);
+    allocated with zeros when omitted.
+
     stage_events: optional list of torch.cuda.Event (enable_timing=True); see
     moe_stage_names for what each boundary marks.
     """
@@ -266,7 +279,7 @@ def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
-        workspace = torch.empty(layer.workspace_bytes(T), dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(layer.workspace_bytes(T), dtype=torch.uint8, device=x.device)
     ev_arr, n_ev = None, 0
     if stage_events:
         n_ev = len(stage_events)

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode.h"
 #include "host_util.h"
 #include "kernels.h"
 
@@ -38,7 +39,7 @@ namespace {
 
 // Workspace sections of one forward call (byte offsets from the base).
 struct Workspace {
-  size_t logits, idx, w, sort_ws, counts, offsets, perm, inv, active, n_active, status;
+  size_t state, logits, idx, w, sort_ws, counts, offsets, perm, inv, active, n_active, status;
   size_t x_b, x_e, h_sh, h, h_b, h_e, part, total;
 };
 
@@ -52,6 +53,7 @@ Workspace plan(const moe_shape& sh, int T) {
     at += round_up(bytes, 256);
     return here;
   };
+  o.state = take(decode_state_bytes(int(E), int(I)));   // persists across calls
   o.logits = take(size_t(T) * E * 4);
   o.idx = take(slots * 4);
   o.w = take(slots * 4);
@@ -106,10 +108,28 @@ extern "C" size_t moe_workspace_bytes(const moe_shape* shape, int T) {
   return plan(*shape, T).total;
 }
 
+// Path for (shape, T) on the current device: the single-launch decode kernel
+// when T <= 4 and the shape fits it, else the per-stage kernels.
+static int select_path(const moe_shape& sh, int T, const DeviceInfo& di) {
+  DecodeArgs probe{};
+  probe.T = T;
+  probe.d = sh.d_model;
+  probe.I = sh.d_ff;
+  probe.E = sh.n_experts;
+  probe.k = sh.top_k;
+  int stages;
+  uint32_t slot, smem;
+  if (T <= kDecodeMaxT && decode_plan(probe, di, &stages, &slot, &smem) == MOE_OK) return MOE_PATH_DECODE_FUSED;
+  return MOE_PATH_DECODE_MMA;
+}
+
 extern "C" int moe_query_path(const moe_shape* shape, int T) {
   const int st = check_shape(shape, T);
   if (st != MOE_OK) return st;
-  return MOE_PATH_DECODE_MMA;
+  DeviceInfo di;
+  const int dst = current_device(&di);
+  if (dst != MOE_OK) return dst;
+  return select_path(*shape, T, di);
 }
 
 extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
@@ -165,6 +185,40 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
     return MOE_OK;
   };
   if ((st = mark())) return st;
+
+  if (select_path(sh, T, di) == MOE_PATH_DECODE_FUSED) {
+    DecodeArgs da{};
+    da.T = T;
+    da.d = d;
+    da.I = I;
+    da.E = E;
+    da.k = k;
+    da.has_shared = sh.has_shared;
+    da.x = x;
+    da.router_w = static_cast<const __nv_bfloat16*>(L->router_w);
+    da.sh_gate = sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_gate) : nullptr;
+    da.sh_up = sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_up) : nullptr;
+    da.sh_down = sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_down) : nullptr;
+    da.gate_up = static_cast<const uint8_t*>(L->gate_up);
+    da.down = static_cast<const uint8_t*>(L->down);
+    da.gu_mat = L->gate_up_desc.bytes_per_mat;
+    da.dn_mat = L->down_desc.bytes_per_mat;
+    da.bias = bias_dev;
+    da.bias_stride = bias_row_stride;
+    da.logits = logits;
+    da.idx_out = idx_out;
+    da.w_out = w_out;
+    da.y = static_cast<__nv_bfloat16*>(y_dev);
+    da.state = at<DecodeState>(B, ws.state);
+    da.state_words = at<uint32_t>(B, ws.state);
+    da.h = at<float>(B, ws.h);
+    da.hB = at<uint8_t>(B, ws.h_b);
+    da.hE = at<int16_t>(B, ws.h_e);
+    da.h_sh = at<float>(B, ws.h_sh);
+    da.status = status;
+    if ((st = launch_decode(da, di, s))) return st;
+    return mark();
+  }
 
   // 1. activations -> e4m3 B-operand terms
   if ((st = launch_act_split(x, true, T, d, at<uint8_t>(B, ws.x_b), at<int16_t>(B, ws.x_e), di, s))) return st;
@@ -239,6 +293,7 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
 }
 
 extern "C" const char* moe_stage_names(int path) {
+  if (path == MOE_PATH_DECODE_FUSED) return "decode_fused";
   if (path == MOE_PATH_DECODE_MMA)
     return "act_split_x,router_shared_gateup,topk,sort,routed_gateup,act_split_h,routed_down,combine";
   return nullptr;
@@ -259,3 +314,24 @@ extern "C" const char* moe_status_string(int status) {
 }
 
 extern "C" const char* moe_version(void) { return "moe_mxfp4 1.0 sm_103a"; }
+
+namespace moe {
+namespace {
+// One thread waits, with the same bounded helper the decode kernel uses, for
+// *flag == want; on expiry MOE_DEV_TIMEOUT is set and the kernel returns.
+__global__ void wait_selftest_kernel(const uint32_t* flag, uint32_t want, long long budget, int* status) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) wait_eq_u32(flag, want, status, budget);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want, long long budget_cycles,
+                                         int* dev_status, moe_stream_t stream) {
+  MOE_CHECK_ARG(flag_dev && dev_status, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(budget_cycles > 0 && budget_cycles <= kSpinBudget, MOE_ERR_INVALID_ARG);
+  DeviceInfo di;
+  int st = current_device(&di);
+  if (st != MOE_OK) return st;
+  wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag_dev, want, budget_cycles, dev_status);
+  return launch_status();
+}

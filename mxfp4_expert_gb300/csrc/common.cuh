@@ -137,4 +137,63 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// ---- acquire/release accesses and bounded waits on global flags ----------
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint2 ld_cg_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// Bounded spins (acquire). Return false on timeout.
+__device__ __forceinline__ bool wait_geq_u64(const unsigned long long* p, unsigned long long target, int* status) {
+  if (ld_acquire_u64(p) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_u64(p) < target) {
+    if (clock64() - t0 > kSpinBudget) {
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+__device__ __forceinline__ bool wait_geq_u32(const uint32_t* p, uint32_t target, int* status) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_u32(p) < target) {
+    if (clock64() - t0 > kSpinBudget) {
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+__device__ __forceinline__ bool wait_eq_u32(const uint32_t* p, uint32_t want, int* status,
+                                            long long budget = kSpinBudget) {
+  if (ld_acquire_u32(p) == want) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_u32(p) != want) {
+    if (clock64() - t0 > budget) {
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 }  // namespace moe

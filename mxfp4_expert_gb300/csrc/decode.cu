@@ -1,0 +1,608 @@
+// Single-launch decode path (T <= 4 tokens): one cooperative persistent kernel,
+// one CTA per SM, so a layer call is a single launch with no host round trips
+// and no idle HBM between stages.
+//
+// Every CTA walks a private sequence of "loads". Each load fills one slot of a
+// shared-memory ring through 1-D bulk copies, and the CTA consumes the loads in
+// order:
+//
+//   R   its slice of router rows             -> logits (global)     phase A
+//   F   its slice of shared gate/up rows     -> h_sh (global)       phase A
+//   SD  shared-down rows of its output tiles -> y accumulators      needs all h_sh
+//   GU  its share of the routed gate/up tiles -> h (global)         needs routing
+//   DN  routed-down units of its output tiles -> y accumulators     needs h blocks
+//
+// R, F and SD do not depend on routing and are requested at kernel start, so
+// HBM is busy from the first cycle. After its R loads a CTA arrives at a
+// counter barrier; it computes its F loads while the other CTAs catch up, then
+// waits, reads all logits and runs the top-k itself (every CTA derives the
+// same routing, so no second exchange is needed). Phase-B loads are requested
+// next. Gate/up tiles publish h per 32-feature block: the last of the four
+// tiles of a block (an atomic counter) splits it into e4m3 terms and sets a
+// ready flag holding the call's epoch; down units wait on those flags. Each
+// CTA owns whole output rows (16-row tiles), so y is written without a
+// cross-CTA reduction. Gate/up tiles are handed out so that every CTA moves
+// about the same number of bytes in phase B, counting its down units.
+//
+// Cross-call state (barrier/epoch counters, per-block counters and flags)
+// lives at the start of the workspace and must be zero before the first call.
+// Counters are reset by the last CTA of a call or compared modulo their
+// per-call increment. Every wait is bounded (kSpinBudget); on timeout the
+// kernel sets MOE_DEV_TIMEOUT and carries on.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "decode.h"
+#include "host_util.h"
+#include "mma_tile.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
+
+// sum over 8 bf16 weights times 8 bf16 activations (both as uint4)
+__device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
+  float s = bf16_lo(w.x) * bf16_lo(x.x);
+  s = fmaf(bf16_hi(w.x), bf16_hi(x.x), s);
+  s = fmaf(bf16_lo(w.y), bf16_lo(x.y), s);
+  s = fmaf(bf16_hi(w.y), bf16_hi(x.y), s);
+  s = fmaf(bf16_lo(w.z), bf16_lo(x.z), s);
+  s = fmaf(bf16_hi(w.z), bf16_hi(x.z), s);
+  s = fmaf(bf16_lo(w.w), bf16_lo(x.w), s);
+  s = fmaf(bf16_hi(w.w), bf16_hi(x.w), s);
+  return s;
+}
+// sum over 8 bf16 weights times 8 fp32 values
+__device__ __forceinline__ float dot8_f32(uint4 w, const float* h) {
+  const float4 a = *reinterpret_cast<const float4*>(h);
+  const float4 b = *reinterpret_cast<const float4*>(h + 4);
+  float s = bf16_lo(w.x) * a.x;
+  s = fmaf(bf16_hi(w.x), a.y, s);
+  s = fmaf(bf16_lo(w.y), a.z, s);
+  s = fmaf(bf16_hi(w.y), a.w, s);
+  s = fmaf(bf16_lo(w.z), b.x, s);
+  s = fmaf(bf16_hi(w.z), b.y, s);
+  s = fmaf(bf16_lo(w.w), b.z, s);
+  s = fmaf(bf16_hi(w.w), b.w, s);
+  return s;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Shared-memory carve-up (byte offsets), identical on host and device.
+struct Smem {
+  uint32_t ring, bars, xs, xb, xe, hsh, yacc, red, sel_e, sel_w, act, act_n, act_slot, first, misc, total;
+};
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline Smem smem_plan(int T, int d, int I, int stages, uint32_t slot_bytes) {
+  Smem s{};
+  uint32_t at = 0;
+  auto take = [&](uint32_t bytes, uint32_t align) {
+    at = align_up(at, align);
+    const uint32_t here = at;
+    at += bytes;
+    return here;
+  };
+  s.ring = take(uint32_t(stages) * slot_bytes, 128);
+  s.bars = take(8u * uint32_t(stages > 0 ? stages : 1), 8);
+  s.xs = take(uint32_t(T) * d * 2, 16);
+  s.xb = take(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
+  s.xe = take(uint32_t(T) * (d / 32) * 2, 4);
+  s.hsh = take(uint32_t(T) * I * 4, 16);
+  s.yacc = take(uint32_t(T) * kDecodeMaxTiles * 16 * 4, 16);
+  s.red = take(uint32_t(kWarps) * kPairsMax * 32 * 2 * 4, 16);
+  s.sel_e = take(kDecodeMaxT * 32 * 4, 4);
+  s.sel_w = take(kDecodeMaxT * 32 * 4, 4);
+  s.act = take(kDecodeMaxT * 32 * 4, 4);
+  s.act_n = take(kDecodeMaxT * 32 * 4, 4);
+  s.act_slot = take(kDecodeMaxT * 32 * kDecodeMaxT * 4, 4);
+  s.first = take(kDecodeMaxT * 32 * 4, 4);
+  s.misc = take(16 * 4, 8);
+  s.total = at;
+  return s;
+}
+
+// Per-CTA load sequence: [0,nR) router, [nR,bF) shared gate/up, [bF,bSD)
+// shared down, [bSD,bGU) routed gate/up tiles, [bGU,bDN) routed down units.
+struct Seq {
+  int r0, r1, f0, f1, t0, ntl;
+  int nR, nF, nSD;
+  int rch, fch, sdch, dnch;
+  int D, g0, g1, nDN;
+  int bF, bSD, bGU, bDN;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int T = a.T, d = a.d, I = a.I, E = a.E, k = a.k;
+  const int KBd = d / kMxBlock, KBi = I / kMxBlock;
+  const int NTgu = 2 * I / kTileRows, NTd = d / kTileRows;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const Smem L = smem_plan(T, d, I, a.stages, a.slot_bytes);
+  uint8_t* ring = sm + L.ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
+  uint8_t* xb = sm + L.xb;
+  int16_t* xe = reinterpret_cast<int16_t*>(sm + L.xe);
+  float* hsh = reinterpret_cast<float*>(sm + L.hsh);
+  float* yacc = reinterpret_cast<float*>(sm + L.yacc);
+  float* red = reinterpret_cast<float*>(sm + L.red);
+  int* sel_e = reinterpret_cast<int*>(sm + L.sel_e);
+  float* sel_w = reinterpret_cast<float*>(sm + L.sel_w);
+  int* act = reinterpret_cast<int*>(sm + L.act);
+  int* act_n = reinterpret_cast<int*>(sm + L.act_n);
+  int* act_slot = reinterpret_cast<int*>(sm + L.act_slot);
+  int* first = reinterpret_cast<int*>(sm + L.first);
+  int* misc = reinterpret_cast<int*>(sm + L.misc);
+
+  DecodeState* st = a.state;
+  uint32_t* hcnt = a.state_words + kDecodeStateWords;
+  uint32_t* hready = hcnt + E * KBi;
+  const uint32_t epoch = ld_acquire_u32(&st->epoch) + 1u;
+  const uint32_t U_gu = uint32_t(KBd) * kUnitBytes, U_dn = uint32_t(KBi) * kUnitBytes;
+  const uint32_t row_bytes = uint32_t(d) * 2, sdrow_bytes = uint32_t(I) * 2;
+  const int ystride = kDecodeMaxTiles * kTileRows;
+
+  Seq s;
+  s.r0 = int((long long)c * E / G);
+  s.r1 = int((long long)(c + 1) * E / G);
+  s.f0 = a.has_shared ? int((long long)c * I / G) : 0;
+  s.f1 = a.has_shared ? int((long long)(c + 1) * I / G) : 0;
+  s.t0 = int((long long)c * NTd / G);
+  s.ntl = int((long long)(c + 1) * NTd / G) - s.t0;
+  s.rch = max(1, int(a.slot_bytes / row_bytes));
+  s.fch = max(1, int(a.slot_bytes / (2 * row_bytes)));
+  s.sdch = max(1, int(a.slot_bytes / sdrow_bytes));
+  s.dnch = max(1, int(a.slot_bytes / U_dn));
+  s.nR = (s.r1 - s.r0 + s.rch - 1) / s.rch;
+  s.nF = (s.f1 - s.f0 + s.fch - 1) / s.fch;
+  s.nSD = a.has_shared ? (s.ntl * kTileRows + s.sdch - 1) / s.sdch : 0;
+  s.bF = s.nR + s.nF;
+  s.bSD = s.bF + s.nSD;
+  s.D = 0;
+  s.g0 = s.g1 = 0;
+  s.nDN = 0;
+  s.bGU = s.bDN = s.bSD;
+
+  // bulk-copy requests of load i into its ring slot (thread 0 only)
+  auto issue = [&](int i) {
+    const int slot = i % a.stages;
+    uint8_t* dst = ring + (size_t)slot * a.slot_bytes;
+    uint64_t* bar = &full[slot];
+    if (i < s.nR) {
+      const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
+      mbar_arrive_expect_tx(bar, n * row_bytes);
+      bulk_g2s(dst, a.router_w + (size_t)r * d, n * row_bytes, bar);
+    } else if (i < s.bF) {
+      const int f = s.f0 + (i - s.nR) * s.fch, n = min(s.fch, s.f1 - f);
+      mbar_arrive_expect_tx(bar, 2 * n * row_bytes);
+      bulk_g2s(dst, a.sh_gate + (size_t)f * d, n * row_bytes, bar);
+      bulk_g2s(dst + (size_t)n * row_bytes, a.sh_up + (size_t)f * d, n * row_bytes, bar);
+    } else if (i < s.bSD) {
+      const int r = s.t0 * kTileRows + (i - s.bF) * s.sdch;
+      const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
+      mbar_arrive_expect_tx(bar, n * sdrow_bytes);
+      bulk_g2s(dst, a.sh_down + (size_t)r * I, n * sdrow_bytes, bar);
+    } else if (i < s.bGU) {
+      const int item = s.g0 + (i - s.bSD);
+      const int e = act[item / NTgu], tile = item % NTgu;
+      mbar_arrive_expect_tx(bar, U_gu);
+      bulk_g2s(dst, a.gate_up + (size_t)e * a.gu_mat + (size_t)tile * U_gu, U_gu, bar);
+    } else {
+      const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
+      mbar_arrive_expect_tx(bar, n * U_dn);
+      for (int j = 0; j < n; ++j) {
+        const int u = u0 + j, tl = u / s.D, ai = u % s.D;
+        const int e = act[ai], tile = s.t0 + tl;
+        bulk_g2s(dst + (size_t)j * U_dn, a.down + (size_t)e * a.dn_mat + (size_t)tile * U_dn, U_dn, bar);
+      }
+    }
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < a.stages; ++i) mbar_init(&full[i], 1);
+    mbar_fence_init();
+    for (int i = 0; i < a.stages && i < s.bSD; ++i) issue(i);
+  }
+  // activations: bf16 copy for the CUDA-core GEMVs, e4m3 terms for the MMAs
+  for (int i = tid; i < T * d / 8; i += kThreads)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+  for (int i = tid; i < T * ystride; i += kThreads) yacc[i] = 0.0f;
+  for (int u = warp; u < T * KBd; u += kWarps) {
+    const int t = u / KBd, kb = u % KBd;
+    const float v = __bfloat162float(a.x[(size_t)t * d + kb * kMxBlock + lane]);
+    const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
+    if (lane == 0) xe[u] = int16_t(ex);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (s.nR == 0) {
+      __threadfence();
+      atomicAdd(&st->bar, 1ull);
+    }
+    if (s.nF == 0) {
+      __threadfence();
+      atomicAdd(&st->shcnt, 1u);
+    }
+  }
+
+  int total = s.bSD;
+  for (int i = 0;; ++i) {
+    if (i == s.bF) {
+      // ---- routing: every CTA has written its router rows -------------------
+      if (tid == 0) wait_geq_u64(&st->bar, (unsigned long long)G, a.status);
+      __syncthreads();
+      if (warp < T) {
+        int e_sel;
+        float w_sel;
+        const float* brow = a.bias ? a.bias + (size_t)warp * a.bias_stride : nullptr;
+        warp_topk<32, true>(a.logits + (size_t)warp * E, brow, E, k, lane, &e_sel, &w_sel);
+        if (lane < k) {
+          sel_e[warp * k + lane] = e_sel;
+          sel_w[warp * k + lane] = w_sel;
+          if (c == 0) {
+            if (a.idx_out) a.idx_out[warp * k + lane] = e_sel;
+            if (a.w_out) a.w_out[warp * k + lane] = w_sel;
+          }
+        }
+      }
+      __syncthreads();
+      // active experts ascending; each with its slots (slot = t*k + j) in token order
+      const int n = T * k;
+      if (tid < n) {
+        const int e = sel_e[tid];
+        int f = 1;
+        for (int j = 0; j < tid; ++j) f &= sel_e[j] != e ? 1 : 0;
+        first[tid] = f;
+      }
+      __syncthreads();
+      if (tid < n) {
+        const int e = sel_e[tid];
+        int rank = 0, pos = 0, cnt = 0;
+        for (int j = 0; j < n; ++j) {
+          const int ej = sel_e[j];
+          rank += (first[j] && ej < e) ? 1 : 0;
+          pos += (j < tid && ej == e) ? 1 : 0;
+          cnt += ej == e ? 1 : 0;
+        }
+        act_slot[rank * kDecodeMaxT + pos] = tid;
+        if (first[tid]) {
+          act[rank] = e;
+          act_n[rank] = cnt;
+        }
+      }
+      if (tid == 0) {
+        int D = 0;
+        for (int j = 0; j < n; ++j) D += first[j];
+        misc[0] = D;
+      }
+      __syncthreads();
+      s.D = misc[0];
+      // gate/up tiles: contiguous ranges, balanced by bytes together with the down units
+      {
+        const long long n_gu = (long long)s.D * NTgu;
+        const long long DT = (long long)s.D * U_dn + (a.has_shared ? (long long)kTileRows * sdrow_bytes : 0LL);
+        const long long total_b = n_gu * U_gu + (long long)NTd * DT;
+        auto raw = [&](int cc) -> long long {
+          if (cc >= G) return n_gu;
+          const long long tiles_before = (long long)cc * NTd / G;
+          const long long budget = (total_b * cc) / G - tiles_before * DT;
+          const long long it = (budget + U_gu / 2) / (long long)U_gu;
+          return it < 0 ? 0 : (it > n_gu ? n_gu : it);
+        };
+        long long lo = 0, hi = 0;
+        for (int cc = 0; cc <= c + 1; ++cc) {   // monotone envelope of the raw cut points
+          const long long r = raw(cc);
+          if (cc <= c) lo = lo > r ? lo : r;
+          hi = hi > r ? hi : r;
+        }
+        s.g0 = int(lo);
+        s.g1 = int(hi);
+      }
+      s.nDN = (s.ntl * s.D + s.dnch - 1) / s.dnch;
+      s.bGU = s.bSD + (s.g1 - s.g0);
+      s.bDN = s.bGU + s.nDN;
+      total = s.bDN;
+      if (tid == 0)   // phase-B loads that fit in the ring now
+        for (int j = s.bSD; j < total && j < s.bF + a.stages; ++j) issue(j);
+      if (s.nSD > 0) {
+        // shared down needs every CTA's slice of h_sh
+        if (tid == 0) wait_geq_u32(&st->shcnt, uint32_t(G), a.status);
+        __syncthreads();
+        for (int j = tid; j < T * I; j += kThreads) hsh[j] = __ldcg(a.h_sh + j);
+      }
+      __syncthreads();
+    }
+    if (i >= total) break;
+
+    const int slot = i % a.stages;
+    const uint8_t* buf = ring + (size_t)slot * a.slot_bytes;
+    const bool ok = __syncthreads_and(mbar_wait(&full[slot], uint32_t(i / a.stages) & 1u, a.status));
+    if (ok && i < s.nR) {
+      // ---- router rows -> logits ----------------------------------------------
+      const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
+      for (int rr = warp; rr < n; rr += kWarps) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(buf + (size_t)rr * row_bytes);
+        float acc[kDecodeMaxT];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
+        for (int j = lane; j < d / 8; j += 32) {
+          const uint4 wv = wrow[j];
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t)
+            if (t < T) acc[t] += dot8_bf16(wv, reinterpret_cast<const uint4*>(xs + (size_t)t * d)[j]);
+        }
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) {
+          if (t < T) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) a.logits[(size_t)t * E + r + rr] = v;
+          }
+        }
+      }
+    } else if (ok && i < s.bF) {
+      // ---- shared gate/up rows -> h_sh -----------------------------------------
+      const int f = s.f0 + (i - s.nR) * s.fch, n = min(s.fch, s.f1 - f);
+      for (int ff = warp; ff < n; ff += kWarps) {
+        const uint4* gr = reinterpret_cast<const uint4*>(buf + (size_t)ff * row_bytes);
+        const uint4* ur = reinterpret_cast<const uint4*>(buf + (size_t)(n + ff) * row_bytes);
+        float ag[kDecodeMaxT], au[kDecodeMaxT];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) ag[t] = au[t] = 0.0f;
+        for (int j = lane; j < d / 8; j += 32) {
+          const uint4 gv = gr[j], uv = ur[j];
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t) {
+            if (t < T) {
+              const uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)t * d)[j];
+              ag[t] += dot8_bf16(gv, xv);
+              au[t] += dot8_bf16(uv, xv);
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) {
+          if (t < T) {
+            const float gs = warp_sum(ag[t]), us = warp_sum(au[t]);
+            if (lane == 0) a.h_sh[(size_t)t * I + f + ff] = silu_f(gs) * us;
+          }
+        }
+      }
+    } else if (ok && i < s.bSD) {
+      // ---- shared down rows of my tiles -> y accumulators ----------------------
+      const int r = s.t0 * kTileRows + (i - s.bF) * s.sdch;
+      const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
+      for (int rr = warp; rr < n; rr += kWarps) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(buf + (size_t)rr * sdrow_bytes);
+        float acc[kDecodeMaxT];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
+        for (int j = lane; j < I / 8; j += 32) {
+          const uint4 wv = wrow[j];
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t)
+            if (t < T) acc[t] += dot8_f32(wv, hsh + (size_t)t * I + j * 8);
+        }
+        const int row_local = r + rr - s.t0 * kTileRows;
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) {
+          if (t < T) {
+            const float v = warp_sum(acc[t]);
+            if (lane == 0) yacc[t * ystride + row_local] = v;
+          }
+        }
+      }
+    } else if (ok && i < s.bGU) {
+      // ---- routed gate/up tile -> h; publish finished 32-feature blocks --------
+      const int item = s.g0 + (i - s.bSD);
+      const int ai = item / NTgu, tile = item % NTgu;
+      const int e = act[ai], nt = act_n[ai];
+      const int* slots = act_slot + ai * kDecodeMaxT;
+      float acc[kPairsMax][2];
+#pragma unroll
+      for (int p = 0; p < kPairsMax; ++p) acc[p][0] = acc[p][1] = 0.0f;
+      for (int kb = warp; kb < KBd; kb += kWarps) {
+        const UnitFrag f = load_unit(buf + (size_t)kb * kUnitBytes, lane);
+#pragma unroll
+        for (int p = 0; p < kPairsMax; ++p) {
+          if (2 * p >= nt) break;
+          const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+          uint2 bv = make_uint2(0u, 0u);
+          if (sb < nt) {
+            const int tb = slots[sb] / k;
+            bv = *reinterpret_cast<const uint2*>(xb + ((size_t)tb * KBd + kb) * kActRowKbBytes + (g & 3) * 32 + q * 8);
+          }
+          const int ex = sc < nt ? int(xe[(slots[sc] / k) * KBd + kb]) : int(kActZeroExp);
+          unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < kPairsMax; ++p) {
+        red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
+        red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
+      }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int p = 0; p < kPairsMax; ++p) {
+          if (2 * p >= nt) break;
+          float v0 = 0.0f, v1 = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
+            v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
+          }
+          v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+          v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+          const int sc = 2 * p + (q >> 1);
+          if ((q & 1) == 0 && sc < nt) a.h[(size_t)slots[sc] * I + tile * 8 + g] = silu_f(v0) * v1;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&hcnt[e * KBi + tile / 4], 1u);
+        misc[1] = (old & 3u) == 3u ? 1 : 0;
+      }
+      __syncthreads();
+      if (misc[1] && warp == 0) {
+        // last of the four tiles of this block: split h into e4m3 terms
+        __threadfence();
+        const int kb = tile / 4;
+        for (int j = 0; j < nt; ++j) {
+          const int sl = slots[j];
+          const float v = __ldcg(a.h + (size_t)sl * I + kb * kMxBlock + lane);
+          const int ex = split_block(v, lane, a.hB + ((size_t)sl * KBi + kb) * kActRowKbBytes);
+          if (lane == 0) a.hE[(size_t)sl * KBi + kb] = int16_t(ex);
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u32(&hready[e * KBi + kb], epoch);
+      }
+    } else if (ok) {
+      // ---- routed down units of my tiles -> y accumulators ---------------------
+      const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
+      for (int j = 0; j < n; ++j) {
+        const int u = u0 + j, tl = u / s.D, ai = u % s.D;
+        const int e = act[ai], nt = act_n[ai];
+        const int* slots = act_slot + ai * kDecodeMaxT;
+        const uint8_t* ubuf = buf + (size_t)j * U_dn;
+        float acc[kPairsMax][2];
+#pragma unroll
+        for (int p = 0; p < kPairsMax; ++p) acc[p][0] = acc[p][1] = 0.0f;
+        for (int kb = warp; kb < KBi; kb += kWarps) {
+          wait_eq_u32(&hready[e * KBi + kb], epoch, a.status);
+          const UnitFrag f = load_unit(ubuf + (size_t)kb * kUnitBytes, lane);
+#pragma unroll
+          for (int p = 0; p < kPairsMax; ++p) {
+            if (2 * p >= nt) break;
+            const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+            uint2 bv = make_uint2(0u, 0u);
+            if (sb < nt)
+              bv = ld_cg_u2(a.hB + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes + (g & 3) * 32 + q * 8);
+            const int ex = sc < nt ? int(__ldcg(a.hE + (size_t)slots[sc] * KBi + kb)) : int(kActZeroExp);
+            unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < kPairsMax; ++p) {
+          red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
+          red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+          for (int p = 0; p < kPairsMax; ++p) {
+            if (2 * p >= nt) break;
+            float v0 = 0.0f, v1 = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+              v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
+              v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
+            }
+            v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+            v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+            const int sc = 2 * p + (q >> 1);
+            if ((q & 1) == 0 && sc < nt) {
+              const int sl = slots[sc], t = sl / k;
+              const float wgt = sel_w[sl];
+              float* yr = yacc + t * ystride + tl * kTileRows;
+              yr[g] = fmaf(wgt, v0, yr[g]);
+              yr[g + 8] = fmaf(wgt, v1, yr[g + 8]);
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // after the last router load: this CTA's logits are written
+    if (i == s.nR - 1 && tid == 0) {
+      __threadfence();
+      atomicAdd(&st->bar, 1ull);
+    }
+    if (s.nF > 0 && i == s.bF - 1 && tid == 0) {
+      __threadfence();
+      atomicAdd(&st->shcnt, 1u);
+    }
+    __syncthreads();
+    if (tid == 0 && i + a.stages < total) issue(i + a.stages);
+  }
+
+  // y rows of my tiles
+  for (int j = tid; j < T * s.ntl * kTileRows; j += kThreads) {
+    const int t = j / (s.ntl * kTileRows), r = j % (s.ntl * kTileRows);
+    a.y[(size_t)t * d + s.t0 * kTileRows + r] = __float2bfloat16_rn(yacc[t * ystride + r]);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t old = atomicAdd(&st->done, 1u);
+    if (old % uint32_t(G) == uint32_t(G) - 1u) {
+      // last CTA of this call: every CTA is past every wait of this call
+      st->bar = 0ull;
+      st->shcnt = 0u;
+      __threadfence();
+      st_release_u32(&st->epoch, epoch);
+    }
+  }
+}
+
+}  // namespace
+
+size_t decode_state_bytes(int E, int I) {
+  return (size_t)kDecodeStateWords * 4 + 2 * (size_t)E * (I / kMxBlock) * 4;
+}
+
+int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t* slot_bytes,
+                uint32_t* smem_bytes) {
+  if (a.T < 1 || a.T > kDecodeMaxT) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a.d % 32 || a.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int NTd = a.d / kTileRows;
+  if (di.sm_count < 1 || (NTd + di.sm_count - 1) / di.sm_count > kDecodeMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
+  uint32_t sb = uint32_t(a.d / kMxBlock) * kUnitBytes;   // one routed gate/up tile
+  const uint32_t cands[3] = {uint32_t(4 * a.d), uint32_t(2 * a.I), uint32_t(a.I / kMxBlock) * kUnitBytes};
+  for (uint32_t v : cands) sb = sb > v ? sb : v;         // a shared feature, a shared-down row, a down unit
+  sb = align_up(sb, 128);
+  const Smem fixed = smem_plan(a.T, a.d, a.I, 0, sb);
+  const size_t budget = di.smem_optin > fixed.total + 1024 ? di.smem_optin - fixed.total - 1024 : 0;
+  int S = int(budget / (sb + 8));
+  if (S > kDecodeMaxStages) S = kDecodeMaxStages;
+  if (S < 3) return MOE_ERR_UNSUPPORTED_SHAPE;
+  *stages = S;
+  *slot_bytes = sb;
+  *smem_bytes = smem_plan(a.T, a.d, a.I, S, sb).total;
+  return MOE_OK;
+}
+
+int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s) {
+  uint32_t smem = 0;
+  int st = decode_plan(a, di, &a.stages, &a.slot_bytes, &smem);
+  if (st != MOE_OK) return st;
+  MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  int per_sm = 0;
+  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem));
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(di.sm_count);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_kernel, a));
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,60 @@
+// Single-launch decode path (see decode.cu).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "host_util.h"
+
+namespace moe {
+
+constexpr int kDecodeMaxT = 4;        // tokens per call on this path
+constexpr int kDecodeMaxTiles = 4;    // 16-row output tiles per CTA
+constexpr int kDecodeMaxStages = 16;
+constexpr int kDecodeStateWords = 16; // header words before the per-block counters
+
+// Cross-call synchronisation words at the start of the workspace (zero before
+// the first call). Followed by hcnt[E * I/32] and hready[E * I/32].
+struct DecodeState {
+  unsigned long long bar;  // CTAs past their router rows (reset by the last CTA)
+  uint32_t epoch;          // calls completed
+  uint32_t done;           // CTAs finished (compared modulo the grid size)
+  uint32_t shcnt;          // CTAs whose shared gate/up slice is written (reset by the last CTA)
+  uint32_t pad[11];
+};
+static_assert(sizeof(DecodeState) == kDecodeStateWords * 4, "state header size");
+
+struct DecodeArgs {
+  int T, d, I, E, k, has_shared;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* router_w;
+  const __nv_bfloat16* sh_gate;
+  const __nv_bfloat16* sh_up;
+  const __nv_bfloat16* sh_down;
+  const uint8_t* gate_up;
+  const uint8_t* down;
+  uint64_t gu_mat, dn_mat;
+  const float* bias;
+  int bias_stride;
+  float* logits;        // [T][E]
+  int32_t* idx_out;     // [T][k] or null
+  float* w_out;         // [T][k] or null
+  __nv_bfloat16* y;     // [T][d]
+  DecodeState* state;
+  uint32_t* state_words;
+  float* h;             // [T*k][I]
+  uint8_t* hB;          // [T*k][I/32][128]
+  int16_t* hE;          // [T*k][I/32]
+  float* h_sh;          // [T][I]
+  int* status;
+  int stages;           // set by launch_decode
+  uint32_t slot_bytes;  // set by launch_decode
+};
+
+size_t decode_state_bytes(int E, int I);
+// MOE_OK if the shape/T can take this path on this device.
+int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t* slot_bytes,
+                uint32_t* smem_bytes);
+int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s);
+
+}  // namespace moe

@@ -89,6 +89,8 @@ def build(mx, w, set_idx=0):
     ("ragged", 17, 512, 96, 24, 5, "natural"),
     ("onehot", 3, 64, 32, 1, 1, "natural"),
     ("wide_k", 2, 128, 32, 40, 32, "natural"),
+    ("three", 3, 256, 64, 16, 3, "natural"),
+    ("four_small", 4, 512, 128, 32, 4, "natural"),
 ])
 def test_small_layers(mx, name, T, d, I, E, k, routing):
     w = wl.Workload(name, T=T, d=d, I=I, E=E, k=k, sets=1, routing=routing, seed=3)
@@ -175,3 +177,44 @@ def test_forward_rejects_bad_inputs(mx):
     with pytest.raises(mx.MoeError) as e:
         mx.moe_forward(layer, x, y=x)
     assert e.value.status == -1
+
+
+def test_paths(mx):
+    s = mx.moe_shape(2560, 768, 512, 8, 1)
+    assert mx.moe_query_path(s, 1) == mx.MOE_PATH_DECODE_FUSED
+    assert mx.moe_query_path(s, 4) == mx.MOE_PATH_DECODE_FUSED
+    assert mx.moe_query_path(s, 5) == mx.MOE_PATH_DECODE_MMA
+    assert mx.moe_stage_names(mx.MOE_PATH_DECODE_FUSED) == ["decode_fused"]
+    assert len(mx.moe_stage_names(mx.MOE_PATH_DECODE_MMA)) == 8
+
+
+def test_fused_workspace_reuse_matches_fresh(mx):
+    """The single-launch path keeps counters in the workspace between calls:
+    a reused workspace must give bit-identical results to fresh ones."""
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.get("mtp_t4")
+    layers = [synthetic.build_layer(w, s) for s in (0, 1)]
+    ins = [synthetic.inputs(w, s) for s in (0, 1)]
+    fresh = [mx.moe_forward(layers[s], *ins[s]) for s in (0, 1)]
+    ws = torch.zeros(layers[0].workspace_bytes(w.T), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for rep in range(5):
+        s = rep % 2
+        y = mx.moe_forward(layers[s], *ins[s], workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), fresh[s].view(torch.int16)), rep
+    assert int(st.item()) == 0
+
+
+def test_bounded_wait_selftest(mx):
+    """A wait on a flag that nothing sets gives up and reports MOE_DEV_TIMEOUT."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mx.moe_selftest_bounded_wait(flag, 1, 2_000_000, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mx.DEV_TIMEOUT
+    st.zero_()
+    flag.fill_(1)
+    mx.moe_selftest_bounded_wait(flag, 1, 2_000_000, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
