@@ -88,7 +88,7 @@ pack_kernel(const float* __restrict__ w, uint8_t* __restrict__ packed, int n_mat
       c |= (fin && signbit(v[i])) ? 8u : 0u;
       codes_sm[warp][r][hh * 16 + i] = uint8_t(c);
     }
-    if (bad && lane == 0 && status) atomicOr(status, MOE_DEV_NONFINITE_INPUT);
+    if (bad && hh == 0 && status) atomicOr(status, MOE_DEV_NONFINITE_INPUT);
     if (!bad && s > 248 && hh == 0 && status) atomicOr(status, MOE_DEV_SCALE_RANGE);
     __syncwarp();
     // assemble this lane's 8 packed bytes: lane = 4g + q
