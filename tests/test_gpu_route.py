@@ -48,13 +48,13 @@ def check_route(mx, l, k, bias=None):
     assert np.all(np.abs(gw[fin].sum(1) - 1.0) <= 2e-6)
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 512, 8), (4, 512, 8), (64, 512, 8), (3, 32, 4), (5, 40, 40),
+@pytest.mark.parametrize("T,E,k", [(1, 512, 8), (4, 512, 8), (64, 512, 8), (3, 32, 4), (5, 40, 32),
                                    (7, 100, 3), (2, 1024, 32), (9, 1, 1), (33, 96, 8)])
 def test_topk_random(mx, T, E, k):
     check_route(mx, make_logits(T, E, T * 1000 + E), k)
 
 
-@pytest.mark.parametrize("T,E,k", [(16, 512, 8), (8, 32, 4), (4, 64, 64)])
+@pytest.mark.parametrize("T,E,k", [(16, 512, 8), (8, 32, 4), (4, 64, 32)])
 def test_topk_ties_and_specials(mx, T, E, k):
     check_route(mx, make_logits(T, E, 7, ties=True), k)
     l = make_logits(T, E, 8, ties=True, specials=True)
