@@ -332,6 +332,13 @@ def run_ours(args, w):
     # distinct experts per set (for algorithmic bytes)
     D_sets = [len(set(i.cpu().numpy().ravel().tolist())) for i in idxs]
 
+    # the library records these inside the graph (external event nodes); one
+    # record through torch first marks them as recorded for elapsed_time()
+    with torch.cuda.stream(stream):
+        for evs in events:
+            for ev in evs:
+                ev.record(stream)
+    torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         one_cycle(True)
