@@ -22,7 +22,9 @@ __all__ = [
     "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp4.so")
+# MOE_MXFP4_LIB may name another build of the same library (e.g. a debug build).
+LIB_PATH = os.environ.get("MOE_MXFP4_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                           "libmoe_mxfp4.so")
 
 MOE_LAYOUT_MMA16 = 1
 MOE_LAYOUT_MMA16_GATEUP = 2

@@ -49,14 +49,19 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source and link the shared library; returns its path."""
+def build(verbose: bool = False, force: bool = False, extra_flags=(), out_path: str = LIB_PATH,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile every CUDA source and link the shared library; returns its path.
+
+    extra_flags / out_path / build_dir allow a separately built variant (for
+    example with a debug define) next to the default library.
+    """
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = _headers()
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, __file__] + hdrs):
             jobs.append([nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj])
@@ -74,11 +79,11 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp"
+    if force or jobs or _stale(out_path, objs):
+        tmp = out_path + ".tmp"
         run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, out_path)
+    return out_path
 
 
 if __name__ == "__main__":

@@ -335,3 +335,13 @@ extern "C" int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want
   wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag_dev, want, budget_cycles, dev_status);
   return launch_status();
 }
+
+#ifdef MOE_DECODE_TRACE
+namespace moe {
+int decode_trace_copy(unsigned long long* host, int n_cta);
+}
+// Debug builds only: phase timestamps of the last single-launch decode call.
+extern "C" int moe_debug_decode_trace(unsigned long long* host, int n_cta) {
+  return moe::decode_trace_copy(host, n_cta);
+}
+#endif

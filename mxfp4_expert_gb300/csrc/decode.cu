@@ -40,6 +40,21 @@
 namespace moe {
 namespace {
 
+#ifdef MOE_DECODE_TRACE
+// Debug builds only: per-CTA globaltimer stamps at phase boundaries.
+constexpr int kTracePoints = 16;
+__device__ unsigned long long g_trace[1024][kTracePoints];
+__device__ __forceinline__ void trace(int point) {
+  if (threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_trace[blockIdx.x][point] = t;
+  }
+}
+#else
+__device__ __forceinline__ void trace(int) {}
+#endif
+
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
@@ -121,6 +136,7 @@ struct Seq {
 
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
+  trace(0);
   const int T = a.T, d = a.d, I = a.I, E = a.E, k = a.k;
   const int KBd = d / kMxBlock, KBi = I / kMxBlock;
   const int NTgu = 2 * I / kTileRows, NTd = d / kTileRows;
@@ -235,12 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
   }
 
+  trace(1);
   int total = s.bSD;
   for (int i = 0;; ++i) {
     if (i == s.bF) {
       // ---- routing: every CTA has written its router rows -------------------
+      trace(3);
       if (tid == 0) wait_geq_u64(&st->bar, (unsigned long long)G, a.status);
       __syncthreads();
+      trace(4);
       if (warp < T) {
         int e_sel;
         float w_sel;
@@ -314,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       total = s.bDN;
       if (tid == 0)   // phase-B loads that fit in the ring now
         for (int j = s.bSD; j < total && j < s.bF + a.stages; ++j) issue(j);
+      trace(5);
       if (s.nSD > 0) {
         // shared down needs every CTA's slice of h_sh
         if (tid == 0) wait_geq_u32(&st->shcnt, uint32_t(G), a.status);
@@ -321,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int j = tid; j < T * I; j += kThreads) hsh[j] = __ldcg(a.h_sh + j);
       }
       __syncthreads();
+      trace(6);
     }
+    if (i == s.bSD) trace(7);
+    if (i == s.bGU) trace(8);
     if (i >= total) break;
 
     const int slot = i % a.stages;
@@ -525,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       }
     }
     // after the last router load: this CTA's logits are written
+    if (i == s.nR - 1) trace(2);
     if (i == s.nR - 1 && tid == 0) {
       __threadfence();
       atomicAdd(&st->bar, 1ull);
@@ -537,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     if (tid == 0 && i + a.stages < total) issue(i + a.stages);
   }
 
+  trace(9);
   // y rows of my tiles
   for (int j = tid; j < T * s.ntl * kTileRows; j += kThreads) {
     const int t = j / (s.ntl * kTileRows), r = j % (s.ntl * kTileRows);
@@ -554,9 +579,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       st_release_u32(&st->epoch, epoch);
     }
   }
+  trace(10);
 }
 
 }  // namespace
+
+#ifdef MOE_DECODE_TRACE
+int decode_trace_copy(unsigned long long* host, int n_cta) {
+  MOE_CUDA_TRY(cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * kTracePoints * n_cta));
+  return MOE_OK;
+}
+#endif
 
 size_t decode_state_bytes(int E, int I) {
   return (size_t)kDecodeStateWords * 4 + 2 * (size_t)E * (I / kMxBlock) * 4;
