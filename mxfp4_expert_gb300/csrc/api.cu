@@ -70,7 +70,7 @@ Workspace plan(const moe_shape& sh, int T) {
   o.h_sh = take(size_t(T) * I * 4);
   o.h = take(slots * I * 4);
   o.h_b = take(slots * (I / 32) * kActRowKbBytes);
-  o.h_e = take(slots * (I / 32) * 2);
+  o.h_e = take(slots * decode_he_stride(int(I)) * 2);
   o.part = take(slots * d * 4);
   o.total = at;
   return o;
@@ -210,8 +210,6 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
     da.w_out = w_out;
     da.y = static_cast<__nv_bfloat16*>(y_dev);
     da.state = at<DecodeState>(B, ws.state);
-    da.state_words = at<uint32_t>(B, ws.state);
-    da.h = at<float>(B, ws.h);
     da.hB = at<uint8_t>(B, ws.h_b);
     da.hE = at<int16_t>(B, ws.h_e);
     da.h_sh = at<float>(B, ws.h_sh);

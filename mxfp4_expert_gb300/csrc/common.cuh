@@ -15,8 +15,8 @@ constexpr int kMxBlock = 32;        // elements per E8M0 scale (OCP MX)
 constexpr int kTileRows = 16;       // rows per packed tile = MMA M
 constexpr int kUnitCodeBytes = 256; // 16 rows x 32 codes x 4 bits
 constexpr int kUnitBytes = 272;     // codes + 16 scale bytes
-constexpr int kActTerms = 4;        // B-operand columns per activation row
-constexpr int kActRowKbBytes = 128; // 4 terms x 32 e4m3 bytes per (row, K-block)
+constexpr int kActTerms = 3;        // e4m3 terms per activation value (MMA B columns 0..2; column 3 is zero)
+constexpr int kActRowKbBytes = 96;  // 3 terms x 32 e4m3 bytes per (row, K-block)
 constexpr int16_t kActZeroExp = -32768;  // marks an all-zero activation block
 
 // Spin budget for any wait on another agent (clock64 cycles, ~1 s at 2 GHz).

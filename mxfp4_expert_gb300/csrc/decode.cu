@@ -9,26 +9,32 @@
 //   R   its slice of router rows             -> logits (global)     phase A
 //   F   its slice of shared gate/up rows     -> h_sh (global)       phase A
 //   SD  shared-down rows of its output tiles -> y accumulators      needs all h_sh
-//   GU  its share of the routed gate/up tiles -> h (global)         needs routing
-//   DN  routed-down units of its output tiles -> y accumulators     needs h blocks
+//   GU  its routed gate/up items             -> h blocks (global)   needs routing
+//   DN  routed-down units of its output tiles -> y accumulators     needs all h blocks
 //
 // R, F and SD do not depend on routing and are requested at kernel start, so
 // HBM is busy from the first cycle. After its R loads a CTA arrives at a
-// counter barrier; it computes its F loads while the other CTAs catch up, then
-// waits, reads all logits and runs the top-k itself (every CTA derives the
-// same routing, so no second exchange is needed). Phase-B loads are requested
-// next. Gate/up tiles publish h per 32-feature block: the last of the four
-// tiles of a block (an atomic counter) splits it into e4m3 terms and sets a
-// ready flag holding the call's epoch; down units wait on those flags. Each
-// CTA owns whole output rows (16-row tiles), so y is written without a
-// cross-CTA reduction. Gate/up tiles are handed out so that every CTA moves
-// about the same number of bytes in phase B, counting its down units.
+// counter barrier; it computes its F loads while the others catch up, then
+// reads all logits and runs the top-k itself (every CTA derives the same
+// routing, so no second exchange is needed), and requests its phase-B loads.
 //
-// Cross-call state (barrier/epoch counters, per-block counters and flags)
-// lives at the start of the workspace and must be zero before the first call.
-// Counters are reset by the last CTA of a call or compared modulo their
-// per-call increment. Every wait is bounded (kSpinBudget); on timeout the
-// kernel sets MOE_DEV_TIMEOUT and carries on.
+// A routed gate/up item is one 32-feature block of one active expert (four
+// 16-row tiles, 87 KB for the Ling shape). The CTA that computes it holds the
+// block's 32 values of h per token and writes them directly as e4m3 terms with
+// one block exponent (the B operand of the down MMA), so no other CTA has to
+// touch h. After its last item a CTA publishes with one release increment;
+// before its down units it waits for all CTAs, then pulls every token's h
+// terms into shared memory with one bulk copy. Down units accumulate in
+// registers across experts and K-blocks; the cross-warp sum is taken once per
+// output tile at the end. Each CTA owns whole 16-row output tiles, so y is
+// written without a cross-CTA reduction. Gate/up items are handed out so that
+// every CTA moves about the same number of bytes in phase B, counting its down
+// and shared-down rows.
+//
+// Cross-call state (counters) lives at the start of the workspace and must be
+// zero before the first call; the last CTA of a call resets it. Every wait is
+// bounded (kSpinBudget); on timeout the kernel sets MOE_DEV_TIMEOUT and
+// carries on.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -58,8 +64,8 @@ __device__ __forceinline__ void trace(int) {}
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
+constexpr int kRowsPerLoad = 8;   // max rows of a "few long rows" GEMV load (split-K over warps)
 
-// sum over 8 bf16 weights times 8 bf16 activations (both as uint4)
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
   float s = bf16_lo(w.x) * bf16_lo(x.x);
   s = fmaf(bf16_hi(w.x), bf16_hi(x.x), s);
@@ -71,7 +77,6 @@ __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
   s = fmaf(bf16_hi(w.w), bf16_hi(x.w), s);
   return s;
 }
-// sum over 8 bf16 weights times 8 fp32 values
 __device__ __forceinline__ float dot8_f32(uint4 w, const float* h) {
   const float4 a = *reinterpret_cast<const float4*>(h);
   const float4 b = *reinterpret_cast<const float4*>(h + 4);
@@ -90,13 +95,69 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
 }
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
-// Shared-memory carve-up (byte offsets), identical on host and device.
+// bf16 rows (row-major, K elements each, in shared memory) times T bf16
+// activation vectors (shared memory), split over all warps along K.
+// out[r * kDecodeMaxT + t] (shared) receives the dot products. n <= kRowsPerLoad.
+__device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfloat16* xs, int T,
+                               float* red, float* out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunks = K / 8;
+  float acc[kRowsPerLoad][kDecodeMaxT];
+#pragma unroll
+  for (int r = 0; r < kRowsPerLoad; ++r)
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxT; ++t) acc[r][t] = 0.0f;
+  for (int j = tid; j < chunks; j += kThreads) {
+    uint4 xv[kDecodeMaxT];
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxT; ++t)
+      if (t < T) xv[t] = reinterpret_cast<const uint4*>(xs + (size_t)t * K)[j];
+#pragma unroll
+    for (int r = 0; r < kRowsPerLoad; ++r) {
+      if (r < n) {
+        const uint4 wv = reinterpret_cast<const uint4*>(rows + (size_t)r * K * 2)[j];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t)
+          if (t < T) acc[r][t] += dot8_bf16(wv, xv[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerLoad; ++r) {
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxT; ++t) {
+      if (r < n && t < T) {
+        const float v = warp_sum(acc[r][t]);
+        if (lane == 0) red[(warp * kRowsPerLoad + r) * kDecodeMaxT + t] = v;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < n * kDecodeMaxT) {
+    const int r = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
+    float v = 0.0f;
+    if (t < T)
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += red[(w * kRowsPerLoad + r) * kDecodeMaxT + t];
+    out[tid] = v;
+  }
+  __syncthreads();
+}
+
+// Shared-memory carve-up (byte offsets), identical on host and device. The
+// phase-A buffers (xs, xb, xe, hsh) and the phase-B h terms (hbs, hes) share
+// one region: the former are dead once the down units start.
 struct Smem {
-  uint32_t ring, bars, xs, xb, xe, hsh, yacc, red, sel_e, sel_w, act, act_n, act_slot, first, misc, total;
+  uint32_t ring, bars, ov, xs, xb, xe, hsh, hbs, hes, hblk, yacc, red, gout, sel_e, sel_w, act, act_n,
+      act_slot, first, misc, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
-__host__ __device__ inline Smem smem_plan(int T, int d, int I, int stages, uint32_t slot_bytes) {
+__host__ __device__ inline uint32_t he_stride(int I) { return align_up(uint32_t(I / kMxBlock), 8); }
+__host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages, uint32_t slot_bytes) {
   Smem s{};
   uint32_t at = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
@@ -106,13 +167,34 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int stages, uint3
     return here;
   };
   s.ring = take(uint32_t(stages) * slot_bytes, 128);
-  s.bars = take(8u * uint32_t(stages > 0 ? stages : 1), 8);
-  s.xs = take(uint32_t(T) * d * 2, 16);
-  s.xb = take(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
-  s.xe = take(uint32_t(T) * (d / 32) * 2, 4);
-  s.hsh = take(uint32_t(T) * I * 4, 16);
+  s.bars = take(8u * uint32_t(stages + 1), 8);
+  // overlay: phase A layout
+  const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
+  const uint32_t xb_b = align_up(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
+  const uint32_t xe_b = align_up(uint32_t(T) * (d / 32) * 2, 16);
+  const uint32_t hsh_b = align_up(uint32_t(T) * I * 4, 16);
+  const uint32_t a_bytes = xs_b + xb_b + xe_b + hsh_b;
+  // overlay: phase B layout (h terms of every slot)
+  const uint32_t slots = uint32_t(T) * k;
+  const uint32_t hbs_b = align_up(slots * (I / 32) * kActRowKbBytes, 16);
+  const uint32_t hes_b = align_up(slots * he_stride(I) * 2, 16);
+  const uint32_t b_bytes = hbs_b + hes_b;
+  s.ov = take(a_bytes > b_bytes ? a_bytes : b_bytes, 128);
+  s.xs = s.ov;
+  s.xb = s.xs + xs_b;
+  s.xe = s.xb + xb_b;
+  s.hsh = s.xe + xe_b;
+  s.hbs = s.ov;
+  s.hes = s.hbs + hbs_b;
+  s.hblk = take(kDecodeMaxT * 32 * 4, 16);
   s.yacc = take(uint32_t(T) * kDecodeMaxTiles * 16 * 4, 16);
-  s.red = take(uint32_t(kWarps) * kPairsMax * 32 * 2 * 4, 16);
+  const uint32_t red_mma = kWarps * kPairsMax * 32 * 2 * 4;
+  const uint32_t red_gemv = kWarps * kRowsPerLoad * kDecodeMaxT * 4;
+  const uint32_t red_dn = kWarps * kDecodeMaxT * 32 * 2 * 4;
+  uint32_t red_b = red_mma > red_gemv ? red_mma : red_gemv;
+  red_b = red_b > red_dn ? red_b : red_dn;
+  s.red = take(red_b, 16);
+  s.gout = take(kRowsPerLoad * kDecodeMaxT * 4, 16);
   s.sel_e = take(kDecodeMaxT * 32 * 4, 4);
   s.sel_w = take(kDecodeMaxT * 32 * 4, 4);
   s.act = take(kDecodeMaxT * 32 * 4, 4);
@@ -125,12 +207,13 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int stages, uint3
 }
 
 // Per-CTA load sequence: [0,nR) router, [nR,bF) shared gate/up, [bF,bSD)
-// shared down, [bSD,bGU) routed gate/up tiles, [bGU,bDN) routed down units.
+// shared down, [bSD,bGU) routed gate/up tiles (4 per item), [bGU,bDN) routed
+// down loads (dnch units each).
 struct Seq {
   int r0, r1, f0, f1, t0, ntl;
   int nR, nF, nSD;
   int rch, fch, sdch, dnch;
-  int D, g0, g1, nDN;
+  int D, i0, i1, nDN;
   int bF, bSD, bGU, bDN;
 };
 
@@ -138,20 +221,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   trace(0);
   const int T = a.T, d = a.d, I = a.I, E = a.E, k = a.k;
-  const int KBd = d / kMxBlock, KBi = I / kMxBlock;
-  const int NTgu = 2 * I / kTileRows, NTd = d / kTileRows;
+  const int KBd = d / kMxBlock, KBi = I / kMxBlock, HES = int(he_stride(I));
+  const int NTd = d / kTileRows;
   const int G = gridDim.x, c = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const Smem L = smem_plan(T, d, I, a.stages, a.slot_bytes);
+  const Smem L = smem_plan(T, d, I, k, a.stages, a.slot_bytes);
   uint8_t* ring = sm + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* hbar = full + a.stages;
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
   uint8_t* xb = sm + L.xb;
   int16_t* xe = reinterpret_cast<int16_t*>(sm + L.xe);
   float* hsh = reinterpret_cast<float*>(sm + L.hsh);
+  uint8_t* hbs = sm + L.hbs;
+  int16_t* hes = reinterpret_cast<int16_t*>(sm + L.hes);
+  float* hblk = reinterpret_cast<float*>(sm + L.hblk);
   float* yacc = reinterpret_cast<float*>(sm + L.yacc);
   float* red = reinterpret_cast<float*>(sm + L.red);
+  float* gout = reinterpret_cast<float*>(sm + L.gout);
   int* sel_e = reinterpret_cast<int*>(sm + L.sel_e);
   float* sel_w = reinterpret_cast<float*>(sm + L.sel_w);
   int* act = reinterpret_cast<int*>(sm + L.act);
@@ -161,9 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   int* misc = reinterpret_cast<int*>(sm + L.misc);
 
   DecodeState* st = a.state;
-  uint32_t* hcnt = a.state_words + kDecodeStateWords;
-  uint32_t* hready = hcnt + E * KBi;
-  const uint32_t epoch = ld_acquire_u32(&st->epoch) + 1u;
   const uint32_t U_gu = uint32_t(KBd) * kUnitBytes, U_dn = uint32_t(KBi) * kUnitBytes;
   const uint32_t row_bytes = uint32_t(d) * 2, sdrow_bytes = uint32_t(I) * 2;
   const int ystride = kDecodeMaxTiles * kTileRows;
@@ -175,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   s.f1 = a.has_shared ? int((long long)(c + 1) * I / G) : 0;
   s.t0 = int((long long)c * NTd / G);
   s.ntl = int((long long)(c + 1) * NTd / G) - s.t0;
-  s.rch = max(1, int(a.slot_bytes / row_bytes));
-  s.fch = max(1, int(a.slot_bytes / (2 * row_bytes)));
+  s.rch = min(kRowsPerLoad, max(1, int(a.slot_bytes / row_bytes)));
+  s.fch = min(kRowsPerLoad / 2, max(1, int(a.slot_bytes / (2 * row_bytes))));
   s.sdch = max(1, int(a.slot_bytes / sdrow_bytes));
   s.dnch = max(1, int(a.slot_bytes / U_dn));
   s.nR = (s.r1 - s.r0 + s.rch - 1) / s.rch;
@@ -185,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   s.bF = s.nR + s.nF;
   s.bSD = s.bF + s.nSD;
   s.D = 0;
-  s.g0 = s.g1 = 0;
+  s.i0 = s.i1 = 0;
   s.nDN = 0;
   s.bGU = s.bDN = s.bSD;
 
@@ -209,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       mbar_arrive_expect_tx(bar, n * sdrow_bytes);
       bulk_g2s(dst, a.sh_down + (size_t)r * I, n * sdrow_bytes, bar);
     } else if (i < s.bGU) {
-      const int item = s.g0 + (i - s.bSD);
-      const int e = act[item / NTgu], tile = item % NTgu;
+      const int j = i - s.bSD;
+      const int item = s.i0 + j / 4, tile = (item % KBi) * 4 + (j % 4);
+      const int e = act[item / KBi];
       mbar_arrive_expect_tx(bar, U_gu);
       bulk_g2s(dst, a.gate_up + (size_t)e * a.gu_mat + (size_t)tile * U_gu, U_gu, bar);
     } else {
@@ -225,21 +311,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   };
 
   if (tid == 0) {
-    for (int i = 0; i < a.stages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i <= a.stages; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
     for (int i = 0; i < a.stages && i < s.bSD; ++i) issue(i);
   }
-  // activations: bf16 copy for the CUDA-core GEMVs, e4m3 terms for the MMAs
+  // activations: bf16 copy for the CUDA-core GEMVs, then e4m3 terms for the MMAs
   for (int i = tid; i < T * d / 8; i += kThreads)
     reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
   for (int i = tid; i < T * ystride; i += kThreads) yacc[i] = 0.0f;
+  __syncthreads();
   for (int u = warp; u < T * KBd; u += kWarps) {
-    const int t = u / KBd, kb = u % KBd;
-    const float v = __bfloat162float(a.x[(size_t)t * d + kb * kMxBlock + lane]);
+    const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
     const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
     if (lane == 0) xe[u] = int16_t(ex);
   }
   __syncthreads();
+  trace(1);
   if (tid == 0) {
     if (s.nR == 0) {
       __threadfence();
@@ -251,7 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
   }
 
-  trace(1);
+  // per-lane down accumulators: [tile][token][row g / row g+8]
+  float dacc[kDecodeMaxTiles][kDecodeMaxT][2];
+#pragma unroll
+  for (int tl = 0; tl < kDecodeMaxTiles; ++tl)
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxT; ++t) dacc[tl][t][0] = dacc[tl][t][1] = 0.0f;
+
   int total = s.bSD;
   for (int i = 0;; ++i) {
     if (i == s.bF) {
@@ -275,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
       }
       __syncthreads();
+      trace(11);
       // active experts ascending; each with its slots (slot = t*k + j) in token order
       const int n = T * k;
       if (tid < n) {
@@ -302,33 +396,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       if (tid == 0) {
         int D = 0;
         for (int j = 0; j < n; ++j) D += first[j];
+        // gate/up items (32-feature blocks): contiguous ranges, balanced by bytes
+        // together with each CTA's down units and shared-down rows. W(c) is the
+        // cumulative budget left for items before CTA c (non-decreasing).
+        const int n_items = D * KBi;
+        const float U = 4.0f * float(U_gu);
+        const float DT = float(D) * float(U_dn) + (a.has_shared ? float(kTileRows) * float(sdrow_bytes) : 0.0f);
+        const float target = (float(n_items) * U + float(NTd) * DT) / float(G);
+        const int qt = NTd / G;
+        const float w0 = fmaxf(0.0f, target - DT * float(qt)), w1 = fmaxf(0.0f, target - DT * float(qt + 1));
+        auto W = [&](int cc) {
+          const int big = (cc * NTd) / G - cc * qt;
+          return float(cc - big) * w0 + float(big) * w1;
+        };
+        const float WG = W(G);
+        auto cut = [&](int cc) {
+          if (cc >= G) return n_items;
+          if (WG <= 0.0f) return 0;
+          const int v = int(floorf(float(n_items) * (W(cc) / WG) + 0.5f));
+          return v < 0 ? 0 : (v > n_items ? n_items : v);
+        };
         misc[0] = D;
+        misc[1] = cut(c);
+        misc[2] = cut(c + 1);
       }
       __syncthreads();
       s.D = misc[0];
-      // gate/up tiles: contiguous ranges, balanced by bytes together with the down units
-      {
-        const long long n_gu = (long long)s.D * NTgu;
-        const long long DT = (long long)s.D * U_dn + (a.has_shared ? (long long)kTileRows * sdrow_bytes : 0LL);
-        const long long total_b = n_gu * U_gu + (long long)NTd * DT;
-        auto raw = [&](int cc) -> long long {
-          if (cc >= G) return n_gu;
-          const long long tiles_before = (long long)cc * NTd / G;
-          const long long budget = (total_b * cc) / G - tiles_before * DT;
-          const long long it = (budget + U_gu / 2) / (long long)U_gu;
-          return it < 0 ? 0 : (it > n_gu ? n_gu : it);
-        };
-        long long lo = 0, hi = 0;
-        for (int cc = 0; cc <= c + 1; ++cc) {   // monotone envelope of the raw cut points
-          const long long r = raw(cc);
-          if (cc <= c) lo = lo > r ? lo : r;
-          hi = hi > r ? hi : r;
-        }
-        s.g0 = int(lo);
-        s.g1 = int(hi);
-      }
+      s.i0 = misc[1];
+      s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
       s.nDN = (s.ntl * s.D + s.dnch - 1) / s.dnch;
-      s.bGU = s.bSD + (s.g1 - s.g0);
+      s.bGU = s.bSD + 4 * (s.i1 - s.i0);
       s.bDN = s.bGU + s.nDN;
       total = s.bDN;
       if (tid == 0)   // phase-B loads that fit in the ring now
@@ -344,7 +441,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       trace(6);
     }
     if (i == s.bSD) trace(7);
-    if (i == s.bGU) trace(8);
+    if (i == s.bGU) {
+      // ---- all h blocks of every CTA: publish mine, wait, stage them ----------
+      trace(8);
+      if (tid == 0) {
+        red_release_add(&st->gudone, 1u);
+        wait_geq_u32(&st->gudone, uint32_t(G), a.status);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const uint32_t hb_bytes = uint32_t(T * k) * KBi * kActRowKbBytes;
+        const uint32_t he_bytes = uint32_t(T * k) * HES * 2;
+        mbar_arrive_expect_tx(hbar, hb_bytes + he_bytes);
+        bulk_g2s(hbs, a.hB, hb_bytes, hbar);
+        bulk_g2s(hes, a.hE, he_bytes, hbar);
+      }
+      __syncthreads();
+      mbar_wait(hbar, 0u, a.status);
+      __syncthreads();
+      trace(9);
+    }
     if (i >= total) break;
 
     const int slot = i % a.stages;
@@ -353,55 +467,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     if (ok && i < s.nR) {
       // ---- router rows -> logits ----------------------------------------------
       const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
-      for (int rr = warp; rr < n; rr += kWarps) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(buf + (size_t)rr * row_bytes);
-        float acc[kDecodeMaxT];
-#pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
-        for (int j = lane; j < d / 8; j += 32) {
-          const uint4 wv = wrow[j];
-#pragma unroll
-          for (int t = 0; t < kDecodeMaxT; ++t)
-            if (t < T) acc[t] += dot8_bf16(wv, reinterpret_cast<const uint4*>(xs + (size_t)t * d)[j]);
-        }
-#pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) {
-          if (t < T) {
-            const float v = warp_sum(acc[t]);
-            if (lane == 0) a.logits[(size_t)t * E + r + rr] = v;
-          }
-        }
-      }
+      gemv_bf16_rows(buf, n, d, xs, T, red, gout);
+      if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T)
+        a.logits[(size_t)(tid % kDecodeMaxT) * E + r + tid / kDecodeMaxT] = gout[tid];
     } else if (ok && i < s.bF) {
       // ---- shared gate/up rows -> h_sh -----------------------------------------
       const int f = s.f0 + (i - s.nR) * s.fch, n = min(s.fch, s.f1 - f);
-      for (int ff = warp; ff < n; ff += kWarps) {
-        const uint4* gr = reinterpret_cast<const uint4*>(buf + (size_t)ff * row_bytes);
-        const uint4* ur = reinterpret_cast<const uint4*>(buf + (size_t)(n + ff) * row_bytes);
-        float ag[kDecodeMaxT], au[kDecodeMaxT];
-#pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) ag[t] = au[t] = 0.0f;
-        for (int j = lane; j < d / 8; j += 32) {
-          const uint4 gv = gr[j], uv = ur[j];
-#pragma unroll
-          for (int t = 0; t < kDecodeMaxT; ++t) {
-            if (t < T) {
-              const uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)t * d)[j];
-              ag[t] += dot8_bf16(gv, xv);
-              au[t] += dot8_bf16(uv, xv);
-            }
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) {
-          if (t < T) {
-            const float gs = warp_sum(ag[t]), us = warp_sum(au[t]);
-            if (lane == 0) a.h_sh[(size_t)t * I + f + ff] = silu_f(gs) * us;
-          }
-        }
+      gemv_bf16_rows(buf, 2 * n, d, xs, T, red, gout);   // rows 0..n-1 gate, n..2n-1 up
+      if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T) {
+        const int ff = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
+        a.h_sh[(size_t)t * I + f + ff] = silu_f(gout[ff * kDecodeMaxT + t]) * gout[(n + ff) * kDecodeMaxT + t];
       }
     } else if (ok && i < s.bSD) {
-      // ---- shared down rows of my tiles -> y accumulators ----------------------
+      // ---- shared down rows of my tiles -> y accumulators (warp per row) -------
       const int r = s.t0 * kTileRows + (i - s.bF) * s.sdch;
       const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
       for (int rr = warp; rr < n; rr += kWarps) {
@@ -425,10 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
       }
     } else if (ok && i < s.bGU) {
-      // ---- routed gate/up tile -> h; publish finished 32-feature blocks --------
-      const int item = s.g0 + (i - s.bSD);
-      const int ai = item / NTgu, tile = item % NTgu;
-      const int e = act[ai], nt = act_n[ai];
+      // ---- routed gate/up tile (one of the 4 of a 32-feature item) -------------
+      const int j = i - s.bSD, sub = j % 4;
+      const int item = s.i0 + j / 4;
+      const int ai = item / KBi, fb = item % KBi;
+      const int nt = act_n[ai];
       const int* slots = act_slot + ai * kDecodeMaxT;
       float acc[kPairsMax][2];
 #pragma unroll
@@ -439,11 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int p = 0; p < kPairsMax; ++p) {
           if (2 * p >= nt) break;
           const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-          uint2 bv = make_uint2(0u, 0u);
-          if (sb < nt) {
-            const int tb = slots[sb] / k;
-            bv = *reinterpret_cast<const uint2*>(xb + ((size_t)tb * KBd + kb) * kActRowKbBytes + (g & 3) * 32 + q * 8);
-          }
+          const uint2 bv = sb < nt ? load_bfrag_smem(xb + ((size_t)(slots[sb] / k) * KBd + kb) * kActRowKbBytes, lane)
+                                   : make_uint2(0u, 0u);
           const int ex = sc < nt ? int(xe[(slots[sc] / k) * KBd + kb]) : int(kActZeroExp);
           unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
         }
@@ -467,84 +543,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
           v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
           const int sc = 2 * p + (q >> 1);
-          if ((q & 1) == 0 && sc < nt) a.h[(size_t)slots[sc] * I + tile * 8 + g] = silu_f(v0) * v1;
+          if ((q & 1) == 0 && sc < nt) hblk[sc * 32 + sub * 8 + g] = silu_f(v0) * v1;
         }
       }
       __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const uint32_t old = atomicAdd(&hcnt[e * KBi + tile / 4], 1u);
-        misc[1] = (old & 3u) == 3u ? 1 : 0;
-      }
-      __syncthreads();
-      if (misc[1] && warp == 0) {
-        // last of the four tiles of this block: split h into e4m3 terms
-        __threadfence();
-        const int kb = tile / 4;
-        for (int j = 0; j < nt; ++j) {
-          const int sl = slots[j];
-          const float v = __ldcg(a.h + (size_t)sl * I + kb * kMxBlock + lane);
-          const int ex = split_block(v, lane, a.hB + ((size_t)sl * KBi + kb) * kActRowKbBytes);
-          if (lane == 0) a.hE[(size_t)sl * KBi + kb] = int16_t(ex);
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) st_release_u32(&hready[e * KBi + kb], epoch);
+      if (sub == 3 && warp < nt) {
+        // the item's 32 features are complete: write them as e4m3 terms
+        const int sl = slots[warp];
+        const int ex = split_block(hblk[warp * 32 + lane], lane, a.hB + ((size_t)sl * KBi + fb) * kActRowKbBytes);
+        if (lane == 0) a.hE[(size_t)sl * HES + fb] = int16_t(ex);
       }
     } else if (ok) {
-      // ---- routed down units of my tiles -> y accumulators ---------------------
+      // ---- routed down units of my tiles -> per-lane accumulators --------------
       const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
       for (int j = 0; j < n; ++j) {
         const int u = u0 + j, tl = u / s.D, ai = u % s.D;
-        const int e = act[ai], nt = act_n[ai];
+        const int nt = act_n[ai];
         const int* slots = act_slot + ai * kDecodeMaxT;
         const uint8_t* ubuf = buf + (size_t)j * U_dn;
-        float acc[kPairsMax][2];
-#pragma unroll
-        for (int p = 0; p < kPairsMax; ++p) acc[p][0] = acc[p][1] = 0.0f;
         for (int kb = warp; kb < KBi; kb += kWarps) {
-          wait_eq_u32(&hready[e * KBi + kb], epoch, a.status);
           const UnitFrag f = load_unit(ubuf + (size_t)kb * kUnitBytes, lane);
 #pragma unroll
           for (int p = 0; p < kPairsMax; ++p) {
             if (2 * p >= nt) break;
             const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-            uint2 bv = make_uint2(0u, 0u);
-            if (sb < nt)
-              bv = ld_cg_u2(a.hB + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes + (g & 3) * 32 + q * 8);
-            const int ex = sc < nt ? int(__ldcg(a.hE + (size_t)slots[sc] * KBi + kb)) : int(kActZeroExp);
-            unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
-          }
-        }
-#pragma unroll
-        for (int p = 0; p < kPairsMax; ++p) {
-          red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
-          red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
-        }
-        __syncthreads();
-        if (warp == 0) {
-#pragma unroll
-          for (int p = 0; p < kPairsMax; ++p) {
-            if (2 * p >= nt) break;
-            float v0 = 0.0f, v1 = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-              v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
-              v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
-            }
-            v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
-            v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
-            const int sc = 2 * p + (q >> 1);
-            if ((q & 1) == 0 && sc < nt) {
-              const int sl = slots[sc], t = sl / k;
+            const uint2 bv = sb < nt ? load_bfrag_smem(hbs + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes, lane)
+                                     : make_uint2(0u, 0u);
+            float d4[4];
+            mma_e4m3(d4, f.a0, f.a1, f.a2, f.a3, bv.x, bv.y);
+            if (sc < nt) {
+              const int sl = slots[sc];
               const float wgt = sel_w[sl];
-              float* yr = yacc + t * ystride + tl * kTileRows;
-              yr[g] = fmaf(wgt, v0, yr[g]);
-              yr[g + 8] = fmaf(wgt, v1, yr[g + 8]);
+              const int ex = int(hes[sl * HES + kb]);
+              const float vlo = (d4[0] + d4[1]) * (wgt * block_factor(f.s_lo, ex));
+              const float vhi = (d4[2] + d4[3]) * (wgt * block_factor(f.s_hi, ex));
+              const int t = sl / k;
+#pragma unroll
+              for (int x = 0; x < kDecodeMaxTiles; ++x) {
+#pragma unroll
+                for (int tt = 0; tt < kDecodeMaxT; ++tt) {
+                  if (x == tl && tt == t) {
+                    dacc[x][tt][0] += vlo;
+                    dacc[x][tt][1] += vhi;
+                  }
+                }
+              }
             }
           }
         }
-        __syncthreads();
       }
     }
     // after the last router load: this CTA's logits are written
@@ -560,14 +606,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     __syncthreads();
     if (tid == 0 && i + a.stages < total) issue(i + a.stages);
   }
+  trace(12);
 
-  trace(9);
+  // cross-warp sum of the down accumulators, one output tile at a time; the
+  // four lanes of a quad hold the same two rows (different columns/slots)
+  for (int tl = 0; tl < s.ntl; ++tl) {
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxT; ++t) {
+#pragma unroll
+      for (int x = 0; x < kDecodeMaxTiles; ++x) {
+        if (x == tl) {
+          red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 0] = dacc[x][t][0];
+          red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 1] = dacc[x][t][1];
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < T * kTileRows) {
+      const int t = tid / kTileRows, r = tid % kTileRows;
+      const int gg = r & 7, half = r >> 3;
+      float v = 0.0f;
+      for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) v += red[((w * kDecodeMaxT + t) * 32 + gg * 4 + qq) * 2 + half];
+      yacc[t * ystride + tl * kTileRows + r] += v;
+    }
+    __syncthreads();
+  }
+
   // y rows of my tiles
   for (int j = tid; j < T * s.ntl * kTileRows; j += kThreads) {
     const int t = j / (s.ntl * kTileRows), r = j % (s.ntl * kTileRows);
     a.y[(size_t)t * d + s.t0 * kTileRows + r] = __float2bfloat16_rn(yacc[t * ystride + r]);
   }
   __syncthreads();
+  trace(10);
   if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(&st->done, 1u);
@@ -575,11 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       // last CTA of this call: every CTA is past every wait of this call
       st->bar = 0ull;
       st->shcnt = 0u;
+      st->gudone = 0u;
       __threadfence();
-      st_release_u32(&st->epoch, epoch);
     }
   }
-  trace(10);
 }
 
 }  // namespace
@@ -592,27 +664,33 @@ int decode_trace_copy(unsigned long long* host, int n_cta) {
 #endif
 
 size_t decode_state_bytes(int E, int I) {
-  return (size_t)kDecodeStateWords * 4 + 2 * (size_t)E * (I / kMxBlock) * 4;
+  (void)E;
+  (void)I;
+  return (size_t)kDecodeStateWords * 4;
 }
+
+uint32_t decode_he_stride(int I) { return he_stride(I); }
 
 int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t* slot_bytes,
                 uint32_t* smem_bytes) {
   if (a.T < 1 || a.T > kDecodeMaxT) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.d % 32 || a.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a.k < 1 || a.k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int NTd = a.d / kTileRows;
   if (di.sm_count < 1 || (NTd + di.sm_count - 1) / di.sm_count > kDecodeMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
   uint32_t sb = uint32_t(a.d / kMxBlock) * kUnitBytes;   // one routed gate/up tile
-  const uint32_t cands[3] = {uint32_t(4 * a.d), uint32_t(2 * a.I), uint32_t(a.I / kMxBlock) * kUnitBytes};
-  for (uint32_t v : cands) sb = sb > v ? sb : v;         // a shared feature, a shared-down row, a down unit
+  const uint32_t cands[4] = {uint32_t(2 * a.d), uint32_t(4 * a.d), uint32_t(2 * a.I),
+                             uint32_t(a.I / kMxBlock) * kUnitBytes};
+  for (uint32_t v : cands) sb = sb > v ? sb : v;         // router row, shared feature, shared-down row, down unit
   sb = align_up(sb, 128);
-  const Smem fixed = smem_plan(a.T, a.d, a.I, 0, sb);
+  const Smem fixed = smem_plan(a.T, a.d, a.I, a.k, 0, sb);
   const size_t budget = di.smem_optin > fixed.total + 1024 ? di.smem_optin - fixed.total - 1024 : 0;
   int S = int(budget / (sb + 8));
   if (S > kDecodeMaxStages) S = kDecodeMaxStages;
   if (S < 3) return MOE_ERR_UNSUPPORTED_SHAPE;
   *stages = S;
   *slot_bytes = sb;
-  *smem_bytes = smem_plan(a.T, a.d, a.I, S, sb).total;
+  *smem_bytes = smem_plan(a.T, a.d, a.I, a.k, S, sb).total;
   return MOE_OK;
 }
 

@@ -13,13 +13,13 @@ constexpr int kDecodeMaxTiles = 4;    // 16-row output tiles per CTA
 constexpr int kDecodeMaxStages = 16;
 constexpr int kDecodeStateWords = 16; // header words before the per-block counters
 
-// Cross-call synchronisation words at the start of the workspace (zero before
-// the first call). Followed by hcnt[E * I/32] and hready[E * I/32].
+// Synchronisation words at the start of the workspace (zero before the
+// first call; the last CTA of every call puts them back to zero).
 struct DecodeState {
-  unsigned long long bar;  // CTAs past their router rows (reset by the last CTA)
-  uint32_t epoch;          // calls completed
-  uint32_t done;           // CTAs finished (compared modulo the grid size)
-  uint32_t shcnt;          // CTAs whose shared gate/up slice is written (reset by the last CTA)
+  unsigned long long bar;  // CTAs past their router rows
+  uint32_t done;           // CTAs finished (compared modulo the grid size; never reset)
+  uint32_t shcnt;          // CTAs whose shared gate/up slice is written
+  uint32_t gudone;         // CTAs whose routed gate/up items are written
   uint32_t pad[11];
 };
 static_assert(sizeof(DecodeState) == kDecodeStateWords * 4, "state header size");
@@ -41,10 +41,8 @@ struct DecodeArgs {
   float* w_out;         // [T][k] or null
   __nv_bfloat16* y;     // [T][d]
   DecodeState* state;
-  uint32_t* state_words;
-  float* h;             // [T*k][I]
-  uint8_t* hB;          // [T*k][I/32][128]
-  int16_t* hE;          // [T*k][I/32]
+  uint8_t* hB;          // [T*k][I/32][96] e4m3 terms of h
+  int16_t* hE;          // [T*k][decode_he_stride(I)] block exponents of h
   float* h_sh;          // [T][I]
   int* status;
   int stages;           // set by launch_decode
@@ -52,6 +50,8 @@ struct DecodeArgs {
 };
 
 size_t decode_state_bytes(int E, int I);
+// Row stride (elements) of the h exponent array: I/32 rounded up to 8.
+uint32_t decode_he_stride(int I);
 // MOE_OK if the shape/T can take this path on this device.
 int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t* slot_bytes,
                 uint32_t* smem_bytes);

@@ -23,25 +23,16 @@
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "mma_tile.cuh"
 
 namespace moe {
 namespace {
-
-// floor(log2(a)) for finite a > 0 (fp32, including subnormals).
-__device__ __forceinline__ int floor_log2(float a) {
-  const uint32_t b = __float_as_uint(a);
-  const int e = int(b >> 23);
-  if (e > 0) return e - 127;
-  return (31 - __clz(int(b & 0x7FFFFFu))) - 149;
-}
 
 // One warp per (row, K-block): 32 values -> e4m3 terms hi, lo, lo2 with
 // value = (hi + lo + lo2) * 2^e, e chosen so the block maximum scaled by 2^-e
 // lies in [128, 256). The remainder after each term is exact in fp32, so three
 // terms carry 12 significant bits; bf16 inputs (8 bits) are reproduced exactly
 // except for elements more than 2^10 below their block maximum.
-// Term bytes are stored in MMA B-fragment order: within a term's 32 bytes,
-// lane q of a quad reads bytes [8q, 8q+8) = k {4q..4q+3, 16+4q..16+4q+3}.
 __global__ void __launch_bounds__(256)
 act_split_kernel(const void* __restrict__ src, int src_bf16, int rows, int K,
                  uint8_t* __restrict__ act_b, int16_t* __restrict__ act_e) {
@@ -55,24 +46,7 @@ act_split_kernel(const void* __restrict__ src, int src_bf16, int rows, int K,
     const long long off = row * K + (long long)kb * kMxBlock + lane;
     const float v = src_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(src)[off])
                              : static_cast<const float*>(src)[off];
-    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
-    uint32_t t0 = 0, t1 = 0, t2 = 0;
-    int e = kActZeroExp;
-    if (amax > 0.0f) {
-      e = floor_log2(amax) - 7;
-      const float sv = ldexpf(v, -e);
-      t0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
-      const float r1 = sv - e4m3_to_f32(t0);
-      t1 = f32x2_to_e4m3x2(r1, 0.0f) & 0xFFu;
-      const float r2 = r1 - e4m3_to_f32(t1);
-      t2 = f32x2_to_e4m3x2(r2, 0.0f) & 0xFFu;
-    }
-    const int pos = ((lane & 15) >> 2) * 8 + (lane >> 4) * 4 + (lane & 3);
-    uint8_t* dst = act_b + u * kActRowKbBytes;
-    dst[pos] = uint8_t(t0);
-    dst[32 + pos] = uint8_t(t1);
-    dst[64 + pos] = uint8_t(t2);
-    dst[96 + pos] = 0;
+    const int e = split_block(v, lane, act_b + u * kActRowKbBytes);
     if (lane == 0) act_e[u] = int16_t(e);
   }
 }
@@ -142,7 +116,7 @@ routed_kernel(RoutedArgs a, int stages, uint32_t item_bytes) {
         for (int pr = 0; pr < kPairs; ++pr) {
           if (c0 + 2 * pr >= n) break;
           uint2 bv = make_uint2(0u, 0u);
-          if (brow[pr] >= 0)
+          if (brow[pr] >= 0 && (g & 3) < kActTerms)
             bv = ldg_nc_u2(a.act_b + ((size_t)brow[pr] * a.KB + kb) * kActRowKbBytes + (g & 3) * 32 + q * 8);
           const int ex = crow[pr] >= 0 ? int(__ldg(a.act_e + (size_t)crow[pr] * a.KB + kb)) : int(kActZeroExp);
           float d[4];

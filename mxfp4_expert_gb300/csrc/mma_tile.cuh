@@ -45,8 +45,9 @@ __device__ __forceinline__ int floor_log2(float a) {
 }
 
 // Whole warp: lane j holds element j of a 32-element block. Writes the three
-// e4m3 terms (and a zero fourth) in B-fragment byte order to dst[0..128) and
-// returns the block exponent e (value = (t0 + t1 + t2) * 2^e), or kActZeroExp.
+// e4m3 terms in B-fragment byte order to dst[0..96) and returns the block
+// exponent e (value = (t0 + t1 + t2) * 2^e), or kActZeroExp. Within a term's
+// 32 bytes, lane q of a quad reads bytes [8q, 8q+8) = k {4q..4q+3, 16+4q..16+4q+3}.
 __device__ __forceinline__ int split_block(float v, int lane, uint8_t* dst) {
   const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
   uint32_t t0 = 0, t1 = 0, t2 = 0;
@@ -64,8 +65,15 @@ __device__ __forceinline__ int split_block(float v, int lane, uint8_t* dst) {
   dst[pos] = uint8_t(t0);
   dst[32 + pos] = uint8_t(t1);
   dst[64 + pos] = uint8_t(t2);
-  dst[96 + pos] = 0;
   return e;
+}
+
+// B-fragment of one (activation row, K-block) for this lane: column g&3 is
+// term g&3 (column 3 is zero), rows k {4q..4q+3} and {16+4q..16+4q+3}.
+__device__ __forceinline__ uint2 load_bfrag_smem(const uint8_t* blk, int lane) {
+  const int col = (lane >> 2) & 3, q = lane & 3;
+  if (col == 3) return make_uint2(0u, 0u);
+  return *reinterpret_cast<const uint2*>(blk + col * 32 + q * 8);
 }
 
 }  // namespace moe
