@@ -119,9 +119,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
 
 // 2^ex as fp32 for an unbiased exponent, including the subnormal/overflow ends.
 __device__ __forceinline__ float exp2i(int ex) {
-  int f = ex + 127;
+  const int f = ex + 127;
   if (f >= 1 && f <= 254) return __uint_as_float(uint32_t(f) << 23);
   return ldexpf(1.0f, ex);
+}
+// v * 2^ex, exact whenever the result is a normal fp32 number.
+__device__ __forceinline__ float scale2(float v, int ex) {
+  if (ex >= -126 && ex <= 127) return v * __uint_as_float(uint32_t(ex + 127) << 23);
+  return ldexpf(v, ex);
 }
 
 // Combined factor of one (weight row, K-block) x (activation row, K-block):

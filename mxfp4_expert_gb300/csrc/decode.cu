@@ -61,10 +61,11 @@ __device__ __forceinline__ void trace(int point) {
 __device__ __forceinline__ void trace(int) {}
 #endif
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
 constexpr int kRowsPerLoad = 8;   // max rows of a "few long rows" GEMV load (split-K over warps)
+constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 4096
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
   float s = bf16_lo(w.x) * bf16_lo(x.x);
@@ -102,35 +103,34 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
 // bf16 rows (row-major, K elements each, in shared memory) times T bf16
 // activation vectors (shared memory), split over all warps along K.
 // out[r * kDecodeMaxT + t] (shared) receives the dot products. n <= kRowsPerLoad.
-__device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfloat16* xs, int T,
+template <int T>
+__device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfloat16* xs,
                                float* red, float* out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunks = K / 8;
-  float acc[kRowsPerLoad][kDecodeMaxT];
+  float acc[kRowsPerLoad][T];
 #pragma unroll
   for (int r = 0; r < kRowsPerLoad; ++r)
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) acc[r][t] = 0.0f;
+    for (int t = 0; t < T; ++t) acc[r][t] = 0.0f;
   for (int j = tid; j < chunks; j += kThreads) {
-    uint4 xv[kDecodeMaxT];
+    uint4 xv[T];
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t)
-      if (t < T) xv[t] = reinterpret_cast<const uint4*>(xs + (size_t)t * K)[j];
+    for (int t = 0; t < T; ++t) xv[t] = reinterpret_cast<const uint4*>(xs + (size_t)t * K)[j];
 #pragma unroll
     for (int r = 0; r < kRowsPerLoad; ++r) {
       if (r < n) {
         const uint4 wv = reinterpret_cast<const uint4*>(rows + (size_t)r * K * 2)[j];
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t)
-          if (t < T) acc[r][t] += dot8_bf16(wv, xv[t]);
+        for (int t = 0; t < T; ++t) acc[r][t] += dot8_bf16(wv, xv[t]);
       }
     }
   }
 #pragma unroll
   for (int r = 0; r < kRowsPerLoad; ++r) {
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) {
-      if (r < n && t < T) {
+    for (int t = 0; t < T; ++t) {
+      if (r < n) {
         const float v = warp_sum(acc[r][t]);
         if (lane == 0) red[(warp * kRowsPerLoad + r) * kDecodeMaxT + t] = v;
       }
@@ -217,10 +217,12 @@ struct Seq {
   int bF, bSD, bGU, bDN;
 };
 
+template <int T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   trace(0);
-  const int T = a.T, d = a.d, I = a.I, E = a.E, k = a.k;
+  constexpr int kPairs = (T + 1) / 2;
+  const int d = a.d, I = a.I, E = a.E, k = a.k;
   const int KBd = d / kMxBlock, KBi = I / kMxBlock, HES = int(he_stride(I));
   const int NTd = d / kTileRows;
   const int G = gridDim.x, c = blockIdx.x;
@@ -338,12 +340,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
   }
 
-  // per-lane down accumulators: [tile][token][row g / row g+8]
-  float dacc[kDecodeMaxTiles][kDecodeMaxT][2];
+  // per-lane down accumulators of the current output tile: [token][row g / row g+8]
+  float dacc[T][2];
 #pragma unroll
-  for (int tl = 0; tl < kDecodeMaxTiles; ++tl)
+  for (int t = 0; t < T; ++t) dacc[t][0] = dacc[t][1] = 0.0f;
+  int dn_tile = -1;
+  // cross-warp sum of the down accumulators into y for output tile tl; the
+  // four lanes of a quad hold the same two rows (different columns/slots)
+  auto flush_tile = [&](int tl) {
 #pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) dacc[tl][t][0] = dacc[tl][t][1] = 0.0f;
+    for (int t = 0; t < T; ++t) {
+      red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 0] = dacc[t][0];
+      red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 1] = dacc[t][1];
+      dacc[t][0] = dacc[t][1] = 0.0f;
+    }
+    __syncthreads();
+    if (tid < T * kTileRows) {
+      const int t = tid / kTileRows, r = tid % kTileRows;
+      const int gg = r & 7, half = r >> 3;
+      float v = 0.0f;
+      for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) v += red[((w * kDecodeMaxT + t) * 32 + gg * 4 + qq) * 2 + half];
+      yacc[t * ystride + tl * kTileRows + r] += v;
+    }
+    __syncthreads();
+  };
 
   int total = s.bSD;
   for (int i = 0;; ++i) {
@@ -357,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         int e_sel;
         float w_sel;
         const float* brow = a.bias ? a.bias + (size_t)warp * a.bias_stride : nullptr;
-        warp_topk<32, true>(a.logits + (size_t)warp * E, brow, E, k, lane, &e_sel, &w_sel);
+        warp_topk<16, true>(a.logits + (size_t)warp * E, brow, E, k, lane, &e_sel, &w_sel);
         if (lane < k) {
           sel_e[warp * k + lane] = e_sel;
           sel_w[warp * k + lane] = w_sel;
@@ -467,13 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     if (ok && i < s.nR) {
       // ---- router rows -> logits ----------------------------------------------
       const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
-      gemv_bf16_rows(buf, n, d, xs, T, red, gout);
+      gemv_bf16_rows<T>(buf, n, d, xs, red, gout);
       if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T)
         a.logits[(size_t)(tid % kDecodeMaxT) * E + r + tid / kDecodeMaxT] = gout[tid];
     } else if (ok && i < s.bF) {
       // ---- shared gate/up rows -> h_sh -----------------------------------------
       const int f = s.f0 + (i - s.nR) * s.fch, n = min(s.fch, s.f1 - f);
-      gemv_bf16_rows(buf, 2 * n, d, xs, T, red, gout);   // rows 0..n-1 gate, n..2n-1 up
+      gemv_bf16_rows<T>(buf, 2 * n, d, xs, red, gout);   // rows 0..n-1 gate, n..2n-1 up
       if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T) {
         const int ff = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
         a.h_sh[(size_t)t * I + f + ff] = silu_f(gout[ff * kDecodeMaxT + t]) * gout[(n + ff) * kDecodeMaxT + t];
@@ -484,22 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
       for (int rr = warp; rr < n; rr += kWarps) {
         const uint4* wrow = reinterpret_cast<const uint4*>(buf + (size_t)rr * sdrow_bytes);
-        float acc[kDecodeMaxT];
+        float acc[T];
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < T; ++t) acc[t] = 0.0f;
         for (int j = lane; j < I / 8; j += 32) {
           const uint4 wv = wrow[j];
 #pragma unroll
-          for (int t = 0; t < kDecodeMaxT; ++t)
-            if (t < T) acc[t] += dot8_f32(wv, hsh + (size_t)t * I + j * 8);
+          for (int t = 0; t < T; ++t) acc[t] += dot8_f32(wv, hsh + (size_t)t * I + j * 8);
         }
         const int row_local = r + rr - s.t0 * kTileRows;
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxT; ++t) {
-          if (t < T) {
-            const float v = warp_sum(acc[t]);
-            if (lane == 0) yacc[t * ystride + row_local] = v;
-          }
+        for (int t = 0; t < T; ++t) {
+          const float v = warp_sum(acc[t]);
+          if (lane == 0) yacc[t * ystride + row_local] = v;
         }
       }
     } else if (ok && i < s.bGU) {
@@ -509,41 +528,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int ai = item / KBi, fb = item % KBi;
       const int nt = act_n[ai];
       const int* slots = act_slot + ai * kDecodeMaxT;
-      float acc[kPairsMax][2];
+      float acc[kPairs][2];
 #pragma unroll
-      for (int p = 0; p < kPairsMax; ++p) acc[p][0] = acc[p][1] = 0.0f;
-      for (int kb = warp; kb < KBd; kb += kWarps) {
-        const UnitFrag f = load_unit(buf + (size_t)kb * kUnitBytes, lane);
+      for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
 #pragma unroll
-        for (int p = 0; p < kPairsMax; ++p) {
-          if (2 * p >= nt) break;
-          const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-          const uint2 bv = sb < nt ? load_bfrag_smem(xb + ((size_t)(slots[sb] / k) * KBd + kb) * kActRowKbBytes, lane)
-                                   : make_uint2(0u, 0u);
-          const int ex = sc < nt ? int(xe[(slots[sc] / k) * KBd + kb]) : int(kActZeroExp);
-          unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
+      for (int jj = 0; jj < kMaxKbPerWarp; ++jj) {
+        const int kb = warp + jj * kWarps;
+        if (kb < KBd) {
+          const UnitFrag f = load_unit(buf + (size_t)kb * kUnitBytes, lane);
+#pragma unroll
+          for (int p = 0; p < kPairs; ++p) {
+            if (2 * p < nt) {
+              const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+              const uint2 bv = sb < nt ? load_bfrag_smem(xb + ((size_t)(slots[sb] / k) * KBd + kb) * kActRowKbBytes, lane)
+                                       : make_uint2(0u, 0u);
+              const int ex = sc < nt ? int(xe[(slots[sc] / k) * KBd + kb]) : int(kActZeroExp);
+              unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
+            }
+          }
         }
       }
 #pragma unroll
-      for (int p = 0; p < kPairsMax; ++p) {
+      for (int p = 0; p < kPairs; ++p) {
         red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
         red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
       }
       __syncthreads();
       if (warp == 0) {
 #pragma unroll
-        for (int p = 0; p < kPairsMax; ++p) {
-          if (2 * p >= nt) break;
-          float v0 = 0.0f, v1 = 0.0f;
+        for (int p = 0; p < kPairs; ++p) {
+          if (2 * p < nt) {
+            float v0 = 0.0f, v1 = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
-            v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
+            for (int w = 0; w < kWarps; ++w) {
+              v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
+              v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
+            }
+            v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+            v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+            const int sc = 2 * p + (q >> 1);
+            if ((q & 1) == 0 && sc < nt) hblk[sc * 32 + sub * 8 + g] = silu_f(v0) * v1;
           }
-          v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
-          v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
-          const int sc = 2 * p + (q >> 1);
-          if ((q & 1) == 0 && sc < nt) hblk[sc * 32 + sub * 8 + g] = silu_f(v0) * v1;
         }
       }
       __syncthreads();
@@ -558,33 +583,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
       for (int j = 0; j < n; ++j) {
         const int u = u0 + j, tl = u / s.D, ai = u % s.D;
+        if (tl != dn_tile) {
+          if (dn_tile >= 0) flush_tile(dn_tile);
+          dn_tile = tl;
+        }
         const int nt = act_n[ai];
         const int* slots = act_slot + ai * kDecodeMaxT;
         const uint8_t* ubuf = buf + (size_t)j * U_dn;
         for (int kb = warp; kb < KBi; kb += kWarps) {
           const UnitFrag f = load_unit(ubuf + (size_t)kb * kUnitBytes, lane);
 #pragma unroll
-          for (int p = 0; p < kPairsMax; ++p) {
-            if (2 * p >= nt) break;
-            const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-            const uint2 bv = sb < nt ? load_bfrag_smem(hbs + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes, lane)
-                                     : make_uint2(0u, 0u);
-            float d4[4];
-            mma_e4m3(d4, f.a0, f.a1, f.a2, f.a3, bv.x, bv.y);
-            if (sc < nt) {
-              const int sl = slots[sc];
-              const float wgt = sel_w[sl];
-              const int ex = int(hes[sl * HES + kb]);
-              const float vlo = (d4[0] + d4[1]) * (wgt * block_factor(f.s_lo, ex));
-              const float vhi = (d4[2] + d4[3]) * (wgt * block_factor(f.s_hi, ex));
-              const int t = sl / k;
+          for (int p = 0; p < kPairs; ++p) {
+            if (2 * p < nt) {
+              const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+              const uint2 bv = sb < nt ? load_bfrag_smem(hbs + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes, lane)
+                                       : make_uint2(0u, 0u);
+              float d4[4];
+              mma_e4m3(d4, f.a0, f.a1, f.a2, f.a3, bv.x, bv.y);
+              if (sc < nt) {
+                const int sl = slots[sc];
+                const float wgt = sel_w[sl];
+                const int ex = int(hes[sl * HES + kb]);
+                const float vlo = (d4[0] + d4[1]) * (wgt * block_factor(f.s_lo, ex));
+                const float vhi = (d4[2] + d4[3]) * (wgt * block_factor(f.s_hi, ex));
+                const int t = sl / k;
 #pragma unroll
-              for (int x = 0; x < kDecodeMaxTiles; ++x) {
-#pragma unroll
-                for (int tt = 0; tt < kDecodeMaxT; ++tt) {
-                  if (x == tl && tt == t) {
-                    dacc[x][tt][0] += vlo;
-                    dacc[x][tt][1] += vhi;
+                for (int tt = 0; tt < T; ++tt) {
+                  if (tt == t) {
+                    dacc[tt][0] += vlo;
+                    dacc[tt][1] += vhi;
                   }
                 }
               }
@@ -608,31 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   }
   trace(12);
 
-  // cross-warp sum of the down accumulators, one output tile at a time; the
-  // four lanes of a quad hold the same two rows (different columns/slots)
-  for (int tl = 0; tl < s.ntl; ++tl) {
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) {
-#pragma unroll
-      for (int x = 0; x < kDecodeMaxTiles; ++x) {
-        if (x == tl) {
-          red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 0] = dacc[x][t][0];
-          red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 1] = dacc[x][t][1];
-        }
-      }
-    }
-    __syncthreads();
-    if (tid < T * kTileRows) {
-      const int t = tid / kTileRows, r = tid % kTileRows;
-      const int gg = r & 7, half = r >> 3;
-      float v = 0.0f;
-      for (int w = 0; w < kWarps; ++w)
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) v += red[((w * kDecodeMaxT + t) * 32 + gg * 4 + qq) * 2 + half];
-      yacc[t * ystride + tl * kTileRows + r] += v;
-    }
-    __syncthreads();
-  }
+  if (dn_tile >= 0) flush_tile(dn_tile);
 
   // y rows of my tiles
   for (int j = tid; j < T * s.ntl * kTileRows; j += kThreads) {
@@ -676,6 +679,7 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t
   if (a.T < 1 || a.T > kDecodeMaxT) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.d % 32 || a.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.k < 1 || a.k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a.E > 512 || a.d > kWarps * kMaxKbPerWarp * kMxBlock) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int NTd = a.d / kTileRows;
   if (di.sm_count < 1 || (NTd + di.sm_count - 1) / di.sm_count > kDecodeMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
   uint32_t sb = uint32_t(a.d / kMxBlock) * kUnitBytes;   // one routed gate/up tile
@@ -694,13 +698,11 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t
   return MOE_OK;
 }
 
-int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s) {
-  uint32_t smem = 0;
-  int st = decode_plan(a, di, &a.stages, &a.slot_bytes, &smem);
-  if (st != MOE_OK) return st;
-  MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+template <int T>
+int launch_decode_t(DecodeArgs a, uint32_t smem, const DeviceInfo& di, cudaStream_t s) {
+  MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
   int per_sm = 0;
-  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem));
+  MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, kThreads, smem));
   if (per_sm < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(di.sm_count);
@@ -712,8 +714,20 @@ int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_kernel, a));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_kernel<T>, a));
   return MOE_OK;
+}
+
+int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s) {
+  uint32_t smem = 0;
+  int st = decode_plan(a, di, &a.stages, &a.slot_bytes, &smem);
+  if (st != MOE_OK) return st;
+  switch (a.T) {
+    case 1: return launch_decode_t<1>(a, smem, di, s);
+    case 2: return launch_decode_t<2>(a, smem, di, s);
+    case 3: return launch_decode_t<3>(a, smem, di, s);
+    default: return launch_decode_t<4>(a, smem, di, s);
+  }
 }
 
 }  // namespace moe

@@ -54,7 +54,7 @@ __device__ __forceinline__ int split_block(float v, int lane, uint8_t* dst) {
   int e = kActZeroExp;
   if (amax > 0.0f) {
     e = floor_log2(amax) - 7;
-    const float sv = ldexpf(v, -e);
+    const float sv = scale2(v, -e);
     t0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
     const float r1 = sv - e4m3_to_f32(t0);
     t1 = f32x2_to_e4m3x2(r1, 0.0f) & 0xFFu;
