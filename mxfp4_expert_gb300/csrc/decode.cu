@@ -61,11 +61,24 @@ __device__ __forceinline__ void trace(int point) {
 __device__ __forceinline__ void trace(int) {}
 #endif
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 15;                  // compute warps
+constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp that issues the bulk copies
+constexpr int kComputeThreads = kWarps * 32;
 constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
 constexpr int kRowsPerLoad = 8;   // max rows of a "few long rows" GEMV load (split-K over warps)
-constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 4096
+constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 3840
+
+// Barrier among the compute warps only (the producer warp never joins it).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory"); }
+__device__ __forceinline__ bool csync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(uint32_t(v)), "n"(kComputeThreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
   float s = bf16_lo(w.x) * bf16_lo(x.x);
@@ -113,7 +126,7 @@ __device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfl
   for (int r = 0; r < kRowsPerLoad; ++r)
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[r][t] = 0.0f;
-  for (int j = tid; j < chunks; j += kThreads) {
+  for (int j = tid; j < chunks; j += kComputeThreads) {
     uint4 xv[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) xv[t] = reinterpret_cast<const uint4*>(xs + (size_t)t * K)[j];
@@ -136,7 +149,7 @@ __device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfl
       }
     }
   }
-  __syncthreads();
+  csync();
   if (tid < n * kDecodeMaxT) {
     const int r = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
     float v = 0.0f;
@@ -145,7 +158,7 @@ __device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfl
       for (int w = 0; w < kWarps; ++w) v += red[(w * kRowsPerLoad + r) * kDecodeMaxT + t];
     out[tid] = v;
   }
-  __syncthreads();
+  csync();
 }
 
 // Shared-memory carve-up (byte offsets), identical on host and device. The
@@ -167,7 +180,7 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages
     return here;
   };
   s.ring = take(uint32_t(stages) * slot_bytes, 128);
-  s.bars = take(8u * uint32_t(stages + 1), 8);
+  s.bars = take(8u * uint32_t(2 * stages + 2), 8);   // full[S], empty[S], h staging, routing
   // overlay: phase A layout
   const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
   const uint32_t xb_b = align_up(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
@@ -231,7 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const Smem L = smem_plan(T, d, I, k, a.stages, a.slot_bytes);
   uint8_t* ring = sm + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
-  uint64_t* hbar = full + a.stages;
+  uint64_t* empty = full + a.stages;
+  uint64_t* hbar = empty + a.stages;
+  uint64_t* rbar = hbar + 1;
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
   uint8_t* xb = sm + L.xb;
   int16_t* xe = reinterpret_cast<int16_t*>(sm + L.xe);
@@ -313,21 +328,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   };
 
   if (tid == 0) {
-    for (int i = 0; i <= a.stages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < 2 * a.stages + 2; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
-    for (int i = 0; i < a.stages && i < s.bSD; ++i) issue(i);
   }
+  __syncthreads();   // the only full-CTA barrier: barriers initialised
+
+  if (warp == kWarps) {
+    // ---- producer warp: issues every bulk copy, in load order ----------------
+    if (lane == 0) {
+      int n_loads = s.bSD;
+      for (int j = 0; j < n_loads || j == s.bSD; ++j) {
+        if (j == s.bSD) {
+          // phase B is known once the compute warps have routed
+          if (!mbar_wait(rbar, 0u, a.status)) break;
+          s.D = misc[0];
+          s.i0 = misc[1];
+          s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
+          s.nDN = (s.ntl * s.D + s.dnch - 1) / s.dnch;
+          s.bGU = s.bSD + 4 * (s.i1 - s.i0);
+          s.bDN = s.bGU + s.nDN;
+          n_loads = s.bDN;
+          if (j >= n_loads) break;
+        }
+        if (j >= a.stages && !mbar_wait(&empty[j % a.stages], uint32_t(j / a.stages - 1) & 1u, a.status)) break;
+        issue(j);
+      }
+    }
+    return;
+  }
+
   // activations: bf16 copy for the CUDA-core GEMVs, then e4m3 terms for the MMAs
-  for (int i = tid; i < T * d / 8; i += kThreads)
+  for (int i = tid; i < T * d / 8; i += kComputeThreads)
     reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
-  for (int i = tid; i < T * ystride; i += kThreads) yacc[i] = 0.0f;
-  __syncthreads();
+  for (int i = tid; i < T * ystride; i += kComputeThreads) yacc[i] = 0.0f;
+  csync();
   for (int u = warp; u < T * KBd; u += kWarps) {
     const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
     const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
     if (lane == 0) xe[u] = int16_t(ex);
   }
-  __syncthreads();
+  csync();
   trace(1);
   if (tid == 0) {
     if (s.nR == 0) {
@@ -354,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 1] = dacc[t][1];
       dacc[t][0] = dacc[t][1] = 0.0f;
     }
-    __syncthreads();
+    csync();
     if (tid < T * kTileRows) {
       const int t = tid / kTileRows, r = tid % kTileRows;
       const int gg = r & 7, half = r >> 3;
@@ -364,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int qq = 0; qq < 4; ++qq) v += red[((w * kDecodeMaxT + t) * 32 + gg * 4 + qq) * 2 + half];
       yacc[t * ystride + tl * kTileRows + r] += v;
     }
-    __syncthreads();
+    csync();
   };
 
   int total = s.bSD;
@@ -373,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       // ---- routing: every CTA has written its router rows -------------------
       trace(3);
       if (tid == 0) wait_geq_u64(&st->bar, (unsigned long long)G, a.status);
-      __syncthreads();
+      csync();
       trace(4);
       if (warp < T) {
         int e_sel;
@@ -389,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           }
         }
       }
-      __syncthreads();
+      csync();
       trace(11);
       // active experts ascending; each with its slots (slot = t*k + j) in token order
       const int n = T * k;
@@ -399,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int j = 0; j < tid; ++j) f &= sel_e[j] != e ? 1 : 0;
         first[tid] = f;
       }
-      __syncthreads();
+      csync();
       if (tid < n) {
         const int e = sel_e[tid];
         int rank = 0, pos = 0, cnt = 0;
@@ -442,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         misc[1] = cut(c);
         misc[2] = cut(c + 1);
       }
-      __syncthreads();
+      csync();
       s.D = misc[0];
       s.i0 = misc[1];
       s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
@@ -450,16 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       s.bGU = s.bSD + 4 * (s.i1 - s.i0);
       s.bDN = s.bGU + s.nDN;
       total = s.bDN;
-      if (tid == 0)   // phase-B loads that fit in the ring now
-        for (int j = s.bSD; j < total && j < s.bF + a.stages; ++j) issue(j);
+      if (tid == 0) mbar_arrive(rbar);   // hands phase B to the producer warp
       trace(5);
       if (s.nSD > 0) {
         // shared down needs every CTA's slice of h_sh
         if (tid == 0) wait_geq_u32(&st->shcnt, uint32_t(G), a.status);
-        __syncthreads();
-        for (int j = tid; j < T * I; j += kThreads) hsh[j] = __ldcg(a.h_sh + j);
+        csync();
+        for (int j = tid; j < T * I; j += kComputeThreads) hsh[j] = __ldcg(a.h_sh + j);
       }
-      __syncthreads();
+      csync();
       trace(6);
     }
     if (i == s.bSD) trace(7);
@@ -476,16 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         bulk_g2s(hbs, a.hB, hb_bytes, hbar);
         bulk_g2s(hes, a.hE, he_bytes, hbar);
       }
-      __syncthreads();
+      csync();
       mbar_wait(hbar, 0u, a.status);
-      __syncthreads();
+      csync();
       trace(9);
     }
     if (i >= total) break;
 
     const int slot = i % a.stages;
     const uint8_t* buf = ring + (size_t)slot * a.slot_bytes;
-    const bool ok = __syncthreads_and(mbar_wait(&full[slot], uint32_t(i / a.stages) & 1u, a.status));
+    const bool ok = csync_and(mbar_wait(&full[slot], uint32_t(i / a.stages) & 1u, a.status));
     if (ok && i < s.nR) {
       // ---- router rows -> logits ----------------------------------------------
       const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
@@ -553,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
         red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
       }
-      __syncthreads();
+      csync();
       if (warp == 0) {
 #pragma unroll
         for (int p = 0; p < kPairs; ++p) {
@@ -571,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           }
         }
       }
-      __syncthreads();
+      csync();
       if (sub == 3 && warp < nt) {
         // the item's 32 features are complete: write them as e4m3 terms
         const int sl = slots[warp];
@@ -630,19 +669,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       __threadfence();
       atomicAdd(&st->shcnt, 1u);
     }
-    __syncthreads();
-    if (tid == 0 && i + a.stages < total) issue(i + a.stages);
+    csync();
+    if (tid == 0) mbar_arrive(&empty[slot]);   // slot free for load i + stages
   }
   trace(12);
 
   if (dn_tile >= 0) flush_tile(dn_tile);
 
   // y rows of my tiles
-  for (int j = tid; j < T * s.ntl * kTileRows; j += kThreads) {
+  for (int j = tid; j < T * s.ntl * kTileRows; j += kComputeThreads) {
     const int t = j / (s.ntl * kTileRows), r = j % (s.ntl * kTileRows);
     a.y[(size_t)t * d + s.t0 * kTileRows + r] = __float2bfloat16_rn(yacc[t * ystride + r]);
   }
-  __syncthreads();
+  csync();
   trace(10);
   if (tid == 0) {
     __threadfence();
