@@ -78,7 +78,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // ---- loads ----------------------------------------------------------------
 __device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint4 ldg_nc_stream_u4(const void* p) {
@@ -92,7 +92,7 @@ __device__ __forceinline__ uint4 ldg_nc_stream_u4(const void* p) {
 // ---- e4m3 warp MMA: D[16x8] = A[16x32] * B[32x8], fp32 accumulate from 0 ----
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%10,%10,%10,%10};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

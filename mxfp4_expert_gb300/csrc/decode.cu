@@ -57,8 +57,18 @@ __device__ __forceinline__ void trace(int point) {
     g_trace[blockIdx.x][point] = t;
   }
 }
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_put(int point, unsigned long long v) {
+  if (threadIdx.x == 0) g_trace[blockIdx.x][point] = v;
+}
 #else
 __device__ __forceinline__ void trace(int) {}
+__device__ __forceinline__ unsigned long long gtime() { return 0; }
+__device__ __forceinline__ void trace_put(int, unsigned long long) {}
 #endif
 
 constexpr int kWarps = 15;                  // compute warps
@@ -166,7 +176,7 @@ __device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfl
 // one region: the former are dead once the down units start.
 struct Smem {
   uint32_t ring, bars, ov, xs, xb, xe, hsh, hbs, hes, hblk, yacc, red, gout, sel_e, sel_w, act, act_n,
-      act_slot, first, misc, total;
+      act_slot, act_tok, first, misc, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline uint32_t he_stride(int I) { return align_up(uint32_t(I / kMxBlock), 8); }
@@ -180,7 +190,7 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages
     return here;
   };
   s.ring = take(uint32_t(stages) * slot_bytes, 128);
-  s.bars = take(8u * uint32_t(2 * stages + 2), 8);   // full[S], empty[S], h staging, routing
+  s.bars = take(8u * uint32_t(2 * stages + 3), 8);   // full[S], empty[S], h staging, routing, x
   // overlay: phase A layout
   const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
   const uint32_t xb_b = align_up(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
@@ -213,6 +223,7 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages
   s.act = take(kDecodeMaxT * 32 * 4, 4);
   s.act_n = take(kDecodeMaxT * 32 * 4, 4);
   s.act_slot = take(kDecodeMaxT * 32 * kDecodeMaxT * 4, 4);
+  s.act_tok = take(kDecodeMaxT * 32 * kDecodeMaxT * 4, 4);
   s.first = take(kDecodeMaxT * 32 * 4, 4);
   s.misc = take(16 * 4, 8);
   s.total = at;
@@ -247,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   uint64_t* empty = full + a.stages;
   uint64_t* hbar = empty + a.stages;
   uint64_t* rbar = hbar + 1;
+  uint64_t* xbar = rbar + 1;
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
   uint8_t* xb = sm + L.xb;
   int16_t* xe = reinterpret_cast<int16_t*>(sm + L.xe);
@@ -262,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   int* act = reinterpret_cast<int*>(sm + L.act);
   int* act_n = reinterpret_cast<int*>(sm + L.act_n);
   int* act_slot = reinterpret_cast<int*>(sm + L.act_slot);
+  int* act_tok = reinterpret_cast<int*>(sm + L.act_tok);   // token of each act_slot entry
   int* first = reinterpret_cast<int*>(sm + L.first);
   int* misc = reinterpret_cast<int*>(sm + L.misc);
 
@@ -328,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   };
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * a.stages + 2; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < 2 * a.stages + 3; ++i) mbar_init(&full[i], 1);
     mbar_fence_init();
   }
   __syncthreads();   // the only full-CTA barrier: barriers initialised
@@ -336,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   if (warp == kWarps) {
     // ---- producer warp: issues every bulk copy, in load order ----------------
     if (lane == 0) {
+      // the activations first, so they are not queued behind the weights
+      mbar_arrive_expect_tx(xbar, uint32_t(T) * d * 2);
+      bulk_g2s(xs, a.x, uint32_t(T) * d * 2, xbar);
       int n_loads = s.bSD;
       for (int j = 0; j < n_loads || j == s.bSD; ++j) {
         if (j == s.bSD) {
@@ -353,20 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         if (j >= a.stages && !mbar_wait(&empty[j % a.stages], uint32_t(j / a.stages - 1) & 1u, a.status)) break;
         issue(j);
       }
+#ifdef MOE_DECODE_TRACE
+      g_trace[blockIdx.x][15] = gtime();
+#endif
     }
     return;
   }
 
-  // activations: bf16 copy for the CUDA-core GEMVs, then e4m3 terms for the MMAs
-  for (int i = tid; i < T * d / 8; i += kComputeThreads)
-    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
   for (int i = tid; i < T * ystride; i += kComputeThreads) yacc[i] = 0.0f;
-  csync();
-  for (int u = warp; u < T * KBd; u += kWarps) {
-    const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
-    const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
-    if (lane == 0) xe[u] = int16_t(ex);
-  }
+  mbar_wait(xbar, 0u, a.status);   // bf16 activations for the CUDA-core GEMVs
   csync();
   trace(1);
   if (tid == 0) {
@@ -408,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   };
 
   int total = s.bSD;
+  unsigned long long t_wait = 0, t_gu = 0;   // debug builds: time waiting for loads / in gate-up tiles
   for (int i = 0;; ++i) {
     if (i == s.bF) {
       // ---- routing: every CTA has written its router rows -------------------
@@ -427,6 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
             if (a.idx_out) a.idx_out[warp * k + lane] = e_sel;
             if (a.w_out) a.w_out[warp * k + lane] = w_sel;
           }
+        }
+      } else {
+        // meanwhile the other warps turn the activations into e4m3 terms
+        for (int u = warp - T; u < T * KBd; u += kWarps - T) {
+          const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
+          const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
+          if (lane == 0) xe[u] = int16_t(ex);
         }
       }
       csync();
@@ -450,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           cnt += ej == e ? 1 : 0;
         }
         act_slot[rank * kDecodeMaxT + pos] = tid;
+        act_tok[rank * kDecodeMaxT + pos] = tid / k;
         if (first[tid]) {
           act[rank] = e;
           act_n[rank] = cnt;
@@ -524,7 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 
     const int slot = i % a.stages;
     const uint8_t* buf = ring + (size_t)slot * a.slot_bytes;
+    const unsigned long long tw0 = gtime();
     const bool ok = csync_and(mbar_wait(&full[slot], uint32_t(i / a.stages) & 1u, a.status));
+    const unsigned long long tw1 = gtime();
+    t_wait += tw1 - tw0;
     if (ok && i < s.nR) {
       // ---- router rows -> logits ----------------------------------------------
       const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
@@ -567,6 +590,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int ai = item / KBi, fb = item % KBi;
       const int nt = act_n[ai];
       const int* slots = act_slot + ai * kDecodeMaxT;
+      const int* toks = act_tok + ai * kDecodeMaxT;
+      // lane-invariant-over-K operand offsets: B rows (token, term column), exponent rows
+      int boff[kPairs], eoff[kPairs];
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+        boff[p] = (sb < nt && (g & 3) < kActTerms) ? toks[sb] * KBd * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
+        eoff[p] = sc < nt ? toks[sc] * KBd : -1;
+      }
       float acc[kPairs][2];
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
@@ -578,10 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
           for (int p = 0; p < kPairs; ++p) {
             if (2 * p < nt) {
-              const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-              const uint2 bv = sb < nt ? load_bfrag_smem(xb + ((size_t)(slots[sb] / k) * KBd + kb) * kActRowKbBytes, lane)
-                                       : make_uint2(0u, 0u);
-              const int ex = sc < nt ? int(xe[(slots[sc] / k) * KBd + kb]) : int(kActZeroExp);
+              const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kb * kActRowKbBytes)
+                                            : make_uint2(0u, 0u);
+              const int ex = eoff[p] >= 0 ? int(xe[eoff[p] + kb]) : int(kActZeroExp);
               unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
             }
           }
@@ -624,31 +655,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const int u = u0 + j, tl = u / s.D, ai = u % s.D;
         if (tl != dn_tile) {
           if (dn_tile >= 0) flush_tile(dn_tile);
+  trace_put(13, t_wait);
+  trace_put(14, t_gu);
           dn_tile = tl;
         }
         const int nt = act_n[ai];
         const int* slots = act_slot + ai * kDecodeMaxT;
+        const int* toks = act_tok + ai * kDecodeMaxT;
         const uint8_t* ubuf = buf + (size_t)j * U_dn;
+        int boff[kPairs], eoff[kPairs], tok[kPairs];
+        float wgt[kPairs];
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+          boff[p] = (sb < nt && (g & 3) < kActTerms) ? slots[sb] * KBi * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
+          eoff[p] = sc < nt ? slots[sc] * HES : -1;
+          tok[p] = sc < nt ? toks[sc] : -1;
+          wgt[p] = sc < nt ? sel_w[slots[sc]] : 0.0f;
+        }
         for (int kb = warp; kb < KBi; kb += kWarps) {
           const UnitFrag f = load_unit(ubuf + (size_t)kb * kUnitBytes, lane);
 #pragma unroll
           for (int p = 0; p < kPairs; ++p) {
             if (2 * p < nt) {
-              const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-              const uint2 bv = sb < nt ? load_bfrag_smem(hbs + ((size_t)slots[sb] * KBi + kb) * kActRowKbBytes, lane)
-                                       : make_uint2(0u, 0u);
+              const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(hbs + boff[p] + kb * kActRowKbBytes)
+                                            : make_uint2(0u, 0u);
               float d4[4];
               mma_e4m3(d4, f.a0, f.a1, f.a2, f.a3, bv.x, bv.y);
-              if (sc < nt) {
-                const int sl = slots[sc];
-                const float wgt = sel_w[sl];
-                const int ex = int(hes[sl * HES + kb]);
-                const float vlo = (d4[0] + d4[1]) * (wgt * block_factor(f.s_lo, ex));
-                const float vhi = (d4[2] + d4[3]) * (wgt * block_factor(f.s_hi, ex));
-                const int t = sl / k;
+              if (eoff[p] >= 0) {
+                const int ex = int(hes[eoff[p] + kb]);
+                const float vlo = (d4[0] + d4[1]) * (wgt[p] * block_factor(f.s_lo, ex));
+                const float vhi = (d4[2] + d4[3]) * (wgt[p] * block_factor(f.s_hi, ex));
 #pragma unroll
                 for (int tt = 0; tt < T; ++tt) {
-                  if (tt == t) {
+                  if (tt == tok[p]) {
                     dacc[tt][0] += vlo;
                     dacc[tt][1] += vhi;
                   }
@@ -659,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
       }
     }
+    if (i >= s.bSD && i < s.bGU) t_gu += gtime() - tw1;
     // after the last router load: this CTA's logits are written
     if (i == s.nR - 1) trace(2);
     if (i == s.nR - 1 && tid == 0) {
@@ -675,6 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   trace(12);
 
   if (dn_tile >= 0) flush_tile(dn_tile);
+  trace_put(13, t_wait);
+  trace_put(14, t_gu);
 
   // y rows of my tiles
   for (int j = tid; j < T * s.ntl * kTileRows; j += kComputeThreads) {
