@@ -52,15 +52,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: returns false (and sets MOE_DEV_TIMEOUT) if the phase never
-// completes within kSpinBudget cycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+// completes within kSpinBudget cycles. Between polls the thread sleeps for
+// sleep_ns, so waiting warps leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, unsigned sleep_ns = 32) {
   if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kSpinBudget) {
       if (status) atomicOr(status, MOE_DEV_TIMEOUT);
       return false;
     }
+    __nanosleep(sleep_ns);
   }
   return true;
 }

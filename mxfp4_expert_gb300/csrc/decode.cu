@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       for (int j = 0; j < n_loads || j == s.bSD; ++j) {
         if (j == s.bSD) {
           // phase B is known once the compute warps have routed
-          if (!mbar_wait(rbar, 0u, a.status)) break;
+          if (!mbar_wait(rbar, 0u, a.status, 256)) break;
           s.D = misc[0];
           s.i0 = misc[1];
           s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           n_loads = s.bDN;
           if (j >= n_loads) break;
         }
-        if (j >= a.stages && !mbar_wait(&empty[j % a.stages], uint32_t(j / a.stages - 1) & 1u, a.status)) break;
+        if (j >= a.stages && !mbar_wait(&empty[j % a.stages], uint32_t(j / a.stages - 1) & 1u, a.status, 256)) break;
         issue(j);
       }
 #ifdef MOE_DECODE_TRACE
