@@ -21,8 +21,9 @@
  *
  * Conventions for every entry point
  *   - Pointers ending in a device buffer are device pointers owned by the
- *     caller; the library allocates no device memory and keeps no mutable
- *     global state. Host pointers are marked "host".
+ *     caller; the library allocates no device memory. The one piece of
+ *     mutable global state is the fixed scratch array behind
+ *     moe_forward_static_scratch. Host pointers are marked "host".
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream). Nothing synchronises the host.
  *   - Return value: MOE_OK (0) or a negative moe_status. Arguments are
@@ -235,6 +236,46 @@ int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
                 void* workspace_dev, size_t workspace_bytes, int* dev_status,
                 void* const* stage_events, int n_stage_events,
                 moe_stream_t stream);
+
+/* Size in bytes of the scratch array inside the library that
+ * moe_forward_static_scratch uses instead of a caller's workspace. */
+#define MOE_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/* moe_forward for callers that cannot allocate device memory.
+ *
+ * Source: none. The paper has no counterpart to this call; it is a library
+ * service, and the layer it computes is exactly moe_forward's.
+ *
+ * Who needs it: code that runs inside a host program whose memory manager
+ * has already reserved the device memory (a further cudaMalloc fails, or
+ * escapes that manager's accounting), and latency-critical loops that cannot
+ * afford the device-wide synchronisation cudaMalloc and cudaFree may cause.
+ * Such callers have no way to provide moe_forward's workspace.
+ *
+ * Instead of a workspace this call uses a MOE_STATIC_SCRATCH_BYTES array that
+ * is part of the library's device image (one per device). It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments are those of moe_forward without workspace and stage events.
+ *
+ *   - Set-up: the first call on each device, with that device current, looks
+ *     up the array's device address (cudaGetSymbolAddress) and keeps it.
+ *     Make that first call before any stream capture begins on the device.
+ *   - Each call first clears, on `stream`, the counters at the head of the
+ *     array that must read zero when its kernels start. No earlier call has to
+ *     have finished cleanly.
+ *   - All calls on one device share the array. Calls that can overlap in
+ *     time (on different streams, or from host threads with no ordering
+ *     between them) race on it and corrupt each other's results: put them on
+ *     one stream or order them with events.
+ *   - Returns MOE_ERR_WORKSPACE_TOO_SMALL, with nothing enqueued, when
+ *     moe_workspace_bytes(&L->shape, T) > MOE_STATIC_SCRATCH_BYTES (at
+ *     d = 2560, I = 768, E = 512, k = 8 that is T > 16). Larger calls need
+ *     moe_forward with a workspace of their own. */
+int moe_forward_static_scratch(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                               const float* bias_dev, int bias_row_stride,
+                               float* logits_out, int32_t* idx_out, float* w_out,
+                               int* dev_status, moe_stream_t stream);
 
 /* Comma-separated names of the stages of `path` in launch order (the
  * boundaries moe_forward's stage_events mark); NULL for an unknown path. */

@@ -19,7 +19,7 @@ __all__ = [
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
-    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
 # MOE_MXFP4_LIB may name another build of the same library (e.g. a debug build).
@@ -31,6 +31,7 @@ MOE_LAYOUT_MMA16_GATEUP = 2
 MOE_PATH_DECODE_MMA = 1
 MOE_PATH_DECODE_FUSED = 2
 DEV_NONFINITE_INPUT, DEV_SCALE_RANGE, DEV_INDEX_OOB, DEV_TIMEOUT = 1, 2, 4, 8
+STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 
 class MoeError(RuntimeError):
@@ -77,6 +78,7 @@ def _load():
         "moe_query_path": (i32, [ctypes.POINTER(moe_shape), i32]),
         "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
                                 ctypes.POINTER(ctypes.c_void_p), i32, vp]),
+        "moe_forward_static_scratch": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, vp]),
         "moe_stage_names": (ctypes.c_char_p, [i32]),
         "moe_selftest_bounded_wait": (i32, [vp, ctypes.c_uint32, ctypes.c_longlong, vp, vp]),
         "moe_status_string": (ctypes.c_char_p, [i32]),
@@ -290,4 +292,27 @@ def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
                            _p(idx_out), _p(w_out), _p(workspace), workspace.numel(), _p(dev_status),
                            ev_arr, n_ev, _s(stream)),
            "moe_forward")
+    return y
+
+
+def moe_forward_static_scratch(layer: Layer, x: torch.Tensor, y: torch.Tensor, bias: torch.Tensor | None = None,
+                               logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
+                               w_out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                               stream=None):
+    """y = layer(x) without a workspace and without allocating: the library's
+    fixed device scratch array (STATIC_SCRATCH_BYTES per device) stands in
+    for it. y (bf16 [T, d]) is the caller's. Calls on one device share that
+    array, so calls that may overlap in time must be ordered by the caller;
+    the first call on a device should come before any stream capture.
+    """
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(y, torch.bfloat16, "y")
+    T = x.shape[0]
+    stride = 0
+    if bias is not None:
+        _cuda(bias, torch.float32, "bias")
+        stride = 0 if bias.dim() == 1 else bias.shape[1]
+    _check(lib.moe_forward_static_scratch(ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride,
+                                          _p(logits_out), _p(idx_out), _p(w_out), _p(dev_status), _s(stream)),
+           "moe_forward_static_scratch")
     return y

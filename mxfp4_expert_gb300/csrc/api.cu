@@ -290,6 +290,54 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
   return mark();
 }
 
+namespace moe {
+namespace {
+// Scratch of moe_forward_static_scratch: part of this library's device image,
+// one copy per device, so that entry point needs no allocation. Every call on
+// a device uses the same bytes.
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on device `dev` (the current device),
+// looked up the first time that device calls and cached afterwards.
+int static_scratch_address(int dev, void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  if (dev < 0 || dev >= 64) return MOE_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_scratch));
+    if (!p) return MOE_ERR_CUDA;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_forward_static_scratch(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                                          const float* bias_dev, int bias_row_stride, float* logits_out,
+                                          int32_t* idx_out, float* w_out, int* dev_status,
+                                          moe_stream_t stream) {
+  MOE_CHECK_ARG(L && x_dev && y_dev, MOE_ERR_INVALID_ARG);
+  int st = check_shape(&L->shape, T);
+  if (st != MOE_OK) return st;
+  const Workspace ws = plan(L->shape, T);
+  if (ws.total > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo di;
+  if ((st = current_device(&di))) return st;
+  void* scratch = nullptr;
+  if ((st = static_scratch_address(di.device, &scratch))) return st;
+  // The synchronisation counters at the head of the workspace must read zero
+  // when the call's kernels start; clear them on the call's own stream so a
+  // call never depends on how an earlier one ended.
+  MOE_CUDA_TRY(cudaMemsetAsync(static_cast<char*>(scratch) + ws.state, 0,
+                               decode_state_bytes(L->shape.n_experts, L->shape.d_ff), (cudaStream_t)stream));
+  return moe_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, scratch,
+                     MOE_STATIC_SCRATCH_BYTES, dev_status, nullptr, 0, stream);
+}
+
 extern "C" const char* moe_stage_names(int path) {
   if (path == MOE_PATH_DECODE_FUSED) return "decode_fused";
   if (path == MOE_PATH_DECODE_MMA)

@@ -1,0 +1,83 @@
+"""moe_forward_static_scratch (no workspace, no allocation) against moe_forward.
+
+The file name sorts last so that pytest runs it after every other test; it
+must also pass on its own in a fresh process, where its first call is the one
+that looks up the library's scratch array.
+
+Two calls in a row through the static-scratch entry point, on different
+inputs, each compared with moe_forward (own zero-filled workspace) on the
+same inputs: indices bit-exact, and y within the layer tests' tolerance
+(relative L2 <= 5e-3, max |err| <= 2e-2 * rms of moe_forward's y).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+MAX_ABS = 2e-2
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import mxfp4_expert_gb300 as mx
+    return mx
+
+
+def _outputs(T, E, k):
+    return (torch.empty((T, E), dtype=torch.float32, device="cuda"),
+            torch.empty((T, k), dtype=torch.int32, device="cuda"),
+            torch.empty((T, k), dtype=torch.float32, device="cuda"),
+            torch.zeros(1, dtype=torch.int32, device="cuda"))
+
+
+def _compare(mx, layer, x, bias, w):
+    T, E, k = x.shape[0], w.E, w.k
+    l_r, i_r, w_r, s_r = _outputs(T, E, k)
+    y_r = mx.moe_forward(layer, x, bias, logits_out=l_r, idx_out=i_r, w_out=w_r, dev_status=s_r)
+    l_s, i_s, w_s, s_s = _outputs(T, E, k)
+    y_s = torch.empty_like(x)
+    mx.moe_forward_static_scratch(layer, x, y_s, bias, logits_out=l_s, idx_out=i_s, w_out=w_s, dev_status=s_s)
+    torch.cuda.synchronize()
+    assert int(s_r.item()) == 0 and int(s_s.item()) == 0
+    assert torch.equal(i_s, i_r)
+    assert torch.allclose(w_s, w_r, rtol=0, atol=2e-6)
+    yr = y_r.float().cpu().numpy().astype(np.float64)
+    ys = y_s.float().cpu().numpy().astype(np.float64)
+    rel = np.linalg.norm(ys - yr) / np.linalg.norm(yr)
+    rms = np.sqrt(np.mean(yr ** 2))
+    assert rel <= REL_L2, rel
+    assert np.max(np.abs(ys - yr)) <= MAX_ABS * rms
+
+
+def _x(w, set_idx, T):
+    g = torch.Generator(device="cpu").manual_seed(9000 + 31 * set_idx + T)
+    return (torch.randn((T, w.d), generator=g) * 0.5).to(torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("ling_t1", 1), ("ling_t1", 4), ("ling_t1", 8)])
+def test_static_scratch_matches_moe_forward_twice(mx, name, T):
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS[name]
+    layer = synthetic.build_layer(w, 0)
+    T = w.T if T is None else T
+    assert mx.moe_workspace_bytes(layer.shape, T) <= mx.STATIC_SCRATCH_BYTES
+    for call in range(2):
+        _compare(mx, layer, _x(w, call, T), None, w)
+
+
+def test_static_scratch_rejects_too_large(mx):
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS["tiny"]
+    layer = synthetic.build_layer(w, 0)
+    T = 1
+    while mx.moe_workspace_bytes(layer.shape, T) <= mx.STATIC_SCRATCH_BYTES:
+        T *= 2
+    x = _x(w, 0, T)
+    y = torch.empty_like(x)
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_forward_static_scratch(layer, x, y)
+    assert ei.value.status == -4  # MOE_ERR_WORKSPACE_TOO_SMALL
