@@ -210,8 +210,7 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
     da.w_out = w_out;
     da.y = static_cast<__nv_bfloat16*>(y_dev);
     da.state = at<DecodeState>(B, ws.state);
-    da.hB = at<uint8_t>(B, ws.h_b);
-    da.hE = at<int16_t>(B, ws.h_e);
+    da.h = at<float>(B, ws.h);
     da.h_sh = at<float>(B, ws.h_sh);
     da.status = status;
     if ((st = launch_decode(da, di, s))) return st;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -77,6 +78,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no shared-memory destination).
+// src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- loads ----------------------------------------------------------------
 __device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
   uint2 v;
@@ -114,6 +121,13 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// e4m3 byte (low 8 bits of c) -> fp32, exact, through the hardware
+// fp8 -> f16x2 conversion (every finite e4m3 value is an f16 value).
+__device__ __forceinline__ float e4m3_to_f32_hw(uint32_t c) {
+  uint32_t h2;
+  asm("{\n .reg .b16 lo;\n cvt.u16.u32 lo, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}\n" : "=r"(h2) : "r"(c));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 // Exact e4m3 -> fp32 (finite codes).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {

@@ -1,40 +1,45 @@
 // Single-launch decode path (T <= 4 tokens): one cooperative persistent kernel,
-// one CTA per SM, so a layer call is a single launch with no host round trips
-// and no idle HBM between stages.
+// one CTA per SM, so a layer call is a single launch with no host round trips.
 //
-// Every CTA walks a private sequence of "loads". Each load fills one slot of a
-// shared-memory ring through 1-D bulk copies, and the CTA consumes the loads in
-// order:
+// Every CTA walks a private sequence of "loads". A producer warp fills the
+// slots of a shared-memory ring with 1-D bulk copies, in load order; the 15
+// compute warps consume every load independently (no CTA-wide barrier per
+// load): each waits for the slot, does its share, and releases the slot
+// (the slot is refilled once all 15 have released it).
 //
-//   R   its slice of router rows             -> logits (global)     phase A
-//   F   its slice of shared gate/up rows     -> h_sh (global)       phase A
-//   SD  shared-down rows of its output tiles -> y accumulators      needs all h_sh
-//   GU  its routed gate/up items             -> h blocks (global)   needs routing
-//   DN  routed-down units of its output tiles -> y accumulators     needs all h blocks
+//   R   its slice of router rows          -> logits (global)      warp per row
+//   F   its slice of shared gate/up rows  -> h_sh (global)        warp per feature
+//   GU  its routed gate/up tiles          -> h (global, fp32)     needs routing
+//   SD  shared-down rows of its tiles     -> y accumulators       needs all h_sh
+//   DN  routed-down units of its tiles    -> y accumulators       needs all h
 //
-// R, F and SD do not depend on routing and are requested at kernel start, so
-// HBM is busy from the first cycle. After its R loads a CTA arrives at a
-// counter barrier; it computes its F loads while the others catch up, then
-// reads all logits and runs the top-k itself (every CTA derives the same
-// routing, so no second exchange is needed), and requests its phase-B loads.
+// A routed gate/up tile (16 rows: 8 gate + 8 up rows of one active expert) is
+// split along K over the warps. Every warp writes its partial sums to one of a
+// few reduction buffers, and the last warp to arrive (a shared-memory counter)
+// adds the fifteen partials in warp order, so results do not depend on timing,
+// and writes 8 features of h.
 //
-// A routed gate/up item is one 32-feature block of one active expert (four
-// 16-row tiles, 87 KB for the Ling shape). The CTA that computes it holds the
-// block's 32 values of h per token and writes them directly as e4m3 terms with
-// one block exponent (the B operand of the down MMA), so no other CTA has to
-// touch h. After its last item a CTA publishes with one release increment;
-// before its down units it waits for all CTAs, then pulls every token's h
-// terms into shared memory with one bulk copy. Down units accumulate in
-// registers across experts and K-blocks; the cross-warp sum is taken once per
-// output tile at the end. Each CTA owns whole 16-row output tiles, so y is
-// written without a cross-CTA reduction. Gate/up items are handed out so that
-// every CTA moves about the same number of bytes in phase B, counting its down
-// and shared-down rows.
+// Routing: once its router rows are in the logits a CTA increments a global
+// counter. While the other CTAs catch up, its warps turn the activations into
+// e4m3 terms; then every CTA reads all logits and runs the top-k itself (all
+// warps: the best k of every 32-expert chunk, then one merge warp per token),
+// so no second exchange is needed, and hands its routed loads to the producer.
+// Gate/up tiles are handed out so every CTA moves about the same number of
+// bytes in the routed phase (tiles, down units and shared-down rows counted
+// together). The shared-down rows are prefetched into L2 while the routing is
+// under way.
+//
+// After its gate/up tiles a CTA publishes with one release increment; before
+// its down units it waits for all CTAs, splits every slot's h into e4m3 terms
+// (with the routing weight folded into the block factor), and runs its down
+// units, which accumulate in registers per output tile. The cross-warp sum is
+// taken once per tile at the end; each CTA owns whole 16-row output tiles, so
+// y is written without a cross-CTA reduction.
 //
 // Cross-call state (counters) lives at the start of the workspace and must be
 // zero before the first call; the last CTA of a call resets it. Every wait is
 // bounded (kSpinBudget); on timeout the kernel sets MOE_DEV_TIMEOUT and
-// carries on.
+// carries on, so it always terminates.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -47,47 +52,55 @@ namespace moe {
 namespace {
 
 #ifdef MOE_DECODE_TRACE
-// Debug builds only: per-CTA globaltimer stamps at phase boundaries.
-constexpr int kTracePoints = 16;
+// Debug builds only: per-CTA globaltimer stamps at phase boundaries and cycle
+// sums of thread 0.
+constexpr int kTracePoints = 32;
 __device__ unsigned long long g_trace[1024][kTracePoints];
-__device__ __forceinline__ void trace(int point) {
-  if (threadIdx.x == 0) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    g_trace[blockIdx.x][point] = t;
-  }
-}
 __device__ __forceinline__ unsigned long long gtime() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+__device__ __forceinline__ void trace(int point) {
+  if (threadIdx.x == 0) g_trace[blockIdx.x][point] = gtime();
+}
 __device__ __forceinline__ void trace_put(int point, unsigned long long v) {
   if (threadIdx.x == 0) g_trace[blockIdx.x][point] = v;
 }
+__device__ __forceinline__ long long dclk() { return clock64(); }
 #else
 __device__ __forceinline__ void trace(int) {}
-__device__ __forceinline__ unsigned long long gtime() { return 0; }
 __device__ __forceinline__ void trace_put(int, unsigned long long) {}
+__device__ __forceinline__ long long dclk() { return 0; }
 #endif
 
 constexpr int kWarps = 15;                  // compute warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp that issues the bulk copies
 constexpr int kComputeThreads = kWarps * 32;
-constexpr int kPairsMax = (kDecodeMaxT + 1) / 2;
-constexpr int kRowsPerLoad = 8;   // max rows of a "few long rows" GEMV load (split-K over warps)
+constexpr int kRedSlots = 4;      // reduction buffers in flight
+constexpr int kRowsPerLoad = 4;   // bf16 rows per load: router rows, or 2 shared features x (gate, up)
 constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 3840
+constexpr int kMergeChunks = 16;  // top-k: E <= 16 chunks of 32 experts
+constexpr int kCtrWords = kRedSlots;   // shared arrival counters of the reduction buffers
+constexpr int kUnroll = 6;        // MMA items per warp issued back to back (no branches in between)
+
+#ifndef MOE_DECODE_STAGE_CAP
+#define MOE_DECODE_STAGE_CAP kDecodeMaxStages
+#endif
+// Ring depth limit (slots per CTA).
+constexpr int kDecodeStageCap = MOE_DECODE_STAGE_CAP;
 
 // Barrier among the compute warps only (the producer warp never joins it).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory"); }
-__device__ __forceinline__ bool csync_and(bool v) {
+// Count of compute threads with v != 0; also a barrier among them.
+__device__ __forceinline__ int csync_count(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      "{\n .reg .pred p;\n setp.ne.u32 p, %1, 0;\n bar.red.popc.u32 %0, 1, %2, p;\n}\n"
       : "=r"(r)
       : "r"(uint32_t(v)), "n"(kComputeThreads)
       : "memory");
-  return r != 0;
+  return int(r);
 }
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
@@ -122,65 +135,53 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
-// bf16 rows (row-major, K elements each, in shared memory) times T bf16
-// activation vectors (shared memory), split over all warps along K.
-// out[r * kDecodeMaxT + t] (shared) receives the dot products. n <= kRowsPerLoad.
+// Weight scale byte -> 2^(s-127) as fp32 (s = 0 gives 0, s = 255 gives +inf).
+__device__ __forceinline__ float scale_lo(uint32_t sc16) { return __uint_as_float((sc16 << 23) & 0x7F800000u); }
+__device__ __forceinline__ float scale_hi(uint32_t sc16) { return __uint_as_float((sc16 << 15) & 0x7F800000u); }
+
+// Factor that turns an MMA result over one (weight block, activation block)
+// into its true value, apart from the weight scale: weights were decoded as
+// 2^-6 x E2M1 value and the activation block stored as terms x 2^-e, so the
+// factor is w x 2^(e+6) (0 for an all-zero block).
+__device__ __forceinline__ float act_factor(int e, float w) {
+  return e == kActZeroExp ? 0.0f : ldexpf(w, e + 6);
+}
+
+// Row (bf16, n8 chunks of 8 elements in shared memory) times T activation
+// rows: one warp, lanes strided over the chunks; every lane gets the sums.
 template <int T>
-__device__ void gemv_bf16_rows(const uint8_t* rows, int n, int K, const __nv_bfloat16* xs,
-                               float* red, float* out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chunks = K / 8;
-  float acc[kRowsPerLoad][T];
+__device__ __forceinline__ void warp_row_dot(const uint4* row, const uint4* xs4, int n8, int lane, float (&out)[T]) {
+  float acc[T];
 #pragma unroll
-  for (int r = 0; r < kRowsPerLoad; ++r)
+  for (int t = 0; t < T; ++t) acc[t] = 0.0f;
+#pragma unroll 4
+  for (int j = lane; j < n8; j += 32) {
+    const uint4 w = row[j];
 #pragma unroll
-    for (int t = 0; t < T; ++t) acc[r][t] = 0.0f;
-  for (int j = tid; j < chunks; j += kComputeThreads) {
-    uint4 xv[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) xv[t] = reinterpret_cast<const uint4*>(xs + (size_t)t * K)[j];
-#pragma unroll
-    for (int r = 0; r < kRowsPerLoad; ++r) {
-      if (r < n) {
-        const uint4 wv = reinterpret_cast<const uint4*>(rows + (size_t)r * K * 2)[j];
-#pragma unroll
-        for (int t = 0; t < T; ++t) acc[r][t] += dot8_bf16(wv, xv[t]);
-      }
-    }
+    for (int t = 0; t < T; ++t) acc[t] += dot8_bf16(w, xs4[t * n8 + j]);
   }
 #pragma unroll
-  for (int r = 0; r < kRowsPerLoad; ++r) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      if (r < n) {
-        const float v = warp_sum(acc[r][t]);
-        if (lane == 0) red[(warp * kRowsPerLoad + r) * kDecodeMaxT + t] = v;
-      }
-    }
-  }
-  csync();
-  if (tid < n * kDecodeMaxT) {
-    const int r = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
-    float v = 0.0f;
-    if (t < T)
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += red[(w * kRowsPerLoad + r) * kDecodeMaxT + t];
-    out[tid] = v;
-  }
-  csync();
+  for (int t = 0; t < T; ++t) out[t] = warp_sum(acc[t]);
 }
 
 // Shared-memory carve-up (byte offsets), identical on host and device. The
-// phase-A buffers (xs, xb, xe, hsh) and the phase-B h terms (hbs, hes) share
-// one region: the former are dead once the down units start.
+// activation terms (xs, xb, xfa; dead after the gate/up tiles), the shared h
+// (hsh; dead after the shared-down rows) and the h terms (hbs, hfa) share
+// one region.
 struct Smem {
-  uint32_t ring, bars, ov, xs, xb, xe, hsh, hbs, hes, hblk, yacc, red, gout, sel_e, sel_w, act, act_n,
+  uint32_t ring, bars, ctr, red, ov, xs, xb, xfa, hsh, hbs, hfa, dnred, ysd, sel_e, sel_w, act, act_n,
       act_slot, act_tok, first, misc, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline uint32_t he_stride(int I) { return align_up(uint32_t(I / kMxBlock), 8); }
-__host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages, uint32_t slot_bytes) {
+__host__ __device__ inline int red_floats(int T) { return 32 * ((T + 1) / 2); }
+__host__ __device__ inline int max_tiles_per_cta(int d, int G) { return (d / kTileRows + G - 1) / G; }
+__host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int stages, uint32_t slot_bytes,
+                                          int max_tiles) {
   Smem s{};
   uint32_t at = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
@@ -189,35 +190,33 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages
     at += bytes;
     return here;
   };
+  const uint32_t KBd = uint32_t(d / kMxBlock), KBi = uint32_t(I / kMxBlock), slots = uint32_t(T * k);
   s.ring = take(uint32_t(stages) * slot_bytes, 128);
-  s.bars = take(8u * uint32_t(2 * stages + 3), 8);   // full[S], empty[S], h staging, routing, x
-  // overlay: phase A layout
+  s.bars = take(8u * uint32_t(2 * stages + kRedSlots + 1), 8);   // full[S], empty[S], redfree[], routing
+  s.ctr = take(4u * kCtrWords, 4);
+  const uint32_t nch = uint32_t((E + 31) / 32), kk = uint32_t(k < 32 ? k : 32);
+  const uint32_t red_b = uint32_t(kRedSlots * kWarps * red_floats(T)) * 4u;
+  const uint32_t cand_b = uint32_t(T) * nch * kk * 8u;
+  s.red = take(red_b > cand_b ? red_b : cand_b, 16);
   const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
-  const uint32_t xb_b = align_up(uint32_t(T) * (d / 32) * kActRowKbBytes, 16);
-  const uint32_t xe_b = align_up(uint32_t(T) * (d / 32) * 2, 16);
+  const uint32_t xb_b = align_up(uint32_t(T) * KBd * kActRowKbBytes, 16);
+  const uint32_t xfa_b = align_up(uint32_t(T) * KBd * 4, 16);
+  const uint32_t a_b = xs_b + xb_b + xfa_b;
   const uint32_t hsh_b = align_up(uint32_t(T) * I * 4, 16);
-  const uint32_t a_bytes = xs_b + xb_b + xe_b + hsh_b;
-  // overlay: phase B layout (h terms of every slot)
-  const uint32_t slots = uint32_t(T) * k;
-  const uint32_t hbs_b = align_up(slots * (I / 32) * kActRowKbBytes, 16);
-  const uint32_t hes_b = align_up(slots * he_stride(I) * 2, 16);
-  const uint32_t b_bytes = hbs_b + hes_b;
-  s.ov = take(a_bytes > b_bytes ? a_bytes : b_bytes, 128);
+  const uint32_t hbs_b = align_up(slots * KBi * kActRowKbBytes, 16);
+  const uint32_t hfa_b = align_up(slots * KBi * 4, 16);
+  const uint32_t b_b = hbs_b + hfa_b;
+  uint32_t ov = a_b > hsh_b ? a_b : hsh_b;
+  ov = ov > b_b ? ov : b_b;
+  s.ov = take(ov, 128);
   s.xs = s.ov;
   s.xb = s.xs + xs_b;
-  s.xe = s.xb + xb_b;
-  s.hsh = s.xe + xe_b;
+  s.xfa = s.xb + xb_b;
+  s.hsh = s.ov;
   s.hbs = s.ov;
-  s.hes = s.hbs + hbs_b;
-  s.hblk = take(kDecodeMaxT * 32 * 4, 16);
-  s.yacc = take(uint32_t(T) * kDecodeMaxTiles * 16 * 4, 16);
-  const uint32_t red_mma = kWarps * kPairsMax * 32 * 2 * 4;
-  const uint32_t red_gemv = kWarps * kRowsPerLoad * kDecodeMaxT * 4;
-  const uint32_t red_dn = kWarps * kDecodeMaxT * 32 * 2 * 4;
-  uint32_t red_b = red_mma > red_gemv ? red_mma : red_gemv;
-  red_b = red_b > red_dn ? red_b : red_dn;
-  s.red = take(red_b, 16);
-  s.gout = take(kRowsPerLoad * kDecodeMaxT * 4, 16);
+  s.hfa = s.hbs + hbs_b;
+  s.dnred = take(uint32_t(max_tiles * kWarps * T * kTileRows) * 4u, 16);
+  s.ysd = take(uint32_t(T * max_tiles * kTileRows) * 4u, 16);
   s.sel_e = take(kDecodeMaxT * 32 * 4, 4);
   s.sel_w = take(kDecodeMaxT * 32 * 4, 4);
   s.act = take(kDecodeMaxT * 32 * 4, 4);
@@ -230,45 +229,90 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int k, int stages
   return s;
 }
 
-// Per-CTA load sequence: [0,nR) router, [nR,bF) shared gate/up, [bF,bSD)
-// shared down, [bSD,bGU) routed gate/up tiles (4 per item), [bGU,bDN) routed
-// down loads (dnch units each).
+// Per-CTA load sequence: [0,nR) router, [nR,bF) shared gate/up, [bF,bGU)
+// routed gate/up tiles, [bGU,bSD) shared down, [bSD,bDN) routed down loads
+// (nL loads of at most dnch units per output tile).
 struct Seq {
   int r0, r1, f0, f1, t0, ntl;
   int nR, nF, nSD;
   int rch, fch, sdch, dnch;
-  int D, i0, i1, nDN;
-  int bF, bSD, bGU, bDN;
+  int D, i0, i1, nL, nDN;
+  int bF, bGU, bSD, bDN;
+  __device__ void set_routed(int D_, int i0_, int i1_) {
+    D = D_;
+    i0 = i0_;
+    i1 = i1_ > i0_ ? i1_ : i0_;
+    bGU = bF + (i1 - i0);
+    bSD = bGU + nSD;
+    nL = (D + dnch - 1) / dnch;
+    nDN = ntl * nL;
+    bDN = bSD + nDN;
+  }
 };
+
+// Routed gate/up tiles reduce through job buffers: tile j uses buffer
+// j % kRedSlots. Before the warp overwrites that buffer it waits until the
+// previous tile there has been reduced.
+__device__ __forceinline__ float* job_buffer(float* red, uint64_t* redfree, int j, int warp, int rf, int* status) {
+  const int rs = j % kRedSlots;
+  if (j >= kRedSlots) mbar_wait(&redfree[rs], uint32_t(j / kRedSlots - 1) & 1u, status);
+  return red + (size_t)(rs * kWarps + warp) * rf;
+}
+// After writing its partials: true in the warp that arrived last (it then
+// owns the reduction of job j and must call job_done).
+__device__ __forceinline__ bool job_last(uint32_t* ctr, int j, int lane) {
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) {
+    __threadfence_block();
+    old = atomicAdd(&ctr[j % kRedSlots], 1u);
+  }
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  const bool last = old == uint32_t(kWarps - 1);
+  if (last) __threadfence_block();
+  return last;
+}
+__device__ __forceinline__ void job_done(uint32_t* ctr, uint64_t* redfree, int j, int lane) {
+  __syncwarp();
+  if (lane == 0) {
+    ctr[j % kRedSlots] = 0u;
+    mbar_arrive(&redfree[j % kRedSlots]);
+  }
+}
 
 template <int T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   trace(0);
+  trace_put(17, (unsigned long long)clock64());
+  long long tacc[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};   // debug builds: cycle sums of thread 0
+  auto trace_add = [&](int point, long long v) { tacc[point - 20] += v; };
   constexpr int kPairs = (T + 1) / 2;
+  constexpr int kRF = 32 * kPairs;
   const int d = a.d, I = a.I, E = a.E, k = a.k;
-  const int KBd = d / kMxBlock, KBi = I / kMxBlock, HES = int(he_stride(I));
-  const int NTd = d / kTileRows;
-  const int G = gridDim.x, c = blockIdx.x;
+  const int KBd = d / kMxBlock, KBi = I / kMxBlock;
+  const int NTd = d / kTileRows, NTg = 2 * I / kTileRows;
+  const int G = gridDim.x, c = blockIdx.x, S = a.stages;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const Smem L = smem_plan(T, d, I, k, a.stages, a.slot_bytes);
+  const int max_tiles = max_tiles_per_cta(d, G);
+  const Smem L = smem_plan(T, d, I, E, k, S, a.slot_bytes, max_tiles);
   uint8_t* ring = sm + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
-  uint64_t* empty = full + a.stages;
-  uint64_t* hbar = empty + a.stages;
-  uint64_t* rbar = hbar + 1;
-  uint64_t* xbar = rbar + 1;
+  uint64_t* empty = full + S;
+  uint64_t* redfree = empty + S;
+  uint64_t* rbar = redfree + kRedSlots;
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(sm + L.ctr);
+  float* red = reinterpret_cast<float*>(sm + L.red);
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
+  const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
   uint8_t* xb = sm + L.xb;
-  int16_t* xe = reinterpret_cast<int16_t*>(sm + L.xe);
+  float* xfa = reinterpret_cast<float*>(sm + L.xfa);
   float* hsh = reinterpret_cast<float*>(sm + L.hsh);
   uint8_t* hbs = sm + L.hbs;
-  int16_t* hes = reinterpret_cast<int16_t*>(sm + L.hes);
-  float* hblk = reinterpret_cast<float*>(sm + L.hblk);
-  float* yacc = reinterpret_cast<float*>(sm + L.yacc);
-  float* red = reinterpret_cast<float*>(sm + L.red);
-  float* gout = reinterpret_cast<float*>(sm + L.gout);
+  float* hfa = reinterpret_cast<float*>(sm + L.hfa);
+  float* dnred = reinterpret_cast<float*>(sm + L.dnred);
+  float* ysd = reinterpret_cast<float*>(sm + L.ysd);
   int* sel_e = reinterpret_cast<int*>(sm + L.sel_e);
   float* sel_w = reinterpret_cast<float*>(sm + L.sel_w);
   int* act = reinterpret_cast<int*>(sm + L.act);
@@ -281,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   DecodeState* st = a.state;
   const uint32_t U_gu = uint32_t(KBd) * kUnitBytes, U_dn = uint32_t(KBi) * kUnitBytes;
   const uint32_t row_bytes = uint32_t(d) * 2, sdrow_bytes = uint32_t(I) * 2;
-  const int ystride = kDecodeMaxTiles * kTileRows;
+  const int ystride = max_tiles * kTileRows;
 
   Seq s;
   s.r0 = int((long long)c * E / G);
@@ -298,15 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   s.nF = (s.f1 - s.f0 + s.fch - 1) / s.fch;
   s.nSD = a.has_shared ? (s.ntl * kTileRows + s.sdch - 1) / s.sdch : 0;
   s.bF = s.nR + s.nF;
-  s.bSD = s.bF + s.nSD;
   s.D = 0;
   s.i0 = s.i1 = 0;
-  s.nDN = 0;
-  s.bGU = s.bDN = s.bSD;
+  s.nL = s.nDN = 0;
+  s.bGU = s.bSD = s.bDN = s.bF;
 
-  // bulk-copy requests of load i into its ring slot (thread 0 only)
+  // bulk-copy requests of load i into its ring slot (producer lane only)
   auto issue = [&](int i) {
-    const int slot = i % a.stages;
+    const int slot = i % S;
     uint8_t* dst = ring + (size_t)slot * a.slot_bytes;
     uint64_t* bar = &full[slot];
     if (i < s.nR) {
@@ -318,147 +361,193 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       mbar_arrive_expect_tx(bar, 2 * n * row_bytes);
       bulk_g2s(dst, a.sh_gate + (size_t)f * d, n * row_bytes, bar);
       bulk_g2s(dst + (size_t)n * row_bytes, a.sh_up + (size_t)f * d, n * row_bytes, bar);
+    } else if (i < s.bGU) {
+      const int gt = s.i0 + (i - s.bF), ai = gt / NTg, tt = gt - ai * NTg;
+      mbar_arrive_expect_tx(bar, U_gu);
+      bulk_g2s(dst, a.gate_up + (size_t)act[ai] * a.gu_mat + (size_t)tt * U_gu, U_gu, bar);
     } else if (i < s.bSD) {
-      const int r = s.t0 * kTileRows + (i - s.bF) * s.sdch;
+      const int r = s.t0 * kTileRows + (i - s.bGU) * s.sdch;
       const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
       mbar_arrive_expect_tx(bar, n * sdrow_bytes);
       bulk_g2s(dst, a.sh_down + (size_t)r * I, n * sdrow_bytes, bar);
-    } else if (i < s.bGU) {
-      const int j = i - s.bSD;
-      const int item = s.i0 + j / 4, tile = (item % KBi) * 4 + (j % 4);
-      const int e = act[item / KBi];
-      mbar_arrive_expect_tx(bar, U_gu);
-      bulk_g2s(dst, a.gate_up + (size_t)e * a.gu_mat + (size_t)tile * U_gu, U_gu, bar);
     } else {
-      const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
+      const int l = i - s.bSD, tl = l / s.nL, a0 = (l - tl * s.nL) * s.dnch, n = min(s.dnch, s.D - a0);
       mbar_arrive_expect_tx(bar, n * U_dn);
-      for (int j = 0; j < n; ++j) {
-        const int u = u0 + j, tl = u / s.D, ai = u % s.D;
-        const int e = act[ai], tile = s.t0 + tl;
-        bulk_g2s(dst + (size_t)j * U_dn, a.down + (size_t)e * a.dn_mat + (size_t)tile * U_dn, U_dn, bar);
-      }
+      for (int j = 0; j < n; ++j)
+        bulk_g2s(dst + (size_t)j * U_dn, a.down + (size_t)act[a0 + j] * a.dn_mat + (size_t)(s.t0 + tl) * U_dn,
+                 U_dn, bar);
     }
   };
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * a.stages + 3; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kWarps);
+    }
+    for (int r = 0; r < kRedSlots; ++r) mbar_init(&redfree[r], 1);
+    mbar_init(rbar, 1);
+    for (int i = 0; i < kCtrWords; ++i) ctr[i] = 0u;
     mbar_fence_init();
   }
-  __syncthreads();   // the only full-CTA barrier: barriers initialised
+  __syncthreads();   // the only full-CTA barrier: barriers and counters initialised
 
   if (warp == kWarps) {
     // ---- producer warp: issues every bulk copy, in load order ----------------
     if (lane == 0) {
-      // the activations first, so they are not queued behind the weights
-      mbar_arrive_expect_tx(xbar, uint32_t(T) * d * 2);
-      bulk_g2s(xs, a.x, uint32_t(T) * d * 2, xbar);
-      int n_loads = s.bSD;
-      for (int j = 0; j < n_loads || j == s.bSD; ++j) {
-        if (j == s.bSD) {
-          // phase B is known once the compute warps have routed
+      int n_loads = s.bF;
+      for (int j = 0;; ++j) {
+        if (j == s.bF) {
+          // shared-down rows into L2 while the routing is under way
+          if (s.nSD > 0) {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(a.sh_down + (size_t)s.t0 * kTileRows * I);
+            const uint32_t bytes = uint32_t(s.ntl * kTileRows) * sdrow_bytes;
+            for (uint32_t o = 0; o < bytes; o += 32768u) prefetch_l2(src + o, min(32768u, bytes - o));
+          }
+          // the routed loads are known once the compute warps have routed
           if (!mbar_wait(rbar, 0u, a.status, 256)) break;
-          s.D = misc[0];
-          s.i0 = misc[1];
-          s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
-          s.nDN = (s.ntl * s.D + s.dnch - 1) / s.dnch;
-          s.bGU = s.bSD + 4 * (s.i1 - s.i0);
-          s.bDN = s.bGU + s.nDN;
+          s.set_routed(misc[0], misc[1], misc[2]);
           n_loads = s.bDN;
-          if (j >= n_loads) break;
         }
-        if (j >= a.stages && !mbar_wait(&empty[j % a.stages], uint32_t(j / a.stages - 1) & 1u, a.status, 256)) break;
+        if (j >= n_loads) break;
+        if (j >= S && !mbar_wait(&empty[j % S], uint32_t(j / S - 1) & 1u, a.status, 256)) break;
         issue(j);
       }
 #ifdef MOE_DECODE_TRACE
-      g_trace[blockIdx.x][15] = gtime();
+      g_trace[blockIdx.x][16] = gtime();
 #endif
     }
     return;
   }
 
-  for (int i = tid; i < T * ystride; i += kComputeThreads) yacc[i] = 0.0f;
-  mbar_wait(xbar, 0u, a.status);   // bf16 activations for the CUDA-core GEMVs
+  // activations: plain loads by the compute warps (read-only during the call)
+  for (int j = tid; j < T * d / 8; j += kComputeThreads)
+    reinterpret_cast<uint4*>(xs)[j] = __ldg(reinterpret_cast<const uint4*>(a.x) + j);
+  for (int i = tid; i < T * ystride; i += kComputeThreads) ysd[i] = 0.0f;
+  if (tid == 0) {
+    if (s.nR == 0) red_release_add_u64(&st->bar, 1ull);
+    if (s.nF == 0) red_release_add(&st->shcnt, 1u);
+  }
   csync();
   trace(1);
-  if (tid == 0) {
-    if (s.nR == 0) {
-      __threadfence();
-      atomicAdd(&st->bar, 1ull);
-    }
-    if (s.nF == 0) {
-      __threadfence();
-      atomicAdd(&st->shcnt, 1u);
-    }
-  }
 
   // per-lane down accumulators of the current output tile: [token][row g / row g+8]
   float dacc[T][2];
 #pragma unroll
   for (int t = 0; t < T; ++t) dacc[t][0] = dacc[t][1] = 0.0f;
   int dn_tile = -1;
-  // cross-warp sum of the down accumulators into y for output tile tl; the
-  // four lanes of a quad hold the same two rows (different columns/slots)
+  // this warp's down partials of output tile tl -> dnred (the four lanes of a
+  // quad hold the same two rows for different columns)
   auto flush_tile = [&](int tl) {
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 0] = dacc[t][0];
-      red[((warp * kDecodeMaxT + t) * 32 + lane) * 2 + 1] = dacc[t][1];
+      float v0 = dacc[t][0], v1 = dacc[t][1];
+      v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
+      v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 2);
+      v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
+      v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 2);
+      if (q == 0) {
+        float* o = dnred + ((size_t)(tl * kWarps + warp) * T + t) * kTileRows;
+        o[g] = v0;
+        o[8 + g] = v1;
+      }
       dacc[t][0] = dacc[t][1] = 0.0f;
     }
-    csync();
-    if (tid < T * kTileRows) {
-      const int t = tid / kTileRows, r = tid % kTileRows;
-      const int gg = r & 7, half = r >> 3;
-      float v = 0.0f;
-      for (int w = 0; w < kWarps; ++w)
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) v += red[((w * kDecodeMaxT + t) * 32 + gg * 4 + qq) * 2 + half];
-      yacc[t * ystride + tl * kTileRows + r] += v;
-    }
-    csync();
   };
+  // down items (unit, K-block) of a load are dealt to the warps round-robin:
+  // item m = warp + 15 j; (unit, kb) of the warp's first item and the step
+  const int dn_u0 = warp / KBi, dn_k0 = warp - dn_u0 * KBi;
+  const int dn_du = kWarps / KBi, dn_dk = kWarps - dn_du * KBi;
 
-  int total = s.bSD;
-  unsigned long long t_wait = 0, t_gu = 0;   // debug builds: time waiting for loads / in gate-up tiles
   for (int i = 0;; ++i) {
-    if (i == s.bF) {
-      // ---- routing: every CTA has written its router rows -------------------
+    if (i == s.nR) {
+      // ---- routing ----------------------------------------------------------
+      csync();   // every router row of this CTA is in the logits
+      if (tid == 0 && s.nR > 0) red_release_add_u64(&st->bar, 1ull);
+      // activations -> e4m3 terms (B operand of the gate/up MMAs)
+#pragma unroll 2
+      for (int u = warp; u < T * KBd; u += kWarps) {
+        const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
+        const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
+        if (lane == 0) xfa[u] = act_factor(ex, 1.0f);
+      }
       trace(3);
       if (tid == 0) wait_geq_u64(&st->bar, (unsigned long long)G, a.status);
       csync();
       trace(4);
-      if (warp < T) {
-        int e_sel;
-        float w_sel;
-        const float* brow = a.bias ? a.bias + (size_t)warp * a.bias_stride : nullptr;
-        warp_topk<16, true>(a.logits + (size_t)warp * E, brow, E, k, lane, &e_sel, &w_sel);
-        if (lane < k) {
-          sel_e[warp * k + lane] = e_sel;
-          sel_w[warp * k + lane] = w_sel;
-          if (c == 0) {
-            if (a.idx_out) a.idx_out[warp * k + lane] = e_sel;
-            if (a.w_out) a.w_out[warp * k + lane] = w_sel;
-          }
+      // stage 1: the best min(k, 32) of every (token, 32-expert chunk), by
+      // key descending, equal keys -> lower expert index
+      const int nch = (E + 31) / 32, kk = k < 32 ? k : 32;
+      uint32_t* ckey = reinterpret_cast<uint32_t*>(red);
+      uint32_t* cidx = ckey + T * nch * kk;
+      for (int task = warp; task < T * nch; task += kWarps) {
+        const int t = task / nch, ch = task - t * nch;
+        const uint32_t e = uint32_t(ch * 32 + lane);
+        uint32_t key = 0u;
+        if (int(e) < E) {
+          float v = __ldcg(a.logits + (size_t)t * E + e);
+          if (a.bias) v = __fadd_rn(v, a.bias[(size_t)t * a.bias_stride + e]);
+          key = rank_key(v);
         }
-      } else {
-        // meanwhile the other warps turn the activations into e4m3 terms
-        for (int u = warp - T; u < T * KBd; u += kWarps - T) {
-          const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
-          const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
-          if (lane == 0) xe[u] = int16_t(ex);
+        for (int r = 0; r < kk; ++r) {
+          const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key);
+          const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, (m != 0u && key == m) ? e : 0xFFFFFFFFu);
+          if (lane == 0) {
+            ckey[task * kk + r] = m;
+            cidx[task * kk + r] = win;
+          }
+          if (e == win) key = 0u;
         }
       }
       csync();
-      trace(11);
+      trace(5);
+      // stage 2: one warp per token merges the sorted chunk lists; lane c
+      // holds the head of chunk c
+      if (warp < T) {
+        const int t = warp;
+        const uint32_t* lk = ckey + (size_t)(t * nch + lane) * kk;
+        const uint32_t* li = cidx + (size_t)(t * nch + lane) * kk;
+        int ptr = 0;
+        uint32_t hk = lane < nch ? lk[0] : 0u, hi = lane < nch ? li[0] : 0xFFFFFFFFu;
+        uint32_t my_e = 0u, my_key = 0u;
+        for (int r = 0; r < k; ++r) {
+          const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, hk);
+          const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, hk == wmax ? hi : 0xFFFFFFFFu);
+          if (lane == r) {
+            my_e = emin;
+            my_key = wmax;
+          }
+          if (hk == wmax && hi == emin) {
+            ++ptr;
+            hk = ptr < kk ? lk[ptr] : 0u;
+            hi = ptr < kk ? li[ptr] : 0xFFFFFFFFu;
+          }
+        }
+        const float v = rank_value(my_key);
+        const float v0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+        const float ex = lane < k ? expf(v - v0) : 0.0f;
+        const float sum = warp_sum(ex);
+        if (lane < k) {
+          const float w = ex / sum;
+          sel_e[t * k + lane] = int(my_e);
+          sel_w[t * k + lane] = w;
+          if (c == 0) {
+            if (a.idx_out) a.idx_out[t * k + lane] = int(my_e);
+            if (a.w_out) a.w_out[t * k + lane] = w;
+          }
+        }
+      }
+      csync();
+      trace(6);
       // active experts ascending; each with its slots (slot = t*k + j) in token order
       const int n = T * k;
+      int f = 0;
       if (tid < n) {
         const int e = sel_e[tid];
-        int f = 1;
+        f = 1;
         for (int j = 0; j < tid; ++j) f &= sel_e[j] != e ? 1 : 0;
         first[tid] = f;
       }
-      csync();
+      const int D = csync_count(f != 0);
       if (tid < n) {
         const int e = sel_e[tid];
         int rank = 0, pos = 0, cnt = 0;
@@ -475,102 +564,197 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
           act_n[rank] = cnt;
         }
       }
-      if (tid == 0) {
-        int D = 0;
-        for (int j = 0; j < n; ++j) D += first[j];
-        // gate/up items (32-feature blocks): contiguous ranges, balanced by bytes
-        // together with each CTA's down units and shared-down rows. W(c) is the
-        // cumulative budget left for items before CTA c (non-decreasing).
-        const int n_items = D * KBi;
-        const float U = 4.0f * float(U_gu);
+      if (tid < 2) {
+        // gate/up tiles: contiguous ranges, balanced by bytes together with
+        // each CTA's down units and shared-down rows. W(c) is the cumulative
+        // budget left for tiles before CTA c (non-decreasing). Thread 0 finds
+        // where my range starts, thread 1 where it ends.
+        const int n_tiles = D * NTg;
+        const float U = float(U_gu);
         const float DT = float(D) * float(U_dn) + (a.has_shared ? float(kTileRows) * float(sdrow_bytes) : 0.0f);
-        const float target = (float(n_items) * U + float(NTd) * DT) / float(G);
+        const float target = (float(n_tiles) * U + float(NTd) * DT) / float(G);
         const int qt = NTd / G;
         const float w0 = fmaxf(0.0f, target - DT * float(qt)), w1 = fmaxf(0.0f, target - DT * float(qt + 1));
         auto W = [&](int cc) {
           const int big = (cc * NTd) / G - cc * qt;
           return float(cc - big) * w0 + float(big) * w1;
         };
-        const float WG = W(G);
-        auto cut = [&](int cc) {
-          if (cc >= G) return n_items;
-          if (WG <= 0.0f) return 0;
-          const int v = int(floorf(float(n_items) * (W(cc) / WG) + 0.5f));
-          return v < 0 ? 0 : (v > n_items ? n_items : v);
-        };
-        misc[0] = D;
-        misc[1] = cut(c);
-        misc[2] = cut(c + 1);
+        const int cc = c + tid;
+        int v = n_tiles;
+        if (cc < G) {
+          const float WG = W(G);
+          v = WG <= 0.0f ? 0 : int(floorf(float(n_tiles) * (W(cc) / WG) + 0.5f));
+          v = v < 0 ? 0 : (v > n_tiles ? n_tiles : v);
+        }
+        misc[1 + tid] = v;
+        if (tid == 0) misc[0] = D;
       }
       csync();
-      s.D = misc[0];
-      s.i0 = misc[1];
-      s.i1 = misc[2] > misc[1] ? misc[2] : misc[1];
-      s.nDN = (s.ntl * s.D + s.dnch - 1) / s.dnch;
-      s.bGU = s.bSD + 4 * (s.i1 - s.i0);
-      s.bDN = s.bGU + s.nDN;
-      total = s.bDN;
-      if (tid == 0) mbar_arrive(rbar);   // hands phase B to the producer warp
-      trace(5);
-      if (s.nSD > 0) {
-        // shared down needs every CTA's slice of h_sh
+      s.set_routed(D, misc[1], misc[2]);
+      if (tid == 0) mbar_arrive(rbar);   // hands the routed loads to the producer warp
+      trace(7);
+    }
+    if (i == s.bF && s.nF > 0) {
+      csync();   // every shared gate/up feature of this CTA is in h_sh
+      if (tid == 0) red_release_add(&st->shcnt, 1u);
+    }
+    if (i == s.bGU) {
+      // ---- publish my h; collect every CTA's h_sh ------------------------------
+      csync();
+      trace(9);
+      if (tid == 0) red_release_add(&st->gudone, 1u);
+      if (a.has_shared) {
         if (tid == 0) wait_geq_u32(&st->shcnt, uint32_t(G), a.status);
         csync();
         for (int j = tid; j < T * I; j += kComputeThreads) hsh[j] = __ldcg(a.h_sh + j);
+        csync();
+      }
+      trace(10);
+    }
+    if (i == s.bSD) {
+      // ---- every CTA's h -> e4m3 terms (routing weight folded into the factor)
+      if (tid == 0) wait_geq_u32(&st->gudone, uint32_t(G), a.status);
+      csync();
+      trace(11);
+      const int nb = T * k * KBi;
+      for (int b0 = warp; b0 < nb; b0 += 8 * kWarps) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int b = min(b0 + u * kWarps, nb - 1);
+          v[u] = __ldcg(a.h + (size_t)b * kMxBlock + lane);   // slot b / KBi, K-block b % KBi
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int b = b0 + u * kWarps;
+          if (b < nb) {
+            const int ex = split_block(v[u], lane, hbs + (size_t)b * kActRowKbBytes);
+            if (lane == 0) hfa[b] = act_factor(ex, sel_w[b / KBi]);
+          }
+        }
       }
       csync();
-      trace(6);
+      trace(12);
     }
-    if (i == s.bSD) trace(7);
-    if (i == s.bGU) {
-      // ---- all h blocks of every CTA: publish mine, wait, stage them ----------
-      trace(8);
-      if (tid == 0) {
-        red_release_add(&st->gudone, 1u);
-        wait_geq_u32(&st->gudone, uint32_t(G), a.status);
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        const uint32_t hb_bytes = uint32_t(T * k) * KBi * kActRowKbBytes;
-        const uint32_t he_bytes = uint32_t(T * k) * HES * 2;
-        mbar_arrive_expect_tx(hbar, hb_bytes + he_bytes);
-        bulk_g2s(hbs, a.hB, hb_bytes, hbar);
-        bulk_g2s(hes, a.hE, he_bytes, hbar);
-      }
-      csync();
-      mbar_wait(hbar, 0u, a.status);
-      csync();
-      trace(9);
-    }
-    if (i >= total) break;
+    if (i >= s.bDN) break;
 
-    const int slot = i % a.stages;
+    const int slot = i % S;
     const uint8_t* buf = ring + (size_t)slot * a.slot_bytes;
-    const unsigned long long tw0 = gtime();
-    const bool ok = csync_and(mbar_wait(&full[slot], uint32_t(i / a.stages) & 1u, a.status));
-    const unsigned long long tw1 = gtime();
-    t_wait += tw1 - tw0;
-    if (ok && i < s.nR) {
-      // ---- router rows -> logits ----------------------------------------------
+    const long long c0 = dclk();
+    mbar_wait(&full[slot], uint32_t(i / S) & 1u, a.status);
+    const long long c1 = dclk();
+    trace_add(20, c1 - c0);
+    if (i < s.nR) {
+      // ---- router rows -> logits (warp per row) ---------------------------------
       const int r = s.r0 + i * s.rch, n = min(s.rch, s.r1 - r);
-      gemv_bf16_rows<T>(buf, n, d, xs, red, gout);
-      if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T)
-        a.logits[(size_t)(tid % kDecodeMaxT) * E + r + tid / kDecodeMaxT] = gout[tid];
-    } else if (ok && i < s.bF) {
-      // ---- shared gate/up rows -> h_sh -----------------------------------------
-      const int f = s.f0 + (i - s.nR) * s.fch, n = min(s.fch, s.f1 - f);
-      gemv_bf16_rows<T>(buf, 2 * n, d, xs, red, gout);   // rows 0..n-1 gate, n..2n-1 up
-      if (tid < n * kDecodeMaxT && (tid % kDecodeMaxT) < T) {
-        const int ff = tid / kDecodeMaxT, t = tid % kDecodeMaxT;
-        a.h_sh[(size_t)t * I + f + ff] = silu_f(gout[ff * kDecodeMaxT + t]) * gout[(n + ff) * kDecodeMaxT + t];
+      if (warp < n) {
+        float v[T];
+        warp_row_dot<T>(reinterpret_cast<const uint4*>(buf + (size_t)warp * row_bytes), xs4, d / 8, lane, v);
+        if (lane == 0)
+#pragma unroll
+          for (int t = 0; t < T; ++t) a.logits[(size_t)t * E + r + warp] = v[t];
       }
-    } else if (ok && i < s.bSD) {
+    } else if (i < s.bF) {
+      // ---- shared gate/up features -> h_sh (warp per feature) --------------------
+      const int fb = (i - s.nR) * s.fch;
+      const int f = s.f0 + fb, n = min(s.fch, s.f1 - f);
+      const int ff = (warp - fb % kWarps + kWarps) % kWarps;
+      if (ff < n) {
+        float gv[T], uv[T];
+        warp_row_dot<T>(reinterpret_cast<const uint4*>(buf + (size_t)ff * row_bytes), xs4, d / 8, lane, gv);
+        warp_row_dot<T>(reinterpret_cast<const uint4*>(buf + (size_t)(n + ff) * row_bytes), xs4, d / 8, lane, uv);
+        if (lane == 0)
+#pragma unroll
+          for (int t = 0; t < T; ++t) a.h_sh[(size_t)t * I + f + ff] = silu_f(gv[t]) * uv[t];
+      }
+      trace_add(24, dclk() - c1);
+    } else if (i < s.bGU) {
+      // ---- routed gate/up tile: 8 gate + 8 up rows of one active expert -------
+      if (i == s.bF) trace(8);
+      const int jb = i - s.bF;
+      const int gt = s.i0 + jb, ai = gt / NTg, tt = gt - ai * NTg;
+      const int nt = act_n[ai];
+      const int* toks = act_tok + ai * kDecodeMaxT;
+      const int* slots = act_slot + ai * kDecodeMaxT;
+      int boff[kPairs], foff[kPairs];
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+        boff[p] = (sb < nt && (g & 3) < kActTerms) ? toks[sb] * KBd * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
+        foff[p] = sc < nt ? toks[sc] * KBd : -1;
+      }
+      float acc[kPairs][2];
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
+      // my K-blocks warp, warp+15, ...: groups of kUnroll without branches
+      // (a K-block past the end is clamped and weighted 0)
+      for (int kb0 = warp; kb0 < KBd; kb0 += kUnroll * kWarps) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int kb = kb0 + u * kWarps;
+          const bool ok = kb < KBd;
+          const int kbc = ok ? kb : KBd - 1;
+          const uint8_t* unit = buf + (size_t)kbc * kUnitBytes;
+          const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+          const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
+          const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
+#pragma unroll
+          for (int p = 0; p < kPairs; ++p) {
+            const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kbc * kActRowKbBytes)
+                                          : make_uint2(0u, 0u);
+            const float fa = foff[p] >= 0 ? xfa[foff[p] + kbc] : 0.0f;
+            float dd[4];
+            mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x,
+                     bv.y);
+            acc[p][0] = fmaf((dd[0] + dd[1]) * fa, fwl, acc[p][0]);
+            acc[p][1] = fmaf((dd[2] + dd[3]) * fa, fwh, acc[p][1]);
+          }
+        }
+      }
+      const long long c2 = dclk();
+      trace_add(21, c2 - c1);
+      trace_add(26, 1);
+      float* part = job_buffer(red, redfree, jb, warp, kRF, a.status);
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float v0 = acc[p][0] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][0], 1);
+        const float v1 = acc[p][1] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][1], 1);
+        if ((q & 1) == 0) {
+          part[p * 32 + g * 2 + (q >> 1)] = v0;        // gate row g, slot column q>>1
+          part[p * 32 + 16 + g * 2 + (q >> 1)] = v1;   // up row g
+        }
+      }
+      const bool gu_last = job_last(ctr, jb, lane);
+      const long long c3 = dclk();
+      trace_add(22, c3 - c2);
+      if (gu_last) {
+        trace_add(27, 1);
+        const float* p0 = red + (size_t)(jb % kRedSlots) * kWarps * kRF;
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          if (2 * p < nt) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += p0[w * kRF + p * 32 + lane];
+            const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
+            const int sc = 2 * p + (lane & 1);
+            if (lane < 16 && sc < nt)
+              a.h[(size_t)slots[sc] * I + tt * 8 + (lane >> 1)] = silu_f(v) * up;
+          }
+        }
+        job_done(ctr, redfree, jb, lane);
+        trace_add(23, dclk() - c3);
+      }
+    } else if (i < s.bSD) {
       // ---- shared down rows of my tiles -> y accumulators (warp per row) -------
-      const int r = s.t0 * kTileRows + (i - s.bF) * s.sdch;
+      const int r = s.t0 * kTileRows + (i - s.bGU) * s.sdch;
       const int n = min(s.sdch, (s.t0 + s.ntl) * kTileRows - r);
       for (int rr = warp; rr < n; rr += kWarps) {
         const uint4* wrow = reinterpret_cast<const uint4*>(buf + (size_t)rr * sdrow_bytes);
         float acc[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) acc[t] = 0.0f;
+#pragma unroll 3
         for (int j = lane; j < I / 8; j += 32) {
           const uint4 wv = wrow[j];
 #pragma unroll
@@ -580,152 +764,85 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const float v = warp_sum(acc[t]);
-          if (lane == 0) yacc[t * ystride + row_local] = v;
+          if (lane == 0) ysd[t * ystride + row_local] = v;
         }
       }
-    } else if (ok && i < s.bGU) {
-      // ---- routed gate/up tile (one of the 4 of a 32-feature item) -------------
-      const int j = i - s.bSD, sub = j % 4;
-      const int item = s.i0 + j / 4;
-      const int ai = item / KBi, fb = item % KBi;
-      const int nt = act_n[ai];
-      const int* slots = act_slot + ai * kDecodeMaxT;
-      const int* toks = act_tok + ai * kDecodeMaxT;
-      // lane-invariant-over-K operand offsets: B rows (token, term column), exponent rows
-      int boff[kPairs], eoff[kPairs];
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-        boff[p] = (sb < nt && (g & 3) < kActTerms) ? toks[sb] * KBd * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
-        eoff[p] = sc < nt ? toks[sc] * KBd : -1;
+    } else {
+      // ---- routed down units (one output tile per load) -> per-lane accumulators
+      trace_add(28, 1);
+      const int l = i - s.bSD, tl = l / s.nL, a0 = (l - tl * s.nL) * s.dnch, n = min(s.dnch, s.D - a0);
+      if (tl != dn_tile) {
+        if (dn_tile >= 0) flush_tile(dn_tile);
+        dn_tile = tl;
       }
-      float acc[kPairs][2];
+      const int items = n * KBi;
+      int un = dn_u0, kb = dn_k0;
+      for (int m0 = warp; m0 < items; m0 += kUnroll * kWarps) {
 #pragma unroll
-      for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
-#pragma unroll
-      for (int jj = 0; jj < kMaxKbPerWarp; ++jj) {
-        const int kb = warp + jj * kWarps;
-        if (kb < KBd) {
-          const UnitFrag f = load_unit(buf + (size_t)kb * kUnitBytes, lane);
+        for (int u = 0; u < kUnroll; ++u) {
+          const bool ok = m0 + u * kWarps < items;
+          const int uc = ok ? un : n - 1, kc = ok ? kb : KBi - 1;
+          const int ai = a0 + uc;
+          const int nt = act_n[ai];
+          const int* slots = act_slot + ai * kDecodeMaxT;
+          const int* toks = act_tok + ai * kDecodeMaxT;
+          const uint8_t* unit = buf + (size_t)uc * U_dn + (size_t)kc * kUnitBytes;
+          const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+          const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
+          const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
 #pragma unroll
           for (int p = 0; p < kPairs; ++p) {
-            if (2 * p < nt) {
-              const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kb * kActRowKbBytes)
-                                            : make_uint2(0u, 0u);
-              const int ex = eoff[p] >= 0 ? int(xe[eoff[p] + kb]) : int(kActZeroExp);
-              unit_mma(f, bv, ex, acc[p][0], acc[p][1]);
+            const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+            const bool bok = sb < nt && (g & 3) < kActTerms;
+            const uint2 bv = bok ? *reinterpret_cast<const uint2*>(hbs + (size_t)(slots[sb] * KBi + kc) * kActRowKbBytes +
+                                                                    (g & 3) * 32 + q * 8)
+                                 : make_uint2(0u, 0u);
+            const bool cok = sc < nt;
+            const float fa = cok ? hfa[slots[sc] * KBi + kc] : 0.0f;
+            const int tok = cok ? toks[sc] : -1;
+            float dd[4];
+            mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x,
+                     bv.y);
+            const float vlo = (dd[0] + dd[1]) * fa * fwl;
+            const float vhi = (dd[2] + dd[3]) * fa * fwh;
+#pragma unroll
+            for (int tt = 0; tt < T; ++tt) {
+              dacc[tt][0] += tt == tok ? vlo : 0.0f;
+              dacc[tt][1] += tt == tok ? vhi : 0.0f;
             }
           }
-        }
-      }
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        red[((warp * kPairsMax + p) * 32 + lane) * 2 + 0] = acc[p][0];
-        red[((warp * kPairsMax + p) * 32 + lane) * 2 + 1] = acc[p][1];
-      }
-      csync();
-      if (warp == 0) {
-#pragma unroll
-        for (int p = 0; p < kPairs; ++p) {
-          if (2 * p < nt) {
-            float v0 = 0.0f, v1 = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-              v0 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 0];
-              v1 += red[((w * kPairsMax + p) * 32 + lane) * 2 + 1];
-            }
-            v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, 1);
-            v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, 1);
-            const int sc = 2 * p + (q >> 1);
-            if ((q & 1) == 0 && sc < nt) hblk[sc * 32 + sub * 8 + g] = silu_f(v0) * v1;
-          }
-        }
-      }
-      csync();
-      if (sub == 3 && warp < nt) {
-        // the item's 32 features are complete: write them as e4m3 terms
-        const int sl = slots[warp];
-        const int ex = split_block(hblk[warp * 32 + lane], lane, a.hB + ((size_t)sl * KBi + fb) * kActRowKbBytes);
-        if (lane == 0) a.hE[(size_t)sl * HES + fb] = int16_t(ex);
-      }
-    } else if (ok) {
-      // ---- routed down units of my tiles -> per-lane accumulators --------------
-      const int u0 = (i - s.bGU) * s.dnch, n = min(s.dnch, s.ntl * s.D - u0);
-      for (int j = 0; j < n; ++j) {
-        const int u = u0 + j, tl = u / s.D, ai = u % s.D;
-        if (tl != dn_tile) {
-          if (dn_tile >= 0) flush_tile(dn_tile);
-  trace_put(13, t_wait);
-  trace_put(14, t_gu);
-          dn_tile = tl;
-        }
-        const int nt = act_n[ai];
-        const int* slots = act_slot + ai * kDecodeMaxT;
-        const int* toks = act_tok + ai * kDecodeMaxT;
-        const uint8_t* ubuf = buf + (size_t)j * U_dn;
-        int boff[kPairs], eoff[kPairs], tok[kPairs];
-        float wgt[kPairs];
-#pragma unroll
-        for (int p = 0; p < kPairs; ++p) {
-          const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-          boff[p] = (sb < nt && (g & 3) < kActTerms) ? slots[sb] * KBi * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
-          eoff[p] = sc < nt ? slots[sc] * HES : -1;
-          tok[p] = sc < nt ? toks[sc] : -1;
-          wgt[p] = sc < nt ? sel_w[slots[sc]] : 0.0f;
-        }
-        for (int kb = warp; kb < KBi; kb += kWarps) {
-          const UnitFrag f = load_unit(ubuf + (size_t)kb * kUnitBytes, lane);
-#pragma unroll
-          for (int p = 0; p < kPairs; ++p) {
-            if (2 * p < nt) {
-              const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(hbs + boff[p] + kb * kActRowKbBytes)
-                                            : make_uint2(0u, 0u);
-              float d4[4];
-              mma_e4m3(d4, f.a0, f.a1, f.a2, f.a3, bv.x, bv.y);
-              if (eoff[p] >= 0) {
-                const int ex = int(hes[eoff[p] + kb]);
-                const float vlo = (d4[0] + d4[1]) * (wgt[p] * block_factor(f.s_lo, ex));
-                const float vhi = (d4[2] + d4[3]) * (wgt[p] * block_factor(f.s_hi, ex));
-#pragma unroll
-                for (int tt = 0; tt < T; ++tt) {
-                  if (tt == tok[p]) {
-                    dacc[tt][0] += vlo;
-                    dacc[tt][1] += vhi;
-                  }
-                }
-              }
-            }
+          un += dn_du;
+          kb += dn_dk;
+          if (kb >= KBi) {
+            kb -= KBi;
+            ++un;
           }
         }
       }
     }
-    if (i >= s.bSD && i < s.bGU) t_gu += gtime() - tw1;
-    // after the last router load: this CTA's logits are written
-    if (i == s.nR - 1) trace(2);
-    if (i == s.nR - 1 && tid == 0) {
-      __threadfence();
-      atomicAdd(&st->bar, 1ull);
-    }
-    if (s.nF > 0 && i == s.bF - 1 && tid == 0) {
-      __threadfence();
-      atomicAdd(&st->shcnt, 1u);
-    }
-    csync();
-    if (tid == 0) mbar_arrive(&empty[slot]);   // slot free for load i + stages
+    if (i >= s.bSD) trace_add(25, dclk() - c1);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);   // my share of load i is done
   }
-  trace(12);
+  trace(13);
 
   if (dn_tile >= 0) flush_tile(dn_tile);
-  trace_put(13, t_wait);
-  trace_put(14, t_gu);
+  csync();
 
-  // y rows of my tiles
+  // y rows of my tiles: shared-down part + the warps' down partials, in warp order
   for (int j = tid; j < T * s.ntl * kTileRows; j += kComputeThreads) {
-    const int t = j / (s.ntl * kTileRows), r = j % (s.ntl * kTileRows);
-    a.y[(size_t)t * d + s.t0 * kTileRows + r] = __float2bfloat16_rn(yacc[t * ystride + r]);
+    const int t = j / (s.ntl * kTileRows), r = j - t * (s.ntl * kTileRows);
+    const int tl = r / kTileRows, rr = r - tl * kTileRows;
+    float v = ysd[t * ystride + r];
+    if (s.D > 0)
+      for (int w = 0; w < kWarps; ++w) v += dnred[((size_t)(tl * kWarps + w) * T + t) * kTileRows + rr];
+    a.y[(size_t)t * d + s.t0 * kTileRows + r] = __float2bfloat16_rn(v);
   }
   csync();
-  trace(10);
+  trace(14);
+  trace_put(18, (unsigned long long)clock64());
+#pragma unroll
+  for (int z = 0; z < 12; ++z) trace_put(20 + z, (unsigned long long)tacc[z]);
   if (tid == 0) {
     __threadfence();
     const uint32_t old = atomicAdd(&st->done, 1u);
@@ -761,22 +878,23 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t
   if (a.T < 1 || a.T > kDecodeMaxT) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.d % 32 || a.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.k < 1 || a.k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (a.E > 512 || a.d > kWarps * kMaxKbPerWarp * kMxBlock) return MOE_ERR_UNSUPPORTED_SHAPE;
-  const int NTd = a.d / kTileRows;
-  if (di.sm_count < 1 || (NTd + di.sm_count - 1) / di.sm_count > kDecodeMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a.E > 32 * kMergeChunks || a.d > kWarps * kMaxKbPerWarp * kMxBlock) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (di.sm_count < 1 || max_tiles_per_cta(a.d, di.sm_count) > kDecodeMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
   uint32_t sb = uint32_t(a.d / kMxBlock) * kUnitBytes;   // one routed gate/up tile
   const uint32_t cands[4] = {uint32_t(2 * a.d), uint32_t(4 * a.d), uint32_t(2 * a.I),
                              uint32_t(a.I / kMxBlock) * kUnitBytes};
   for (uint32_t v : cands) sb = sb > v ? sb : v;         // router row, shared feature, shared-down row, down unit
   sb = align_up(sb, 128);
-  const Smem fixed = smem_plan(a.T, a.d, a.I, a.k, 0, sb);
+  const int mt = max_tiles_per_cta(a.d, di.sm_count);
+  const Smem fixed = smem_plan(a.T, a.d, a.I, a.E, a.k, 0, sb, mt);
   const size_t budget = di.smem_optin > fixed.total + 1024 ? di.smem_optin - fixed.total - 1024 : 0;
-  int S = int(budget / (sb + 8));
+  int S = int(budget / (sb + 16));
+  if (S > kDecodeStageCap) S = kDecodeStageCap;
   if (S > kDecodeMaxStages) S = kDecodeMaxStages;
   if (S < 3) return MOE_ERR_UNSUPPORTED_SHAPE;
   *stages = S;
   *slot_bytes = sb;
-  *smem_bytes = smem_plan(a.T, a.d, a.I, a.k, S, sb).total;
+  *smem_bytes = smem_plan(a.T, a.d, a.I, a.E, a.k, S, sb, mt).total;
   return MOE_OK;
 }
 

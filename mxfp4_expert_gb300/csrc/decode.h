@@ -41,8 +41,7 @@ struct DecodeArgs {
   float* w_out;         // [T][k] or null
   __nv_bfloat16* y;     // [T][d]
   DecodeState* state;
-  uint8_t* hB;          // [T*k][I/32][96] e4m3 terms of h
-  int16_t* hE;          // [T*k][decode_he_stride(I)] block exponents of h
+  float* h;             // [T*k][I] routed SwiGLU outputs, exchanged between CTAs
   float* h_sh;          // [T][I]
   int* status;
   int stages;           // set by launch_decode

@@ -56,9 +56,9 @@ __device__ __forceinline__ int split_block(float v, int lane, uint8_t* dst) {
     e = floor_log2(amax) - 7;
     const float sv = scale2(v, -e);
     t0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
-    const float r1 = sv - e4m3_to_f32(t0);
+    const float r1 = sv - e4m3_to_f32_hw(t0);
     t1 = f32x2_to_e4m3x2(r1, 0.0f) & 0xFFu;
-    const float r2 = r1 - e4m3_to_f32(t1);
+    const float r2 = r1 - e4m3_to_f32_hw(t1);
     t2 = f32x2_to_e4m3x2(r2, 0.0f) & 0xFFu;
   }
   const int pos = ((lane & 15) >> 2) * 8 + (lane >> 4) * 4 + (lane & 3);
