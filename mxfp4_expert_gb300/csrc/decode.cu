@@ -77,12 +77,17 @@ __device__ __forceinline__ long long dclk() { return 0; }
 constexpr int kWarps = 15;                  // compute warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp that issues the bulk copies
 constexpr int kComputeThreads = kWarps * 32;
-constexpr int kRedSlots = 4;      // reduction buffers in flight
+constexpr int kGroupWarps = 3;    // warps that share one routed gate/up tile (K split in three)
+constexpr int kGroups = kWarps / kGroupWarps;   // tiles in flight per CTA
 constexpr int kRowsPerLoad = 4;   // bf16 rows per load: router rows, or 2 shared features x (gate, up)
 constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 3840
 constexpr int kMergeChunks = 16;  // top-k: E <= 16 chunks of 32 experts
-constexpr int kCtrWords = kRedSlots;   // shared arrival counters of the reduction buffers
-constexpr int kUnroll = 6;        // MMA items per warp issued back to back (no branches in between)
+#ifndef MOE_DECODE_UNROLL
+#define MOE_DECODE_UNROLL 6
+#endif
+constexpr int kUnroll = MOE_DECODE_UNROLL;   // gate/up MMA items per warp issued back to back (no branches in between)
+constexpr int kHTermBytes = 64;   // h of one (slot, K-block): 2 e4m3 terms x 32 features
+constexpr int kHGroups = 4;       // 8-feature groups per K-block, one exponent each
 
 #ifndef MOE_DECODE_STAGE_CAP
 #define MOE_DECODE_STAGE_CAP kDecodeMaxStages
@@ -101,6 +106,11 @@ __device__ __forceinline__ int csync_count(bool v) {
       : "r"(uint32_t(v)), "n"(kComputeThreads)
       : "memory");
   return int(r);
+}
+
+// Barrier among the kGroupWarps warps of group gid (ids 2.. are free).
+__device__ __forceinline__ void group_sync(int gid) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + gid), "n"(kGroupWarps * 32) : "memory");
 }
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
@@ -148,7 +158,7 @@ __device__ __forceinline__ float scale_hi(uint32_t sc16) { return __uint_as_floa
 // 2^-6 x E2M1 value and the activation block stored as terms x 2^-e, so the
 // factor is w x 2^(e+6) (0 for an all-zero block).
 __device__ __forceinline__ float act_factor(int e, float w) {
-  return e == kActZeroExp ? 0.0f : ldexpf(w, e + 6);
+  return e == kActZeroExp ? 0.0f : scale2(w, e + 6);
 }
 
 // Row (bf16, n8 chunks of 8 elements in shared memory) times T activation
@@ -173,7 +183,7 @@ __device__ __forceinline__ void warp_row_dot(const uint4* row, const uint4* xs4,
 // (hsh; dead after the shared-down rows) and the h terms (hbs, hfa) share
 // one region.
 struct Smem {
-  uint32_t ring, bars, ctr, red, ov, xs, xb, xfa, hsh, hbs, hfa, dnred, ysd, sel_e, sel_w, act, act_n,
+  uint32_t ring, bars, red, ov, xs, xb, xfa, hsh, hbs, hfa, dnred, ysd, sel_e, sel_w, act, act_n,
       act_slot, act_tok, first, misc, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -192,10 +202,10 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int
   };
   const uint32_t KBd = uint32_t(d / kMxBlock), KBi = uint32_t(I / kMxBlock), slots = uint32_t(T * k);
   s.ring = take(uint32_t(stages) * slot_bytes, 128);
-  s.bars = take(8u * uint32_t(2 * stages + kRedSlots + 1), 8);   // full[S], empty[S], redfree[], routing
-  s.ctr = take(4u * kCtrWords, 4);
+  s.bars = take(8u * uint32_t(2 * stages + 1), 8);   // full[S], empty[S], routing
   const uint32_t nch = uint32_t((E + 31) / 32), kk = uint32_t(k < 32 ? k : 32);
-  const uint32_t red_b = uint32_t(kRedSlots * kWarps * red_floats(T)) * 4u;
+  // gate/up partials: per group, two tiles in turn, one row per warp
+  const uint32_t red_b = uint32_t(kGroups * 2 * kGroupWarps * red_floats(T)) * 4u;
   const uint32_t cand_b = uint32_t(T) * nch * kk * 8u;
   s.red = take(red_b > cand_b ? red_b : cand_b, 16);
   const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
@@ -203,8 +213,8 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int
   const uint32_t xfa_b = align_up(uint32_t(T) * KBd * 4, 16);
   const uint32_t a_b = xs_b + xb_b + xfa_b;
   const uint32_t hsh_b = align_up(uint32_t(T) * I * 4, 16);
-  const uint32_t hbs_b = align_up(slots * KBi * kActRowKbBytes, 16);
-  const uint32_t hfa_b = align_up(slots * KBi * 4, 16);
+  const uint32_t hbs_b = align_up(slots * KBi * kHTermBytes, 16);
+  const uint32_t hfa_b = align_up(slots * KBi * kHGroups * 4, 16);
   const uint32_t b_b = hbs_b + hfa_b;
   uint32_t ov = a_b > hsh_b ? a_b : hsh_b;
   ov = ov > b_b ? ov : b_b;
@@ -250,38 +260,9 @@ struct Seq {
   }
 };
 
-// Routed gate/up tiles reduce through job buffers: tile j uses buffer
-// j % kRedSlots. Before the warp overwrites that buffer it waits until the
-// previous tile there has been reduced.
-__device__ __forceinline__ float* job_buffer(float* red, uint64_t* redfree, int j, int warp, int rf, int* status) {
-  const int rs = j % kRedSlots;
-  if (j >= kRedSlots) mbar_wait(&redfree[rs], uint32_t(j / kRedSlots - 1) & 1u, status);
-  return red + (size_t)(rs * kWarps + warp) * rf;
-}
-// After writing its partials: true in the warp that arrived last (it then
-// owns the reduction of job j and must call job_done).
-__device__ __forceinline__ bool job_last(uint32_t* ctr, int j, int lane) {
-  __syncwarp();
-  uint32_t old = 0;
-  if (lane == 0) {
-    __threadfence_block();
-    old = atomicAdd(&ctr[j % kRedSlots], 1u);
-  }
-  old = __shfl_sync(0xFFFFFFFFu, old, 0);
-  const bool last = old == uint32_t(kWarps - 1);
-  if (last) __threadfence_block();
-  return last;
-}
-__device__ __forceinline__ void job_done(uint32_t* ctr, uint64_t* redfree, int j, int lane) {
-  __syncwarp();
-  if (lane == 0) {
-    ctr[j % kRedSlots] = 0u;
-    mbar_arrive(&redfree[j % kRedSlots]);
-  }
-}
-
+// L: the shared-memory carve-up, computed once on the host (smem_plan).
 template <int T>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem L) {
   extern __shared__ __align__(128) uint8_t sm[];
   trace(0);
   trace_put(17, (unsigned long long)clock64());
@@ -296,13 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int max_tiles = max_tiles_per_cta(d, G);
-  const Smem L = smem_plan(T, d, I, E, k, S, a.slot_bytes, max_tiles);
   uint8_t* ring = sm + L.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
   uint64_t* empty = full + S;
-  uint64_t* redfree = empty + S;
-  uint64_t* rbar = redfree + kRedSlots;
-  uint32_t* ctr = reinterpret_cast<uint32_t*>(sm + L.ctr);
+  uint64_t* rbar = empty + S;
   float* red = reinterpret_cast<float*>(sm + L.red);
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm + L.xs);
   const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
@@ -328,12 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int ystride = max_tiles * kTileRows;
 
   Seq s;
-  s.r0 = int((long long)c * E / G);
-  s.r1 = int((long long)(c + 1) * E / G);
-  s.f0 = a.has_shared ? int((long long)c * I / G) : 0;
-  s.f1 = a.has_shared ? int((long long)(c + 1) * I / G) : 0;
-  s.t0 = int((long long)c * NTd / G);
-  s.ntl = int((long long)(c + 1) * NTd / G) - s.t0;
+  s.r0 = c * E / G;
+  s.r1 = (c + 1) * E / G;
+  s.f0 = a.has_shared ? c * I / G : 0;
+  s.f1 = a.has_shared ? (c + 1) * I / G : 0;
+  s.t0 = c * NTd / G;
+  s.ntl = (c + 1) * NTd / G - s.t0;
   s.rch = min(kRowsPerLoad, max(1, int(a.slot_bytes / row_bytes)));
   s.fch = min(kRowsPerLoad / 2, max(1, int(a.slot_bytes / (2 * row_bytes))));
   s.sdch = max(1, int(a.slot_bytes / sdrow_bytes));
@@ -384,9 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kWarps);
     }
-    for (int r = 0; r < kRedSlots; ++r) mbar_init(&redfree[r], 1);
     mbar_init(rbar, 1);
-    for (int i = 0; i < kCtrWords; ++i) ctr[i] = 0u;
     mbar_fence_init();
   }
   __syncthreads();   // the only full-CTA barrier: barriers and counters initialised
@@ -453,10 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       dacc[t][0] = dacc[t][1] = 0.0f;
     }
   };
-  // down items (unit, K-block) of a load are dealt to the warps round-robin:
-  // item m = warp + 15 j; (unit, kb) of the warp's first item and the step
-  const int dn_u0 = warp / KBi, dn_k0 = warp - dn_u0 * KBi;
-  const int dn_du = kWarps / KBi, dn_dk = kWarps - dn_du * KBi;
 
   for (int i = 0;; ++i) {
     if (i == s.nR) {
@@ -464,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       csync();   // every router row of this CTA is in the logits
       if (tid == 0 && s.nR > 0) red_release_add_u64(&st->bar, 1ull);
       // activations -> e4m3 terms (B operand of the gate/up MMAs)
-#pragma unroll 2
+#pragma unroll 1
       for (int u = warp; u < T * KBd; u += kWarps) {
         const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
         const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
@@ -479,15 +451,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       const int nch = (E + 31) / 32, kk = k < 32 ? k : 32;
       uint32_t* ckey = reinterpret_cast<uint32_t*>(red);
       uint32_t* cidx = ckey + T * nch * kk;
-      for (int task = warp; task < T * nch; task += kWarps) {
-        const int t = task / nch, ch = task - t * nch;
-        const uint32_t e = uint32_t(ch * 32 + lane);
-        uint32_t key = 0u;
-        if (int(e) < E) {
+      // all my tasks' logits are requested before the first round
+      constexpr int kTasksPerWarp = (kDecodeMaxT * kMergeChunks + kWarps - 1) / kWarps;
+      uint32_t keys[kTasksPerWarp];
+#pragma unroll
+      for (int m = 0; m < kTasksPerWarp; ++m) {
+        const int task = warp + m * kWarps, t = task / nch;
+        const int e = (task - t * nch) * 32 + lane;
+        keys[m] = 0u;
+        if (task < T * nch && e < E) {
           float v = __ldcg(a.logits + (size_t)t * E + e);
           if (a.bias) v = __fadd_rn(v, a.bias[(size_t)t * a.bias_stride + e]);
-          key = rank_key(v);
+          keys[m] = rank_key(v);
         }
+      }
+#pragma unroll
+      for (int m = 0; m < kTasksPerWarp; ++m) {
+        const int task = warp + m * kWarps;
+        if (task >= T * nch) break;
+        const uint32_t e = uint32_t((task % nch) * 32 + lane);
+        uint32_t key = keys[m];
+#pragma unroll 1
         for (int r = 0; r < kk; ++r) {
           const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key);
           const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, (m != 0u && key == m) ? e : 0xFFFFFFFFu);
@@ -509,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         int ptr = 0;
         uint32_t hk = lane < nch ? lk[0] : 0u, hi = lane < nch ? li[0] : 0xFFFFFFFFu;
         uint32_t my_e = 0u, my_key = 0u;
+#pragma unroll 1
         for (int r = 0; r < k; ++r) {
           const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, hk);
           const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, hk == wmax ? hi : 0xFFFFFFFFu);
@@ -616,23 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       if (tid == 0) wait_geq_u32(&st->gudone, uint32_t(G), a.status);
       csync();
       trace(11);
-      const int nb = T * k * KBi;
-      for (int b0 = warp; b0 < nb; b0 += 8 * kWarps) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int b = min(b0 + u * kWarps, nb - 1);
-          v[u] = __ldcg(a.h + (size_t)b * kMxBlock + lane);   // slot b / KBi, K-block b % KBi
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int b = b0 + u * kWarps;
-          if (b < nb) {
-            const int ex = split_block(v[u], lane, hbs + (size_t)b * kActRowKbBytes);
-            if (lane == 0) hfa[b] = act_factor(ex, sel_w[b / KBi]);
-          }
-        }
-      }
+      // every slot's h terms and group factors (contiguous in the workspace
+      // and in shared memory)
+      const int n16 = T * k * KBi * (kHTermBytes + kHGroups * 4) / 16;
+      for (int j = tid; j < n16; j += kComputeThreads)
+        reinterpret_cast<uint4*>(hbs)[j] = __ldcg(reinterpret_cast<const uint4*>(a.h) + j);
       csync();
       trace(12);
     }
@@ -670,80 +643,100 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       trace_add(24, dclk() - c1);
     } else if (i < s.bGU) {
       // ---- routed gate/up tile: 8 gate + 8 up rows of one active expert -------
+      // Tile jb belongs to warp group jb % kGroups; its 3 warps split K, and
+      // the group's first warp adds the 3 partials (in warp order) and writes
+      // the tile's 8 features of h per slot as the B operand of the down MMA:
+      // 2 e4m3 terms with one exponent for the 8 features.
       if (i == s.bF) trace(8);
-      const int jb = i - s.bF;
-      const int gt = s.i0 + jb, ai = gt / NTg, tt = gt - ai * NTg;
-      const int nt = act_n[ai];
-      const int* toks = act_tok + ai * kDecodeMaxT;
-      const int* slots = act_slot + ai * kDecodeMaxT;
-      int boff[kPairs], foff[kPairs];
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-        boff[p] = (sb < nt && (g & 3) < kActTerms) ? toks[sb] * KBd * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
-        foff[p] = sc < nt ? toks[sc] * KBd : -1;
-      }
-      float acc[kPairs][2];
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
-      // my K-blocks warp, warp+15, ...: groups of kUnroll without branches
-      // (a K-block past the end is clamped and weighted 0)
-      for (int kb0 = warp; kb0 < KBd; kb0 += kUnroll * kWarps) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int kb = kb0 + u * kWarps;
-          const bool ok = kb < KBd;
-          const int kbc = ok ? kb : KBd - 1;
-          const uint8_t* unit = buf + (size_t)kbc * kUnitBytes;
-          const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
-          const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
-#pragma unroll
-          for (int p = 0; p < kPairs; ++p) {
-            const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kbc * kActRowKbBytes)
-                                          : make_uint2(0u, 0u);
-            const float fa = foff[p] >= 0 ? xfa[foff[p] + kbc] : 0.0f;
-            float dd[4];
-            mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x,
-                     bv.y);
-            acc[p][0] = fmaf((dd[0] + dd[1]) * fa, fwl, acc[p][0]);
-            acc[p][1] = fmaf((dd[2] + dd[3]) * fa, fwh, acc[p][1]);
-          }
-        }
-      }
-      const long long c2 = dclk();
-      trace_add(21, c2 - c1);
-      trace_add(26, 1);
-      float* part = job_buffer(red, redfree, jb, warp, kRF, a.status);
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const float v0 = acc[p][0] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][0], 1);
-        const float v1 = acc[p][1] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][1], 1);
-        if ((q & 1) == 0) {
-          part[p * 32 + g * 2 + (q >> 1)] = v0;        // gate row g, slot column q>>1
-          part[p * 32 + 16 + g * 2 + (q >> 1)] = v1;   // up row g
-        }
-      }
-      const bool gu_last = job_last(ctr, jb, lane);
-      const long long c3 = dclk();
-      trace_add(22, c3 - c2);
-      if (gu_last) {
-        trace_add(27, 1);
-        const float* p0 = red + (size_t)(jb % kRedSlots) * kWarps * kRF;
+      const int jb = i - s.bF, gid = warp / kGroupWarps, gw = warp - gid * kGroupWarps;
+      if (gid == jb % kGroups) {
+        const int gt = s.i0 + jb, ai = gt / NTg, tt = gt - ai * NTg;
+        const int nt = act_n[ai];
+        const int* toks = act_tok + ai * kDecodeMaxT;
+        const int* slots = act_slot + ai * kDecodeMaxT;
+        int boff[kPairs], foff[kPairs];
 #pragma unroll
         for (int p = 0; p < kPairs; ++p) {
-          if (2 * p < nt) {
-            float v = 0.0f;
+          const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
+          boff[p] = (sb < nt && (g & 3) < kActTerms) ? toks[sb] * KBd * kActRowKbBytes + (g & 3) * 32 + q * 8 : -1;
+          foff[p] = sc < nt ? toks[sc] * KBd : -1;
+        }
+        float acc[kPairs][2];
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += p0[w * kRF + p * 32 + lane];
-            const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
-            const int sc = 2 * p + (lane & 1);
-            if (lane < 16 && sc < nt)
-              a.h[(size_t)slots[sc] * I + tt * 8 + (lane >> 1)] = silu_f(v) * up;
+        for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
+        // my K-blocks gw, gw+3, ...: groups of kUnroll without branches (a
+        // K-block past the end is clamped and weighted 0)
+        for (int kb0 = gw; kb0 < KBd; kb0 += kUnroll * kGroupWarps) {
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * kGroupWarps;
+            const bool ok = kb < KBd;
+            const int kbc = ok ? kb : KBd - 1;
+            const uint8_t* unit = buf + (size_t)kbc * kUnitBytes;
+            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
+            const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
+#pragma unroll
+            for (int p = 0; p < kPairs; ++p) {
+              const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kbc * kActRowKbBytes)
+                                            : make_uint2(0u, 0u);
+              const float fa = foff[p] >= 0 ? xfa[foff[p] + kbc] : 0.0f;
+              float dd[4];
+              mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x,
+                       bv.y);
+              acc[p][0] = fmaf((dd[0] + dd[1]) * fa, fwl, acc[p][0]);
+              acc[p][1] = fmaf((dd[2] + dd[3]) * fa, fwh, acc[p][1]);
+            }
           }
         }
-        job_done(ctr, redfree, jb, lane);
-        trace_add(23, dclk() - c3);
+        trace_add(21, dclk() - c1);
+        float* gbuf = red + (size_t)(gid * 2 + ((jb / kGroups) & 1)) * kGroupWarps * kRF;
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          const float v0 = acc[p][0] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][0], 1);
+          const float v1 = acc[p][1] + __shfl_xor_sync(0xFFFFFFFFu, acc[p][1], 1);
+          if ((q & 1) == 0) {
+            gbuf[gw * kRF + p * 32 + g * 2 + (q >> 1)] = v0;        // gate row g, slot column q>>1
+            gbuf[gw * kRF + p * 32 + 16 + g * 2 + (q >> 1)] = v1;   // up row g
+          }
+        }
+        group_sync(gid);
+        if (gw == 0) {
+          uint8_t* hT = reinterpret_cast<uint8_t*>(a.h);
+          float* hF = reinterpret_cast<float*>(hT + (size_t)T * k * KBi * kHTermBytes);
+          const int kbh = tt >> 2, grp = tt & 3;
+#pragma unroll
+          for (int p = 0; p < kPairs; ++p) {
+            if (2 * p < nt) {
+              float v = gbuf[p * 32 + lane];
+#pragma unroll
+              for (int w = 1; w < kGroupWarps; ++w) v += gbuf[w * kRF + p * 32 + lane];
+              const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
+              const float hv = lane < 16 ? silu_f(v) * up : 0.0f;   // feature lane>>1, slot column lane&1
+              float am = fabsf(hv);
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 8));
+              int ex = kActZeroExp;
+              uint32_t t0 = 0u, t1 = 0u;
+              if (am > 0.0f) {
+                ex = floor_log2(am) - 7;
+                const float sv = scale2(hv, -ex);
+                t0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
+                t1 = f32x2_to_e4m3x2(sv - e4m3_to_f32_hw(t0), 0.0f) & 0xFFu;
+              }
+              const int sc = 2 * p + (lane & 1);
+              if (lane < 16 && sc < nt) {
+                const int sl = slots[sc];
+                const size_t base = ((size_t)sl * KBi + kbh) * kHTermBytes + grp * 8 + (lane >> 1);
+                hT[base] = uint8_t(t0);
+                hT[base + 32] = uint8_t(t1);
+                if ((lane >> 1) == 0) hF[((size_t)sl * KBi + kbh) * kHGroups + grp] = act_factor(ex, sel_w[sl]);
+              }
+            }
+          }
+        }
+        trace_add(23, dclk() - c1);
       }
     } else if (i < s.bSD) {
       // ---- shared down rows of my tiles -> y accumulators (warp per row) -------
@@ -772,52 +765,68 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
       trace_add(28, 1);
       const int l = i - s.bSD, tl = l / s.nL, a0 = (l - tl * s.nL) * s.dnch, n = min(s.dnch, s.D - a0);
       if (tl != dn_tile) {
+        const long long f0 = dclk();
         if (dn_tile >= 0) flush_tile(dn_tile);
         dn_tile = tl;
+        trace_add(29, dclk() - f0);
       }
-      const int items = n * KBi;
-      int un = dn_u0, kb = dn_k0;
-      for (int m0 = warp; m0 < items; m0 += kUnroll * kWarps) {
+      // half units (one expert, half of K) per warp: half h of unit j of tile
+      // tl goes to warp (2 (tl * D + a0 + j) + h) % 15, so the unit's tables are
+      // read once per half and all warps take part
+      const int KBh = (KBi + 1) / 2;
+      for (int jh = 0; jh < 2 * n; ++jh) {
+        if ((2 * (tl * s.D + a0) + jh) % kWarps != warp) continue;
+        const int j = jh >> 1, kbb = (jh & 1) * KBh, kbe = min(KBi, kbb + KBh);
+        const int ai = a0 + j;
+        const int nt = act_n[ai];
+        const int* slots = act_slot + ai * kDecodeMaxT;
+        const int* toks = act_tok + ai * kDecodeMaxT;
+        const uint8_t* ub = buf + (size_t)j * U_dn;
+        // B columns: 4 groups of 8 features x 2 terms; lane (g, q) holds the
+        // C columns of group q, so the quad sum in flush_tile adds the groups
+        const int grp = g >> 1;
+        int hbo[T], hfo[T], tok[T];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const bool ok = m0 + u * kWarps < items;
-          const int uc = ok ? un : n - 1, kc = ok ? kb : KBi - 1;
-          const int ai = a0 + uc;
-          const int nt = act_n[ai];
-          const int* slots = act_slot + ai * kDecodeMaxT;
-          const int* toks = act_tok + ai * kDecodeMaxT;
-          const uint8_t* unit = buf + (size_t)uc * U_dn + (size_t)kc * kUnitBytes;
-          const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
-          const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
+        for (int si = 0; si < T; ++si) {
+          const int sl = si < nt ? slots[si] : 0;
+          hbo[si] = sl * KBi * kHTermBytes + (g & 1) * 32 + 4 * q + (grp == (q >> 1) ? 0 : 16);
+          hfo[si] = sl * KBi * kHGroups + q;
+          tok[si] = si < nt ? toks[si] : -1;
+        }
+        const bool lo_ok = grp == (q >> 1), hi_ok = grp == 2 + (q >> 1);
+        const long long k0 = dclk();
+        for (int kb0 = kbb; kb0 < kbe; kb0 += 4) {
 #pragma unroll
-          for (int p = 0; p < kPairs; ++p) {
-            const int sb = 2 * p + (g >> 2), sc = 2 * p + (q >> 1);
-            const bool bok = sb < nt && (g & 3) < kActTerms;
-            const uint2 bv = bok ? *reinterpret_cast<const uint2*>(hbs + (size_t)(slots[sb] * KBi + kc) * kActRowKbBytes +
-                                                                    (g & 3) * 32 + q * 8)
-                                 : make_uint2(0u, 0u);
-            const bool cok = sc < nt;
-            const float fa = cok ? hfa[slots[sc] * KBi + kc] : 0.0f;
-            const int tok = cok ? toks[sc] : -1;
-            float dd[4];
-            mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x,
-                     bv.y);
-            const float vlo = (dd[0] + dd[1]) * fa * fwl;
-            const float vhi = (dd[2] + dd[3]) * fa * fwh;
+          for (int u = 0; u < 4; ++u) {
+            const int kb = kb0 + u;
+            const bool ok = kb < kbe;
+            const int kc = ok ? kb : kbe - 1;
+            const uint8_t* unit = ub + (size_t)kc * kUnitBytes;
+            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
+            const float fwl = ok ? scale_lo(sc16) : 0.0f, fwh = ok ? scale_hi(sc16) : 0.0f;
+            // T = 1: no branch (one slot per expert); else skip the expert's
+            // missing slots
 #pragma unroll
-            for (int tt = 0; tt < T; ++tt) {
-              dacc[tt][0] += tt == tok ? vlo : 0.0f;
-              dacc[tt][1] += tt == tok ? vhi : 0.0f;
+            for (int si = 0; si < T; ++si) {
+              if (T > 1 && si >= nt) continue;
+              const uint32_t bw = *reinterpret_cast<const uint32_t*>(hbs + hbo[si] + kc * kHTermBytes);
+              const float fa = hfa[hfo[si] + kc * kHGroups];
+              float dd[4];
+              mma_e4m3(dd, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y),
+                       lo_ok ? bw : 0u, hi_ok ? bw : 0u);
+              const float vlo = (dd[0] + dd[1]) * fa * fwl;
+              const float vhi = (dd[2] + dd[3]) * fa * fwh;
+#pragma unroll
+              for (int tt = 0; tt < T; ++tt) {
+                dacc[tt][0] += tt == tok[si] ? vlo : 0.0f;
+                dacc[tt][1] += tt == tok[si] ? vhi : 0.0f;
+              }
             }
           }
-          un += dn_du;
-          kb += dn_dk;
-          if (kb >= KBi) {
-            kb -= KBi;
-            ++un;
-          }
         }
+        trace_add(26, dclk() - k0);
+        trace_add(27, 1);
       }
     }
     if (i >= s.bSD) trace_add(25, dclk() - c1);
@@ -900,6 +909,7 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t
 
 template <int T>
 int launch_decode_t(DecodeArgs a, uint32_t smem, const DeviceInfo& di, cudaStream_t s) {
+  const Smem L = smem_plan(T, a.d, a.I, a.E, a.k, a.stages, a.slot_bytes, max_tiles_per_cta(a.d, di.sm_count));
   MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
   int per_sm = 0;
   MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, kThreads, smem));
@@ -914,7 +924,7 @@ int launch_decode_t(DecodeArgs a, uint32_t smem, const DeviceInfo& di, cudaStrea
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_kernel<T>, a));
+  MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, decode_kernel<T>, a, L));
   return MOE_OK;
 }
 
