@@ -254,7 +254,7 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
   ra.act_b = at<uint8_t>(B, ws.x_b);
   ra.act_e = at<int16_t>(B, ws.x_e);
   ra.act_by_token = 1;
-  ra.max_items = max_active * ra.n_tiles;
+  ra.max_items = (max_active + (T * k + 7) / 8) * ra.n_tiles;   // (expert, 8-row chunk, tile) items
   ra.out = at<float>(B, ws.h);
   ra.out_ld = I;
   ra.status = status;
@@ -275,7 +275,7 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
   rd.act_b = at<uint8_t>(B, ws.h_b);
   rd.act_e = at<int16_t>(B, ws.h_e);
   rd.act_by_token = 0;
-  rd.max_items = max_active * rd.n_tiles;
+  rd.max_items = (max_active + (T * k + 7) / 8) * rd.n_tiles;
   rd.out = at<float>(B, ws.part);
   rd.out_ld = d;
   if ((st = launch_routed(kModeDown, rd, di, s))) return st;
