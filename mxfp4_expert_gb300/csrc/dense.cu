@@ -1,7 +1,22 @@
-// bf16 GEMVs on CUDA cores: the router (E rows) and the shared expert's gate
-// and up projections (routing-independent, one kernel), and the final
-// combine: shared down projection plus the routing-weighted sum of the routed
-// experts' outputs, rounded to bf16.
+// bf16 GEMMs on the warp-level tensor-core MMA (m16n8k16, fp32 accumulate)
+// for the routing-independent dense parts of the per-stage path:
+//   * the router and the shared expert's gate/up projections in one kernel
+//     (SwiGLU in the epilogue), and
+//   * the combine: the shared down projection plus the routing-weighted sum of
+//     the routed experts' outputs, rounded to bf16.
+//
+// C[weight row][token] = sum_k W[row][k] * X[token][k]: the weight rows are
+// the MMA's M dimension (16 per warp), the tokens its N dimension (8 per MMA),
+// both operands K-contiguous in memory. A block computes 64 weight rows x 64
+// tokens; K goes in steps of 32 through padded shared-memory tiles (80-byte
+// rows, so the ldmatrix row reads hit distinct banks), with the next step's
+// tiles loaded into registers while the current one is multiplied.
+//
+// In the first kernel the shared gate and up rows are interleaved 8 + 8 per
+// 16-row tile (the MMA16_GATEUP idea), so one lane holds gate and up of the
+// same feature for the SwiGLU. The shared down projection reads h_sh (fp32)
+// as two bf16 terms, hi = bf16(h) and lo = bf16(h - hi), about 16 significant
+// bits, with one MMA per term.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -11,123 +26,173 @@
 namespace moe {
 namespace {
 
-constexpr int kTokChunk = 8;    // activation rows held in shared memory per pass
-constexpr int kDenseWarps = 8;
+constexpr int kBM = 64;            // weight rows per block
+constexpr int kBN = 64;            // tokens per block
+constexpr int kBK = 32;            // K per step
+constexpr int kLd = kBK + 8;       // shared-memory row, bf16 elements (80 bytes)
+constexpr int kDWarps = kBM / 16;  // each warp: 16 weight rows x 64 tokens
+constexpr int kDThreads = kDWarps * 32;
 
-// sum over 8 bf16 weights (one uint4) times 8 fp32 activations
-__device__ __forceinline__ float dot8(uint4 w, const float* x) {
-  const float4 xa = *reinterpret_cast<const float4*>(x);
-  const float4 xb = *reinterpret_cast<const float4*>(x + 4);
-  float s = bf16_lo(w.x) * xa.x;
-  s = fmaf(bf16_hi(w.x), xa.y, s);
-  s = fmaf(bf16_lo(w.y), xa.z, s);
-  s = fmaf(bf16_hi(w.y), xa.w, s);
-  s = fmaf(bf16_lo(w.z), xb.x, s);
-  s = fmaf(bf16_hi(w.z), xb.y, s);
-  s = fmaf(bf16_lo(w.w), xb.z, s);
-  s = fmaf(bf16_hi(w.w), xb.w, s);
-  return s;
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
+// Weight row n of the first kernel: router rows [0, Ep) (rows >= E are zero),
+// then the shared expert's rows in 16-row tiles of 8 gate + 8 up rows.
+__device__ __forceinline__ const __nv_bfloat16* front_row(const FrontArgs& a, int Ep, int n) {
+  if (n < Ep) return n < a.E ? a.router_w + (size_t)n * a.d : nullptr;
+  const int s = n - Ep;
+  if (!a.sh_gate || s >= 2 * a.I) return nullptr;
+  const int f = (s >> 4) * 8 + (s & 7);
+  return ((s & 8) ? a.sh_up : a.sh_gate) + (size_t)f * a.d;
 }
 
-// Items: router rows e in [0, E), then shared features i in [0, I) (gate row i
-// and up row i together). One warp per item; lanes stride K by 8 elements.
-__global__ void __launch_bounds__(kDenseWarps * 32)
-front_kernel(FrontArgs a) {
-  extern __shared__ __align__(16) float xs[];   // [kTokChunk][d]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n_items = a.E + (a.sh_gate ? a.I : 0);
-  for (int t0 = 0; t0 < a.T; t0 += kTokChunk) {
-    const int tn = min(kTokChunk, a.T - t0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < tn * a.d; i += blockDim.x)
-      xs[i] = __bfloat162float(a.x[(size_t)t0 * a.d + i]);
-    __syncthreads();
-    for (int item = blockIdx.x * kDenseWarps + warp; item < n_items; item += gridDim.x * kDenseWarps) {
-      const bool router = item < a.E;
-      const __nv_bfloat16* r0 = router ? a.router_w + (size_t)item * a.d
-                                       : a.sh_gate + (size_t)(item - a.E) * a.d;
-      const __nv_bfloat16* r1 = router ? nullptr : a.sh_up + (size_t)(item - a.E) * a.d;
-      float acc0[kTokChunk], acc1[kTokChunk];
+// MODE 0: router + shared gate/up (FrontArgs). MODE 1: shared down + combine
+// (CombineArgs). Both share the tiling; P carries the mode's arguments.
+template <int MODE, typename P>
+__global__ void __launch_bounds__(kDThreads)
+dense_kernel(P a, int Ep, int N, int K) {
+  __shared__ __align__(16) __nv_bfloat16 Ws[kBM * kLd];
+  __shared__ __align__(16) __nv_bfloat16 Xh[kBN * kLd];
+  __shared__ __align__(16) __nv_bfloat16 Xl[MODE == 1 ? kBN * kLd : 8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n0 = blockIdx.x * kBM, t0 = blockIdx.y * kBN;
+  const int T = a.T;
+  bool have_w = true;
+  if constexpr (MODE == 1) have_w = a.sh_down != nullptr;
+
+  // per thread: 2 chunks of 16 bytes of the weight tile and of the token tile
+  // (4 x 8 fp32 of h_sh in MODE 1), rows tid / 4 and tid / 4 + 32, column (tid % 4) * 8
+  const __nv_bfloat16* wrow[2];
+  const void* xrow[2];
+  const int cr = tid >> 2, cc = (tid & 3) * 8;
 #pragma unroll
-      for (int tt = 0; tt < kTokChunk; ++tt) acc0[tt] = acc1[tt] = 0.0f;
-#pragma unroll 4
-      for (int j = lane * 8; j < a.d; j += 256) {
-        const uint4 w0 = ldg_nc_stream_u4(r0 + j);
-        uint4 w1 = make_uint4(0, 0, 0, 0);
-        if (!router) w1 = ldg_nc_stream_u4(r1 + j);
+  for (int h = 0; h < 2; ++h) {
+    const int r = cr + 32 * h;
+    if constexpr (MODE == 0) {
+      wrow[h] = front_row(a, Ep, n0 + r);
+      xrow[h] = t0 + r < T ? static_cast<const void*>(a.x + (size_t)(t0 + r) * K) : nullptr;
+    } else {
+      wrow[h] = (have_w && n0 + r < N) ? a.sh_down + (size_t)(n0 + r) * K : nullptr;
+      xrow[h] = t0 + r < T ? static_cast<const void*>(a.h_sh + (size_t)(t0 + r) * K) : nullptr;
+    }
+  }
+  uint4 wreg[2], xh[2], xl[2];
+  auto load = [&](int k0) {
 #pragma unroll
-        for (int tt = 0; tt < kTokChunk; ++tt) {
-          if (tt < tn) {
-            acc0[tt] += dot8(w0, xs + tt * a.d + j);
-            if (!router) acc1[tt] += dot8(w1, xs + tt * a.d + j);
-          }
+    for (int h = 0; h < 2; ++h) {
+      wreg[h] = wrow[h] ? ldg_nc_stream_u4(wrow[h] + k0 + cc) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (MODE == 0) {
+        xh[h] = xrow[h] ? __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xrow[h]) + k0 + cc))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (xrow[h]) {
+          const float4 u0 = *reinterpret_cast<const float4*>(static_cast<const float*>(xrow[h]) + k0 + cc);
+          const float4 u1 = *reinterpret_cast<const float4*>(static_cast<const float*>(xrow[h]) + k0 + cc + 4);
+          v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
+          v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
         }
-      }
+        uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int tt = 0; tt < kTokChunk; ++tt) {
-        if (tt < tn) {
-          const float g = warp_sum(acc0[tt]);
-          const float u = router ? 0.0f : warp_sum(acc1[tt]);
-          if (lane == 0) {
-            if (router) a.logits[(size_t)(t0 + tt) * a.E + item] = g;
-            else a.h_sh[(size_t)(t0 + tt) * a.I + (item - a.E)] = silu_f(g) * u;
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = __bfloat162float(__float2bfloat16_rn(v[2 * e]));
+          const float a1 = __bfloat162float(__float2bfloat16_rn(v[2 * e + 1]));
+          hi[e] = pack_bf16(a0, a1);
+          lo[e] = pack_bf16(v[2 * e] - a0, v[2 * e + 1] - a1);
+        }
+        xh[h] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        xl[h] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+  };
+  auto store = [&]() {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = cr + 32 * h;
+      *reinterpret_cast<uint4*>(Ws + r * kLd + cc) = wreg[h];
+      *reinterpret_cast<uint4*>(Xh + r * kLd + cc) = xh[h];
+      if constexpr (MODE == 1) *reinterpret_cast<uint4*>(Xl + r * kLd + cc) = xl[h];
+    }
+  };
+
+  float acc[kBN / 8][4];
+#pragma unroll
+  for (int j = 0; j < kBN / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+
+  if (have_w) {
+    load(0);
+    for (int k0 = 0; k0 < K; k0 += kBK) {
+      __syncthreads();   // the previous step's tiles are no longer read
+      store();
+      __syncthreads();
+      if (k0 + kBK < K) load(k0 + kBK);   // next step's tiles in flight during the MMAs
+#pragma unroll
+      for (int ks = 0; ks < kBK; ks += 16) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(a0, a1, a2, a3, Ws + (warp * 16 + (lane & 15)) * kLd + ks + (lane >> 4) * 8);
+#pragma unroll
+        for (int j = 0; j < kBN / 8; j += 2) {
+          const int xr = j * 8 + (lane & 7) + ((lane >> 4) << 3), xc = ks + ((lane >> 3) & 1) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b0, b1, b2, b3, Xh + xr * kLd + xc);
+          mma_bf16(acc[j], a0, a1, a2, a3, b0, b1);
+          mma_bf16(acc[j + 1], a0, a1, a2, a3, b2, b3);
+          if constexpr (MODE == 1) {
+            ldsm_x4(b0, b1, b2, b3, Xl + xr * kLd + xc);
+            mma_bf16(acc[j], a0, a1, a2, a3, b0, b1);
+            mma_bf16(acc[j + 1], a0, a1, a2, a3, b2, b3);
           }
         }
       }
     }
   }
-}
 
-// One block per 16 output rows. Phase 1: shared down rows dot h_sh (warps
-// split rows, lanes split I). Phase 2: y = shared + sum_j w[t][j] * part[slot][r].
-__global__ void __launch_bounds__(kDenseWarps * 32)
-combine_kernel(CombineArgs a) {
-  extern __shared__ __align__(16) float sm[];    // h_sh chunk [kTokChunk][I], then sh_out[kTokChunk][16]
-  float* hs = sm;
-  float* sh_out = sm + kTokChunk * a.I;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r0 = blockIdx.x * 16;
-  for (int t0 = 0; t0 < a.T; t0 += kTokChunk) {
-    const int tn = min(kTokChunk, a.T - t0);
-    __syncthreads();
-    if (a.sh_down) {
-      for (int i = threadIdx.x; i < tn * a.I; i += blockDim.x) hs[i] = a.h_sh[(size_t)t0 * a.I + i];
-    }
-    __syncthreads();
-    for (int rr = warp; rr < 16; rr += kDenseWarps) {
-      float acc[kTokChunk];
+  // lane (g, q): rows m = n0 + 16 warp + g (c[0], c[1]) and m + 8 (c[2], c[3]),
+  // tokens t0 + 8 j + 2 q + {0, 1}
+  const int g = lane >> 2, q = lane & 3;
+  const int m = n0 + warp * 16 + g;
 #pragma unroll
-      for (int tt = 0; tt < kTokChunk; ++tt) acc[tt] = 0.0f;
-      if (a.sh_down) {
-        const __nv_bfloat16* wr = a.sh_down + (size_t)(r0 + rr) * a.I;
-        for (int j = lane * 8; j < a.I; j += 256) {
-          const uint4 w = ldg_nc_stream_u4(wr + j);
+  for (int j = 0; j < kBN / 8; ++j) {
 #pragma unroll
-          for (int tt = 0; tt < kTokChunk; ++tt)
-            if (tt < tn) acc[tt] += dot8(w, hs + tt * a.I + j);
+    for (int u = 0; u < 2; ++u) {
+      const int t = t0 + j * 8 + 2 * q + u;
+      if (t >= T) continue;
+      if constexpr (MODE == 0) {
+        if (n0 + warp * 16 < Ep) {
+          if (m < a.E) a.logits[(size_t)t * a.E + m] = acc[j][u];
+          if (m + 8 < a.E) a.logits[(size_t)t * a.E + m + 8] = acc[j][2 + u];
+        } else if (a.sh_gate) {
+          const int s = m - Ep;   // gate row of feature f in c[u], its up row in c[2 + u]
+          const int f = (s >> 4) * 8 + (s & 7);
+          if (f < a.I) a.h_sh[(size_t)t * a.I + f] = silu_f(acc[j][u]) * acc[j][2 + u];
+        }
+      } else {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = m + 8 * hh;
+          if (r >= N) continue;
+          float y = acc[j][2 * hh + u];
+          for (int jj = 0; jj < a.k; ++jj) {
+            const int slot = a.inv[(size_t)t * a.k + jj];
+            if (slot >= 0) y = fmaf(a.w[(size_t)t * a.k + jj], a.part[(size_t)slot * a.d + r], y);
+          }
+          a.y[(size_t)t * a.d + r] = __float2bfloat16_rn(y);
         }
       }
-#pragma unroll
-      for (int tt = 0; tt < kTokChunk; ++tt) {
-        const float v = warp_sum(acc[tt]);
-        if (lane == 0 && tt < tn) sh_out[tt * 16 + rr] = v;
-      }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < tn * 16; i += blockDim.x) {
-      const int tt = i >> 4, r = i & 15, t = t0 + tt;
-      float y = sh_out[tt * 16 + r];
-      for (int j = 0; j < a.k; ++j) {
-        const int slot = a.inv[(size_t)t * a.k + j];
-        if (slot >= 0) y = fmaf(a.w[(size_t)t * a.k + j], a.part[(size_t)slot * a.d + r0 + r], y);
-      }
-      a.y[(size_t)t * a.d + r0 + r] = __float2bfloat16_rn(y);
     }
   }
 }
@@ -135,20 +200,18 @@ combine_kernel(CombineArgs a) {
 }  // namespace
 
 int launch_front(const FrontArgs& a, const DeviceInfo& di, cudaStream_t s) {
-  const size_t smem = sizeof(float) * kTokChunk * a.d;
-  MOE_CUDA_TRY(cudaFuncSetAttribute(front_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-  const int n_items = a.E + (a.sh_gate ? a.I : 0);
-  int grid = (n_items + kDenseWarps - 1) / kDenseWarps;
-  if (grid > di.sm_count * 2) grid = di.sm_count * 2;
-  front_kernel<<<grid, kDenseWarps * 32, smem, s>>>(a);
+  (void)di;
+  const int Ep = (a.E + 15) / 16 * 16;
+  const int N = Ep + (a.sh_gate ? 2 * a.I : 0);
+  const dim3 grid((N + kBM - 1) / kBM, (a.T + kBN - 1) / kBN);
+  dense_kernel<0, FrontArgs><<<grid, kDThreads, 0, s>>>(a, Ep, N, a.d);
   return launch_status();
 }
 
 int launch_combine(const CombineArgs& a, const DeviceInfo& di, cudaStream_t s) {
   (void)di;
-  const size_t smem = sizeof(float) * (kTokChunk * a.I + kTokChunk * 16);
-  MOE_CUDA_TRY(cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
-  combine_kernel<<<a.d / 16, kDenseWarps * 32, smem, s>>>(a);
+  const dim3 grid((a.d + kBM - 1) / kBM, (a.T + kBN - 1) / kBN);
+  dense_kernel<1, CombineArgs><<<grid, kDThreads, 0, s>>>(a, 0, a.d, a.I);
   return launch_status();
 }
 
