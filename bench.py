@@ -383,7 +383,8 @@ def run_ours(args, w):
     achieved = dom_bytes / (stage_mean[dom] * 1e-6) / 1e9
     kernel_src = os.path.join(ROOT, "mxfp4_expert_gb300", "csrc",
                               "decode.cu" if dom == "decode_fused" else
-                              "experts.cu" if dom.startswith("routed") else "dense.cu")
+                              ("umma.cu" if "routed_down" in stage_mean and "act_split_h" not in stage_mean
+                               else "experts.cu") if dom.startswith("routed") else "dense.cu")
     traffic = profiled_traffic(kernel_src, dom)
     algo_bytes = float(np.mean([weight_bytes_per_call(w, D) for D in D_sets]))
     eff_gbs = algo_bytes * calls * ws / (ms * 1e-3) / 1e9     # whole-job weight bytes per second

@@ -133,9 +133,13 @@ typedef struct moe_layer {
 typedef enum moe_path {
   MOE_PATH_DECODE_MMA = 1,   /* per-stage kernels: router GEMV, top-k + sort,
                                 MXFP4 expert GEMVs on e4m3 mma.sync, combine */
-  MOE_PATH_DECODE_FUSED = 2  /* T <= 4: one cooperative persistent kernel per
+  MOE_PATH_DECODE_FUSED = 2, /* T <= 4: one cooperative persistent kernel per
                                 call (router, top-k, shared and routed experts,
                                 combine), one CTA per SM */
+  MOE_PATH_PREFILL_TC = 3    /* T >= 32: per-stage kernels with the routed
+                                experts as grouped GEMMs on the tcgen05 tensor
+                                cores (MXFP4 decoded to bf16 in shared memory,
+                                fp32 accumulators in tensor memory) */
 } moe_path;
 
 /* ---- packing ------------------------------------------------------------ */

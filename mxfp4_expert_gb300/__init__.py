@@ -15,7 +15,7 @@ import torch
 
 __all__ = [
     "MoeError", "LIB_PATH", "lib", "MOE_LAYOUT_MMA16", "MOE_LAYOUT_MMA16_GATEUP",
-    "MOE_PATH_DECODE_MMA", "MOE_PATH_DECODE_FUSED", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
+    "MOE_PATH_DECODE_MMA", "MOE_PATH_DECODE_FUSED", "MOE_PATH_PREFILL_TC", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
@@ -30,6 +30,7 @@ MOE_LAYOUT_MMA16 = 1
 MOE_LAYOUT_MMA16_GATEUP = 2
 MOE_PATH_DECODE_MMA = 1
 MOE_PATH_DECODE_FUSED = 2
+MOE_PATH_PREFILL_TC = 3
 DEV_NONFINITE_INPUT, DEV_SCALE_RANGE, DEV_INDEX_OOB, DEV_TIMEOUT = 1, 2, 4, 8
 STATIC_SCRATCH_BYTES = 4 * 1024 * 1024
 

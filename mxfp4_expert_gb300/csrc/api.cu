@@ -108,8 +108,12 @@ extern "C" size_t moe_workspace_bytes(const moe_shape* shape, int T) {
   return plan(*shape, T).total;
 }
 
+// Tokens from which the routed experts run as tcgen05 grouped GEMMs.
+constexpr int kPrefillMinT = 32;
+
 // Path for (shape, T) on the current device: the single-launch decode kernel
-// when T <= 4 and the shape fits it, else the per-stage kernels.
+// when T <= 4 and the shape fits it; the per-stage kernels with tcgen05
+// routed GEMMs from kPrefillMinT tokens; else the per-stage kernels.
 static int select_path(const moe_shape& sh, int T, const DeviceInfo& di) {
   DecodeArgs probe{};
   probe.T = T;
@@ -120,6 +124,7 @@ static int select_path(const moe_shape& sh, int T, const DeviceInfo& di) {
   int stages;
   uint32_t slot, smem;
   if (T <= kDecodeMaxT && decode_plan(probe, di, &stages, &slot, &smem) == MOE_OK) return MOE_PATH_DECODE_FUSED;
+  if (T >= kPrefillMinT) return MOE_PATH_PREFILL_TC;
   return MOE_PATH_DECODE_MMA;
 }
 
@@ -217,9 +222,12 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
     return mark();
   }
 
-  // 1. activations -> e4m3 B-operand terms
-  if ((st = launch_act_split(x, true, T, d, at<uint8_t>(B, ws.x_b), at<int16_t>(B, ws.x_e), di, s))) return st;
-  if ((st = mark())) return st;
+  const bool tc = select_path(sh, T, di) == MOE_PATH_PREFILL_TC;
+  // 1. activations -> e4m3 B-operand terms (the tcgen05 path reads x as bf16)
+  if (!tc) {
+    if ((st = launch_act_split(x, true, T, d, at<uint8_t>(B, ws.x_b), at<int16_t>(B, ws.x_e), di, s))) return st;
+    if ((st = mark())) return st;
+  }
   // 2. router logits and shared gate/up (routing-independent)
   FrontArgs fa{x, T, d, E, I, static_cast<const __nv_bfloat16*>(L->router_w),
                sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_gate) : nullptr,
@@ -240,6 +248,44 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
     return st;
   if ((st = mark())) return st;
   const int max_active = T * k < E ? T * k : E;
+  if (tc) {
+    // routed gate/up (x rows as bf16) -> h as bf16 hi + lo terms; routed down
+    // (both terms as separate columns) -> part [slots][d]; both on tcgen05
+    RoutedArgs ua{};
+    ua.w = static_cast<const uint8_t*>(L->gate_up);
+    ua.mat_bytes = L->gate_up_desc.bytes_per_mat;
+    ua.n_tiles = 2 * I / kTileRows;
+    ua.KB = d / kMxBlock;
+    ua.active = active;
+    ua.n_active = n_active;
+    ua.offsets = offsets;
+    ua.perm = perm;
+    ua.k = k;
+    ua.act_raw = x;
+    ua.n_rows = T * k;
+    ua.out = at<float>(B, ws.h);   // written as bf16 hi [slots][I], then lo [slots][I]
+    ua.out_ld = I;
+    ua.status = status;
+    if ((st = launch_umma_routed(kModeGateUp, ua, di, s))) return st;
+    if ((st = mark())) return st;
+    RoutedArgs ud = ua;
+    ud.w = static_cast<const uint8_t*>(L->down);
+    ud.mat_bytes = L->down_desc.bytes_per_mat;
+    ud.n_tiles = d / kTileRows;
+    ud.KB = I / kMxBlock;
+    ud.act_raw = at<__nv_bfloat16>(B, ws.h);
+    ud.act_raw2 = at<__nv_bfloat16>(B, ws.h) + (size_t)T * k * I;
+    ud.out = at<float>(B, ws.part);
+    ud.out_ld = d;
+    if ((st = launch_umma_routed(kModeDown, ud, di, s))) return st;
+    if ((st = mark())) return st;
+    CombineArgs ca{T, d, I, k,
+                   sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_down) : nullptr,
+                   at<float>(B, ws.h_sh), w, inv, at<float>(B, ws.part),
+                   static_cast<__nv_bfloat16*>(y_dev)};
+    if ((st = launch_combine(ca, di, s))) return st;
+    return mark();
+  }
   // 5. routed gate/up + SwiGLU -> h [slots][I]
   RoutedArgs ra{};
   ra.w = static_cast<const uint8_t*>(L->gate_up);
@@ -341,6 +387,7 @@ extern "C" const char* moe_stage_names(int path) {
   if (path == MOE_PATH_DECODE_FUSED) return "decode_fused";
   if (path == MOE_PATH_DECODE_MMA)
     return "act_split_x,router_shared_gateup,topk,sort,routed_gateup,act_split_h,routed_down,combine";
+  if (path == MOE_PATH_PREFILL_TC) return "router_shared_gateup,topk,sort,routed_gateup,routed_down,combine";
   return nullptr;
 }
 

@@ -36,15 +36,23 @@ struct RoutedArgs {
   const int32_t* offsets;   // [E+1] sorted-slot offsets per expert
   const int32_t* perm;      // sorted slot -> p = t*k + j
   int k;
-  const uint8_t* act_b;     // B-operand rows
+  const uint8_t* act_b;     // B-operand rows (e4m3 terms)
   const int16_t* act_e;
+  const void* act_raw;      // tensor-core path: x (bf16 [T][K]) for gate/up; h hi terms (bf16 [slots][K]) for down
+  const void* act_raw2;     // tensor-core path, down: h lo terms (bf16 [slots][K])
+  int n_rows;               // tensor-core path: slots (rows of h)
   int act_by_token;         // 1: activation row = perm[slot] / k; 0: = slot
   int max_items;            // upper bound on n_active * n_tiles (grid sizing)
   float* out;               // gate/up: h [slots][N/2]; down: part [slots][N]
+                            // (tensor-core gate/up: h as bf16 hi [slots][N/2] then lo [slots][N/2])
   int out_ld;
   int* status;
 };
 int launch_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+// umma.cu: the same routed GEMMs on tcgen05 (bf16 operands decoded from
+// MXFP4 in shared memory, fp32 accumulator in tensor memory), for large T.
+int launch_umma_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
 
 // dense.cu
 struct FrontArgs {
