@@ -4,25 +4,34 @@
 // Work items are (active expert, block of 128 weight rows = 8 packed 16-row
 // tiles, block of that expert's rows / tokens), split into contiguous ranges
 // per CTA (one CTA per SM, persistent). Along K an item goes in slices of two
-// 32-wide K-blocks:
-//   * a producer thread streams the slice's packed MXFP4 bytes (8 tiles x 2
-//     units of 272 bytes) into a ring of shared-memory slots with 1-D bulk
-//     copies, several slices ahead;
-//   * the 8 warps decode them (one tile each) into bf16 with the E8M0 block
-//     scale applied (exact), in the K-major no-swizzle layout the MMA reads
-//     (8-row x 16-byte core matrices);
-//   * the slice of the activation rows (bf16 x; for the down projection h as
-//     two bf16 terms, hi and lo, in separate columns) is copied into the same
-//     layout with cp.async two slices ahead;
-//   * one thread issues the slice's tcgen05.mma (kind::f16, M = 128, N = the
-//     item's column count, K = 16 each) into an fp32 accumulator in tensor
-//     memory and commits them to an mbarrier.
-// Slices use four shared-memory buffers in turn, so the loads and the decode
-// of the next slices overlap the MMAs of the previous ones. At the end of an
-// item the accumulator is read back with tcgen05.ld: SwiGLU of the gate and up
-// rows of a tile (they sit 8 TMEM lanes apart), written as bf16 hi and lo
-// terms for the down pass; or, for the down pass, the sum of the hi and lo
-// columns.
+// 32-wide K-blocks. The CTA is a pipeline of warp roles that meet only at
+// mbarriers (no block-wide barrier per slice):
+//   * producer (one thread): 1-D bulk copies of the packed MXFP4 bytes of a
+//     chunk of 4 slices (8 tiles x 8 units of 272 bytes; one copy per tile,
+//     since small copies are issued too slowly) into a ring of raw slots.
+//     The ring is too small to cover the HBM latency on its own, so whole
+//     items are also prefetched into L2 about 8 chunks ahead;
+//   * 8 decode warps (one tile each): raw slot -> bf16 with the E8M0 block
+//     scale applied (exact, integer and bf16-multiply instructions only), in
+//     the K-major 128-byte-swizzled operand layout the MMA reads;
+//   * 4 loader warps: the slice of the activation rows (bf16 x gathered by
+//     token; for the down projection h as two bf16 terms, hi and lo, in
+//     separate columns) copied with cp.async into the same layout; each
+//     thread's copies arrive on the stage's barrier when they land
+//     (cp.async.mbarrier.arrive.noinc), so a loader never waits for its own
+//     copies, and the MMA thread fences the generic -> async proxy after it
+//     has seen the barrier complete;
+//   * MMA (one thread): tcgen05.mma kind::f16, M = 128, N = the item's column
+//     count, K = 16, into one of two fp32 accumulators in tensor memory; each
+//     slice's MMAs are committed to the barrier that frees its operand stage,
+//     the item's last slice also to the accumulator's "full" barrier;
+//   * 4 epilogue warps (one per 32-lane quarter of tensor memory): tcgen05.ld,
+//     then SwiGLU of the gate and up rows of a tile (8 lanes apart) written as
+//     bf16 hi and lo terms, or for the down pass the sum of the hi and lo
+//     columns; then the accumulator is released to the next item but one.
+// Every wait is bounded; a timeout sets MOE_DEV_TIMEOUT and an abort flag that
+// ends the other roles' waits at once, and the kernel drains its own copies
+// and MMAs before it frees tensor memory and returns.
 #include <cuda_runtime.h>
 #ifdef MOE_UMMA_TRACE
 #include <cstdio>
@@ -36,22 +45,30 @@
 namespace moe {
 namespace {
 
-constexpr int kUWarps = 8;
-constexpr int kUThreads = kUWarps * 32;
-constexpr int kURows = 128;                 // weight rows per item (MMA M)
-constexpr int kUTiles = kURows / kTileRows; // packed tiles per item (one per warp)
-constexpr int kUSliceKb = 2;                // 32-wide K-blocks per slice
+constexpr int kURows = 128;                  // weight rows per item (MMA M)
+constexpr int kUTiles = kURows / kTileRows;  // packed tiles per item (one per decode warp)
+constexpr int kUSliceKb = 2;                 // 32-wide K-blocks per slice
 constexpr int kUSliceK = kUSliceKb * kMxBlock;
-constexpr int kUBuf = 4;                    // operand buffers (slice s uses s % 4)
-constexpr int kURing = 10;                  // packed weight slices in flight
-constexpr int kUCols = 128;                 // TMEM columns = largest MMA N
+constexpr int kUStages = 5;                  // operand stages (bf16 weights + activations)
+constexpr int kUChunk = 4;                   // slices per raw weight copy
+constexpr int kURing = 3;                    // raw weight chunks in flight
+constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about this many chunks ahead
+constexpr int kUAcc = 2;                     // accumulators in tensor memory
+constexpr int kUCols = 128;                  // columns per accumulator = largest MMA N
 constexpr int kUMaxActive = 1024;
-constexpr uint32_t kURawBytes = kUTiles * kUSliceKb * kUnitBytes;   // one slice of packed weights
+constexpr uint32_t kUTileChunk = kUChunk * kUSliceKb * kUnitBytes;   // one tile's part of a chunk
+constexpr uint32_t kURawBytes = kUTiles * kUTileChunk;                  // one chunk of packed weights
 constexpr uint32_t kUABytes = kURows * kUSliceK * 2;                 // one slice of bf16 weights
 constexpr uint32_t kUBBytes = kUCols * kUSliceK * 2;                 // one slice of bf16 activations
 
+// warp roles
+constexpr int kWProducer = 0, kWMma = 1, kWEpi = 2, kNEpi = 4, kWLoad = kWEpi + kNEpi, kNLoad = 4,
+              kWDec = kWLoad + kNLoad, kNDec = kUTiles;
+constexpr int kUBlock = (kWDec + kNDec) * 32;
+constexpr int kScanThreads = 256;
+
 struct UmmaSmem {
-  uint32_t ring, a, b, iofs, bars, tslot, total;
+  uint32_t ring, a, b, iofs, bars, misc, total;
 };
 __host__ __device__ inline UmmaSmem umma_smem() {
   UmmaSmem m{};
@@ -63,34 +80,50 @@ __host__ __device__ inline UmmaSmem umma_smem() {
     return here;
   };
   m.ring = take(kURing * kURawBytes, 128);
-  m.a = take(kUBuf * kUABytes, 1024);
-  m.b = take(kUBuf * kUBBytes, 1024);
+  m.a = take(kUStages * kUABytes, 1024);
+  m.b = take(kUStages * kUBBytes, 1024);
   m.iofs = take((kUMaxActive + 1) * 4, 16);
-  m.bars = take((kURing + kUBuf) * 8, 8);
-  m.tslot = take(16, 16);
-  m.total = at;
+  m.bars = take((2 * kURing + 3 * kUStages + 2 * kUAcc) * 8, 8);
+  m.misc = take(16, 16);   // tensor-memory address, abort flag
+  m.total = at + 1024;     // slack: the swizzled buffers are aligned to 1024 in the shared window
   return m;
 }
 
-// byte offset of element (row r, k) in a K-major no-swizzle operand of `rows`
-// rows: core matrix (k / 8, r / 8) at ((k / 8) * rows / 8 + r / 8) * 128
-__device__ __forceinline__ uint32_t kmajor_off(int r, int k, int rows) {
-  return (uint32_t)(((k >> 3) * (rows >> 3) + (r >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+// byte offset of element (row r, k < 64) in a K-major operand with 128-byte
+// swizzle: row r in atom r / 8 (1024 bytes each), line r % 8 (128 bytes), its
+// 16-byte chunk k / 8 stored at chunk (k / 8) ^ (r % 8)
+__device__ __forceinline__ uint32_t sw128_off(int r, int k) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((k >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
 }
 
-// four e4m3 bytes (each 2^-6 x an E2M1 value) times f -> four bf16 (exact
-// when f is a power of two and the result is in range)
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t v, float f) {
-  uint32_t h01, h23;
-  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n"
-      " cvt.rn.f16x2.e4m3x2 %1, hi;\n}\n"
-      : "=r"(h01), "=r"(h23)
-      : "r"(v));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-  const __nv_bfloat162 p = __floats2bfloat162_rn(a.x * f, a.y * f);
-  const __nv_bfloat162 q = __floats2bfloat162_rn(b.x * f, b.y * f);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&p), *reinterpret_cast<const uint32_t*>(&q));
+// E2M1 -> bf16 without conversion instructions. Input: four codes in the
+// byte form of decode_rowlo (sign in bit 7, the 3 magnitude bits e1 e0 m in
+// bits 4..2 of each byte). The magnitude bits are moved to bf16 bits 8..6
+// and the sign to bit 15: that bf16 number is the E2M1 value times 2^-126
+// (the E2M1 subnormal 0.5 lands on the bf16 subnormal 2^-127). One exact bf16
+// multiply by 2^(s-1) then gives value * 2^(s-127); block scales s > 128
+// (2^(s-1) not a bf16) take a second multiply.
+__device__ __forceinline__ uint32_t e2m1_pair_raw(uint32_t b, uint32_t sel) {
+  const uint32_t p = __byte_perm(b, 0u, sel);   // two code bytes into the high bytes of the halves
+  return (p & 0x80008000u) | ((p >> 4) & 0x01C001C0u);
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r =
+      __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// the two factors of block scale s (E8M0), as bf16 pairs: 2^(min(s,128)-1)
+// and 2^(s-min(s,128))
+__device__ __forceinline__ uint32_t scale_f1(uint32_t s) { return ((min(s, 128u) + 126u) << 7) * 0x10001u; }
+__device__ __forceinline__ uint32_t scale_f2(uint32_t s) { return ((s - min(s, 128u) + 127u) << 7) * 0x10001u; }
+__device__ __forceinline__ uint2 e2m1x4_to_bf16x4(uint32_t b, uint32_t f1, uint32_t f2, bool big) {
+  uint32_t lo = bf16x2_mul(e2m1_pair_raw(b, 0x1404u), f1);   // codes 0, 1
+  uint32_t hi = bf16x2_mul(e2m1_pair_raw(b, 0x3424u), f1);   // codes 2, 3
+  if (big) {
+    lo = bf16x2_mul(lo, f2);
+    hi = bf16x2_mul(hi, f2);
+  }
+  return make_uint2(lo, hi);
 }
 
 // 16-byte asynchronous global -> shared copy; zero-filled when !valid
@@ -99,23 +132,64 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// arrive on *bar once every cp.async issued so far by this thread has landed
+// (does not add to the barrier's expected count)
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Bounded mbarrier wait that also gives up at once when another role of the
+// CTA has timed out (*abort set).
+__device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kSpinBudget) {
+      *abort = 1;
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(20);
+  }
+  return true;
+}
+
+// debug build only: cycles per slice spent in up to four sections of a role
+#ifdef MOE_UMMA_TRACE
+#define UT_DECL long long ut_acc[4] = {0, 0, 0, 0}; long long ut_t = clock64();
+#define UT(i) do { const long long _t = clock64(); ut_acc[i] += _t - ut_t; ut_t = _t; } while (0)
+#define UT_PRINT(role, n)                                                                                  \
+  if (blockIdx.x == 0)                                                                                     \
+    printf("  %-9s cycles per slice: %6lld %6lld %6lld %6lld\n", role, ut_acc[0] / (n), ut_acc[1] / (n), \
+           ut_acc[2] / (n), ut_acc[3] / (n));
+#else
+#define UT_DECL
+#define UT(i) do { } while (0)
+#define UT_PRINT(role, n) (void)0;
+#endif
 
 template <int MODE>
-__global__ void __launch_bounds__(kUThreads, 1) umma_routed_kernel(RoutedArgs a, UmmaSmem L) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, UmmaSmem L) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the 128-byte swizzle is a function of the shared address: align the plan's base to 1024
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem + L.ring;
   uint8_t* abuf = smem + L.a;
   uint8_t* bbuf = smem + L.b;
   int* iofs = reinterpret_cast<int*>(smem + L.iofs);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* mdone = full + kURing;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.tslot);
+  uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty_raw = full_raw + kURing;
+  uint64_t* a_full = empty_raw + kURing;
+  uint64_t* b_full = a_full + kUStages;
+  uint64_t* op_empty = b_full + kUStages;
+  uint64_t* acc_full = op_empty + kUStages;
+  uint64_t* acc_empty = acc_full + kUAcc;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, q = lane & 3;
   const int D = *a.n_active, KB = a.KB, K = KB * kMxBlock;
   const int nrb = (a.n_tiles + kUTiles - 1) / kUTiles;
   // tokens per item: gate/up columns are tokens; down columns are hi and lo terms of h
@@ -124,49 +198,69 @@ __global__ void __launch_bounds__(kUThreads, 1) umma_routed_kernel(RoutedArgs a,
 
   // iofs[i] = items of the active experts before i (nrb per block of kNTok rows)
   {
-    constexpr int kPer = kUMaxActive / kUThreads;
-    int v[kPer], run = 0;
-#pragma unroll
-    for (int r = 0; r < kPer; ++r) {
-      const int ai = tid * kPer + r;
-      int c = 0;
-      if (ai < D) {
-        const int e = a.active[ai];
-        c = nrb * ((a.offsets[e + 1] - a.offsets[e] + kNTok - 1) / kNTok);
-      }
-      v[r] = run;
-      run += c;
-    }
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
-    }
+    constexpr int kPer = kUMaxActive / kScanThreads;
+    int v[kPer], run = 0, incl = 0;
     int* wsum = reinterpret_cast<int*>(bbuf);
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int base = incl - run;
-    for (int w = 0; w < warp; ++w) base += wsum[w];
+    if (tid < kScanThreads) {
 #pragma unroll
-    for (int r = 0; r < kPer; ++r) {
-      const int ai = tid * kPer + r;
-      if (ai < D) iofs[ai] = base + v[r];
+      for (int r = 0; r < kPer; ++r) {
+        const int ai = tid * kPer + r;
+        int c = 0;
+        if (ai < D) {
+          const int e = a.active[ai];
+          c = nrb * ((a.offsets[e + 1] - a.offsets[e] + kNTok - 1) / kNTok);
+        }
+        v[r] = run;
+        run += c;
+      }
+      incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
     }
-    if (tid == kUThreads - 1) iofs[D] = base + run;
+    __syncthreads();
+    if (tid < kScanThreads) {
+      int base = incl - run;
+      for (int w = 0; w < warp; ++w) base += wsum[w];
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int ai = tid * kPer + r;
+        if (ai < D) iofs[ai] = base + v[r];
+      }
+      if (tid == kScanThreads - 1) iofs[D] = base + run;
+    }
     __syncthreads();
   }
   const int n_items = iofs[D];
   const int lo = int((long long)blockIdx.x * n_items / gridDim.x);
   const int hi = int((long long)(blockIdx.x + 1) * n_items / gridDim.x);
   if (lo >= hi) return;
-  const int n_stream = (hi - lo) * ns;   // my slices, item after item
+  const int n_mine = hi - lo;
+  const int n_stream = n_mine * ns;   // my slices, item after item
+  const int nch = (ns + kUChunk - 1) / kUChunk;   // raw chunks per item
+  const int n_chunks = n_mine * nch;
 
   if (tid == 0) {
-    for (int i = 0; i < kURing + kUBuf; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kURing; ++i) {
+      mbar_init(&full_raw[i], 1);
+      mbar_init(&empty_raw[i], kNDec);
+    }
+    for (int i = 0; i < kUStages; ++i) {
+      mbar_init(&a_full[i], kNDec);
+      mbar_init(&b_full[i], kNLoad * 32);
+      mbar_init(&op_empty[i], 1);
+    }
+    for (int i = 0; i < kUAcc; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kNEpi);
+    }
+    *abort = 0;
     mbar_fence_init();
   }
-  if (warp == 0) tmem_alloc(tslot, kUCols);
+  if (warp == kWProducer) tmem_alloc(tslot, kUAcc * kUCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -181,41 +275,18 @@ __global__ void __launch_bounds__(kUThreads, 1) umma_routed_kernel(RoutedArgs a,
     }
     return l;
   };
-  // packed bytes of stream slice p -> ring slot p % kURing (producer thread,
-  // which keeps the item it last looked up)
-  int pr_it = -1, pr_rb = 0, pr_nt = 0;
-  const uint8_t* pr_wm = nullptr;
-  auto issue = [&](int p) {
-    const int it = lo + p / ns, sl = p - (p / ns) * ns;
-    if (it != pr_it) {
-      const int ai = expert_of(it), rem = it - iofs[ai];
-      pr_it = it;
-      pr_rb = rem % nrb;
-      pr_nt = min(kUTiles, a.n_tiles - pr_rb * kUTiles);
-      pr_wm = a.w + (uint64_t)a.active[ai] * a.mat_bytes + (uint64_t)pr_rb * kUTiles * KB * kUnitBytes;
-    }
-    const int kb0 = sl * kUSliceKb, nkb = min(kUSliceKb, KB - kb0);
-    uint8_t* dst = ring + (size_t)(p % kURing) * kURawBytes;
-    uint64_t* bar = &full[p % kURing];
-    mbar_arrive_expect_tx(bar, uint32_t(pr_nt * nkb) * kUnitBytes);
-    for (int t = 0; t < pr_nt; ++t)
-      bulk_g2s(dst + (size_t)t * kUSliceKb * kUnitBytes, pr_wm + ((uint64_t)t * KB + kb0) * kUnitBytes,
-               uint32_t(nkb) * kUnitBytes, bar);
-  };
-  constexpr int kProducer = 32;   // lane 0 of warp 1: thread 0 issues the MMAs
-  if (tid == kProducer)
-    for (int p = 0; p < kURing && p < n_stream; ++p) issue(p);
-
-  // item of stream slice p: expert row block, first row (slot), rows, MMA N
+  // my item j: expert, row block, first row (sorted slot), rows, MMA N
   struct Item {
-    int rb, pos0, ntok, nmma, n16;
+    int e, rb, pos0, ntok, nmma, n16;
   };
-  auto item_of = [&](int p) {
+  auto item_of = [&](int j) {
     Item f;
-    const int it = lo + p / ns, ai = expert_of(it), rem = it - iofs[ai];
-    const int e = a.active[ai], tb = rem / nrb, n_e = a.offsets[e + 1] - a.offsets[e];
-    f.rb = rem % nrb;
-    f.pos0 = a.offsets[e] + tb * kNTok;
+    const int it = lo + j, ai = expert_of(it), rem = it - iofs[ai];
+    const int tb = rem / nrb;
+    f.e = a.active[ai];
+    const int n_e = a.offsets[f.e + 1] - a.offsets[f.e];
+    f.rb = rem - tb * nrb;
+    f.pos0 = a.offsets[f.e] + tb * kNTok;
     f.ntok = min(kNTok, n_e - tb * kNTok);
     if (MODE == kModeGateUp) {
       f.n16 = 0;
@@ -226,75 +297,214 @@ __global__ void __launch_bounds__(kUThreads, 1) umma_routed_kernel(RoutedArgs a,
     }
     return f;
   };
-  // activation rows of stream slice p -> operand buffer p % kUBuf (one
-  // cp.async group per call, empty past the stream). Chunk j = 8 r + c is row
-  // r, 16-byte chunk c; a thread's rows are the same in every slice of an
-  // item, so their source rows are looked up once per item.
-  constexpr int kRowsPerThread = kUCols * 8 / kUThreads;
-  int b_it = -1;
-  Item b_f{};
-  int b_row[kRowsPerThread];
-  auto issue_b = [&](int p) {
-    if (p < n_stream) {
-      const int it = lo + p / ns;
-      if (it != b_it) {
-        b_it = it;
-        b_f = item_of(p);
-#pragma unroll
-        for (int m = 0; m < kRowsPerThread; ++m) {
-          const int r = (tid + m * kUThreads) >> 3;
-          b_row[m] = r < b_f.ntok ? (MODE == kModeGateUp ? a.perm[b_f.pos0 + r] / a.k : b_f.pos0 + r) : 0;
+
+  if (warp == kWProducer) {
+    // ---- packed weights -> raw ring ----------------------------------------------
+    if (lane == 0) {
+      UT_DECL
+      int issued = 0, pf_next = 0;
+      const int pf_items = (kUPrefetchChunks + nch - 1) / nch;
+      const uint8_t* wm = nullptr;
+      int nt = 0;
+      auto item_base = [&](const Item& f) {
+        return a.w + (uint64_t)f.e * a.mat_bytes + (uint64_t)f.rb * kUTiles * KB * kUnitBytes;
+      };
+      for (int c = 0; c < n_chunks; ++c) {
+        const int j = c / nch, cc = c - j * nch, s = c % kURing;
+        if (c >= kURing && !uwait(&empty_raw[s], uint32_t(c / kURing - 1) & 1u, abort, a.status)) break;
+        UT(0);
+        if (cc == 0) {
+          UT(0);
+          const Item f = item_of(j);
+          nt = min(kUTiles, a.n_tiles - f.rb * kUTiles);
+          wm = item_base(f);
+          // items j .. j + pf_items into L2 (each tile's units over all K are contiguous)
+          for (; pf_next <= j + pf_items && pf_next < n_mine; ++pf_next) {
+            const Item g = item_of(pf_next);
+            const int gt = min(kUTiles, a.n_tiles - g.rb * kUTiles);
+            prefetch_l2(item_base(g), uint32_t(gt) * KB * kUnitBytes);
+          }
+          UT(2);
         }
+        const int kb0 = cc * kUChunk * kUSliceKb, nkb = min(kUChunk * kUSliceKb, KB - kb0);
+        uint8_t* dst = ring + (size_t)s * kURawBytes;
+        mbar_arrive_expect_tx(&full_raw[s], uint32_t(nt * nkb) * kUnitBytes);
+        for (int t = 0; t < nt; ++t)
+          bulk_g2s(dst + (size_t)t * kUTileChunk, wm + ((uint64_t)t * KB + kb0) * kUnitBytes,
+                   uint32_t(nkb) * kUnitBytes, &full_raw[s]);
+        issued = c + 1;
+        UT(1);
       }
-      const int kb0 = (p % ns) * kUSliceKb, nc = min(kUSliceKb, KB - kb0) * kMxBlock / 8;
-      uint8_t* bb = bbuf + (size_t)(p % kUBuf) * kUBBytes;
-      const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
-      const __nv_bfloat16* src1 = static_cast<const __nv_bfloat16*>(a.act_raw2);
-      const int nrow = MODE == kModeGateUp ? b_f.nmma : b_f.n16;
-#pragma unroll
-      for (int m = 0; m < kRowsPerThread; ++m) {
-        const int j = tid + m * kUThreads, r = j >> 3, c = j & 7;
-        if (r < nrow && c < nc) {
-          const bool valid = r < b_f.ntok;
-          const size_t o = (size_t)b_row[m] * K + kb0 * kMxBlock + c * 8;
-          cp_async16(bb + kmajor_off(r, c * 8, b_f.nmma), src0 + o, valid);
-          if (MODE == kModeDown) cp_async16(bb + kmajor_off(b_f.n16 + r, c * 8, b_f.nmma), src1 + o, valid);
-        }
-      }
+      if (*abort)   // copies still in flight land before the CTA's shared memory goes away
+        for (int c = issued > kURing ? issued - kURing : 0; c < issued; ++c)
+          mbar_wait(&full_raw[c % kURing], uint32_t(c / kURing) & 1u, a.status);
+      UT_PRINT("producer", n_stream)
     }
-    cp_async_commit();
-  };
-  issue_b(0);
-  issue_b(1);
-
-  Item cur{};
-#ifdef MOE_UMMA_TRACE
-  long long tt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  long long tm[3] = {0, 0, 0};
-  long long tc0 = clock64();
-#define UT(i) do { const long long _t = clock64(); tt[i] += _t - tc0; tc0 = _t; } while (0)
-#else
-#define UT(i) do { } while (0)
-#endif
-  for (int p = 0; p < n_stream; ++p) {
-    const int sl = p % ns, buf = p % kUBuf;
-    if (sl == 0) cur = item_of(p);
-    UT(7);
-    // buffer (p + 2) % 4 was last read by the MMAs of slice p - 2
-    if (p >= 2) mbar_wait(&mdone[(p + 2) % kUBuf], uint32_t((p - 2) / kUBuf) & 1u, a.status);
-    UT(0);
-    issue_b(p + 2);
-    UT(1);
-    const int kb0 = sl * kUSliceKb, nkb = min(kUSliceKb, KB - kb0);
-    uint8_t* ab = abuf + (size_t)buf * kUABytes;
-    uint8_t* bb = bbuf + (size_t)buf * kUBBytes;
-
-    // ---- weights: packed MXFP4 -> bf16 (warp w decodes tile w) ---------------
-    mbar_wait(&full[p % kURing], uint32_t(p / kURing) & 1u, a.status);
-    UT(2);
-    {
-      const int t = warp, tile = cur.rb * kUTiles + t;
-      const uint8_t* raw = ring + (size_t)(p % kURing) * kURawBytes + (size_t)t * kUSliceKb * kUnitBytes;
+  } else if (warp == kWMma) {
+    // ---- tcgen05.mma issue -----------------------------------------------------------
+    if (lane == 0) {
+      UT_DECL
+      uint64_t* last = nullptr;
+      uint32_t last_par = 0;
+      bool ok = true;
+      for (int j = 0; j < n_mine && ok; ++j) {
+        UT(0);
+        const Item f = item_of(j);
+        UT(2);
+        const int ab = j % kUAcc;
+        if (j >= kUAcc && !uwait(&acc_empty[ab], uint32_t(j / kUAcc - 1) & 1u, abort, a.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + uint32_t(ab * kUCols);
+        const uint32_t idesc = umma_idesc_bf16(kURows, f.nmma);
+        for (int sl = 0; sl < ns; ++sl) {
+          const int p = j * ns + sl, st = p % kUStages;
+          const uint32_t par = uint32_t(p / kUStages) & 1u;
+          if (!uwait(&a_full[st], par, abort, a.status) || !uwait(&b_full[st], par, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          UT(0);
+          fence_async_smem();   // the loaders' cp.async writes -> visible to the tensor cores
+          tc_fence_after();
+          UT(3);
+          const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
+          const uint32_t as = smem_addr(abuf + (size_t)st * kUABytes);
+          const uint32_t bs = smem_addr(bbuf + (size_t)st * kUBBytes);
+          for (int kk = 0; kk < nkb * 2; ++kk)   // K = 16 steps: 32 bytes into the swizzle atoms
+            umma_bf16(d, umma_desc_sw128(as + 32 * kk), umma_desc_sw128(bs + 32 * kk), idesc, sl > 0 || kk > 0);
+          umma_commit(&op_empty[st]);
+          last = &op_empty[st];
+          last_par = par;
+          if (sl == ns - 1) umma_commit(&acc_full[ab]);
+          UT(1);
+        }
+      }
+      // every MMA has finished before tensor memory is freed
+      if (last) mbar_wait(last, last_par, a.status);
+      UT_PRINT("mma", n_stream)
+    }
+  } else if (warp < kWLoad) {
+    // ---- epilogue: accumulator -> outputs --------------------------------------------
+    UT_DECL
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;   // TMEM lane = weight row of the item
+    for (int j = 0; j < n_mine; ++j) {
+      const int ab = j % kUAcc;
+      if (!uwait(&acc_full[ab], uint32_t(j / kUAcc) & 1u, abort, a.status)) break;
+      UT(0);
+      tc_fence_after();
+      const Item f = item_of(j);
+      UT(2);
+      const uint32_t trow = tmem + uint32_t(ab * kUCols) + ((uint32_t)(quarter * 32) << 16);
+      if (MODE == kModeGateUp) {
+        // rows 16t .. 16t+7: gate of features 8 (rb*8 + t) + 0..7; rows +8: up.
+        // h goes out as bf16 terms: hi = bf16(h), lo = bf16(h - hi)
+        __nv_bfloat16* hhi = reinterpret_cast<__nv_bfloat16*>(a.out);
+        __nv_bfloat16* hlo = hhi + (size_t)a.n_rows * a.out_ld;
+        const int t = row >> 4, r16 = row & 15, tile = f.rb * kUTiles + t;
+        const int fe = tile * 8 + (r16 & 7);
+        const bool st_ok = r16 < 8 && tile < a.n_tiles;
+        for (int c0 = 0; c0 < f.nmma; c0 += 8) {
+          uint32_t v[8];
+          tmem_ld8(trow + c0, v);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float gv = __uint_as_float(v[jj]);
+            const float uv = __shfl_down_sync(0xFFFFFFFFu, gv, 8);
+            if (st_ok && c0 + jj < f.ntok) {
+              const float h = silu_f(gv) * uv;
+              const __nv_bfloat16 hb = __float2bfloat16_rn(h);
+              const size_t o = (size_t)(f.pos0 + c0 + jj) * a.out_ld + fe;
+              hhi[o] = hb;
+              hlo[o] = __float2bfloat16_rn(h - __bfloat162float(hb));
+            }
+          }
+        }
+      } else {
+        const int r = f.rb * kURows + row;   // output feature
+        const bool st_ok = r < a.n_tiles * kTileRows;
+        for (int c0 = 0; c0 < f.n16; c0 += 8) {
+          uint32_t vh[8], vl[8];
+          tmem_ld8(trow + c0, vh);
+          tmem_ld8(trow + f.n16 + c0, vl);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (st_ok && c0 + jj < f.ntok)
+              a.out[(size_t)(f.pos0 + c0 + jj) * a.out_ld + r] = __uint_as_float(vh[jj]) + __uint_as_float(vl[jj]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      UT(1);
+    }
+    if (lane == 0 && warp == kWEpi) UT_PRINT("epilogue", n_stream)
+  } else if (warp < kWDec) {
+    // ---- activation rows -> operand stage (cp.async) --------------------------------
+    // Thread lt copies 16-byte column c = lt % 8 of rows lt / 8 + 16 m. Gate/up:
+    // the rows are tokens (x rows gathered through perm). Down: the rows are
+    // sorted slots, hi terms to B rows r and lo terms to B rows n16 + r.
+    UT_DECL
+    const int lt = tid - kWLoad * 32, c = lt & 7, rr = lt >> 3;
+    constexpr int kRows = MODE == kModeGateUp ? kUCols / 16 : kUCols / 32;   // rows per thread
+    const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
+    const __nv_bfloat16* src1 = static_cast<const __nv_bfloat16*>(a.act_raw2);
+    int b_row[kRows];
+    Item f{};
+    for (int p = 0; p < n_stream; ++p) {
+      const int j = p / ns, sl = p - j * ns, st = p % kUStages;
+      if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
+      UT(0);
+      if (sl == 0) {
+        f = item_of(j);
+        UT(2);
+#pragma unroll
+        for (int m = 0; m < kRows; ++m) {
+          const int r = rr + 16 * m;
+          b_row[m] = r < f.ntok ? (MODE == kModeGateUp ? a.perm[f.pos0 + r] / a.k : f.pos0 + r) : 0;
+        }
+        UT(3);
+      }
+      const int kb0 = sl * kUSliceKb, nc = min(kUSliceKb, KB - kb0) * (kMxBlock / 8);
+      uint8_t* bb = bbuf + (size_t)st * kUBBytes;
+      const int nrow = MODE == kModeGateUp ? f.nmma : f.n16;
+      if (c < nc) {
+#pragma unroll
+        for (int m = 0; m < kRows; ++m) {
+          const int r = rr + 16 * m;
+          if (r < nrow) {
+            const bool valid = r < f.ntok;
+            const size_t o = (size_t)b_row[m] * K + kb0 * kMxBlock + c * 8;
+            cp_async16(bb + sw128_off(r, c * 8), src0 + o, valid);
+            if (MODE == kModeDown) cp_async16(bb + sw128_off(f.n16 + r, c * 8), src1 + o, valid);
+          }
+        }
+      }
+      cp_async_arrive_noinc(&b_full[st]);
+      UT(1);
+    }
+    cp_async_wait_all();   // nothing lands after the CTA's shared memory goes away
+    if (lt == 0) UT_PRINT("loader", n_stream)
+  } else {
+    // ---- raw ring -> bf16 weights (decode warp t decodes tile t of the item) ----------
+    UT_DECL
+    const int t = warp - kWDec;
+    const int g = lane >> 2, q = lane & 3;
+    int tile = 0;
+    for (int p = 0; p < n_stream; ++p) {
+      const int j = p / ns, sl = p - j * ns, st = p % kUStages;
+      const int cc = sl / kUChunk, sub = sl - cc * kUChunk, c = j * nch + cc, s = c % kURing;
+      if (sub == 0 && !uwait(&full_raw[s], uint32_t(c / kURing) & 1u, abort, a.status)) break;
+      UT(0);
+      if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
+      UT(1);
+      if (sl == 0) {
+        tile = item_of(j).rb * kUTiles + t;
+        UT(3);
+      }
+      const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
+      const uint8_t* raw = ring + (size_t)s * kURawBytes + (size_t)t * kUTileChunk + (size_t)sub * kUSliceKb * kUnitBytes;
+      uint8_t* ab = abuf + (size_t)st * kUABytes;
 #pragma unroll
       for (int u = 0; u < kUSliceKb; ++u) {
         const int r0 = t * kTileRows + g, r1 = r0 + 8;
@@ -303,114 +513,38 @@ __global__ void __launch_bounds__(kUThreads, 1) umma_routed_kernel(RoutedArgs a,
           const uint8_t* unit = raw + (size_t)u * kUnitBytes;
           const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
           const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          // weights were decoded as 2^-6 x value: scale by 2^(s-127) * 64
-          const float flo = __uint_as_float((sc16 << 23) & 0x7F800000u) * 64.0f;
-          const float fhi = __uint_as_float((sc16 << 15) & 0x7F800000u) * 64.0f;
-          c0 = e4m3x4_to_bf16x4(decode_rowlo(wv.x), flo);   // row g,   k 4q .. 4q+3
-          c1 = e4m3x4_to_bf16x4(decode_rowhi(wv.x), fhi);   // row g+8
-          c2 = e4m3x4_to_bf16x4(decode_rowlo(wv.y), flo);   // row g,   k 16+4q ..
-          c3 = e4m3x4_to_bf16x4(decode_rowhi(wv.y), fhi);   // row g+8
+          const uint32_t slo = sc16 & 0xFFu, shi = sc16 >> 8;   // block scales of rows g and g+8
+          const bool big = __any_sync(0xFFFFFFFFu, (slo | shi) > 128u);
+          const uint32_t f1lo = scale_f1(slo), f2lo = scale_f2(slo), f1hi = scale_f1(shi), f2hi = scale_f2(shi);
+          c0 = e2m1x4_to_bf16x4(decode_rowlo(wv.x), f1lo, f2lo, big);   // row g,   k 4q .. 4q+3
+          c1 = e2m1x4_to_bf16x4(decode_rowhi(wv.x), f1hi, f2hi, big);   // row g+8
+          c2 = e2m1x4_to_bf16x4(decode_rowlo(wv.y), f1lo, f2lo, big);   // row g,   k 16+4q ..
+          c3 = e2m1x4_to_bf16x4(decode_rowhi(wv.y), f1hi, f2hi, big);   // row g+8
         }
         const int k0 = u * kMxBlock + 4 * q;
-        *reinterpret_cast<uint2*>(ab + kmajor_off(r0, k0, kURows)) = c0;
-        *reinterpret_cast<uint2*>(ab + kmajor_off(r1, k0, kURows)) = c1;
-        *reinterpret_cast<uint2*>(ab + kmajor_off(r0, k0 + 16, kURows)) = c2;
-        *reinterpret_cast<uint2*>(ab + kmajor_off(r1, k0 + 16, kURows)) = c3;
+        *reinterpret_cast<uint2*>(ab + sw128_off(r0, k0)) = c0;
+        *reinterpret_cast<uint2*>(ab + sw128_off(r1, k0)) = c1;
+        *reinterpret_cast<uint2*>(ab + sw128_off(r0, k0 + 16)) = c2;
+        *reinterpret_cast<uint2*>(ab + sw128_off(r1, k0 + 16)) = c3;
       }
-    }
-    UT(3);
-    cp_async_wait<2>();   // this slice's activation rows (issued two slices ago) have landed
-    fence_async_smem();
-    __syncthreads();   // operands written; ring slot p % kURing is free again
-    UT(4);
-    if (tid == kProducer && p + kURing < n_stream) issue(p + kURing);
-    if (tid == 0) {
-      // ---- the slice's MMAs ---------------------------------------------------
-      tc_fence_after();
-      const uint32_t idesc = umma_idesc_bf16(kURows, cur.nmma);
-      const uint32_t a_lbo = (kURows / 8) * 128, b_lbo = uint32_t(cur.nmma / 8) * 128;
-#ifdef MOE_UMMA_TRACE
-      const long long m0 = clock64();
-#endif
-      for (int kk = 0; kk < nkb * 2; ++kk) {
-        const uint64_t ad = umma_desc(smem_addr(ab) + 2 * kk * a_lbo, a_lbo, 128);
-        const uint64_t bd = umma_desc(smem_addr(bb) + 2 * kk * b_lbo, b_lbo, 128);
-        umma_bf16(tmem, ad, bd, idesc, sl > 0 || kk > 0);
-#ifdef MOE_UMMA_TRACE
-        if (kk == 0) tm[0] += clock64() - m0;
-#endif
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&a_full[st]);
+        if (sub == kUChunk - 1 || sl == ns - 1) mbar_arrive(&empty_raw[s]);   // chunk consumed
       }
-#ifdef MOE_UMMA_TRACE
-      const long long m1 = clock64();
-      tm[1] += m1 - m0;
-#endif
-      umma_commit(&mdone[buf]);
-#ifdef MOE_UMMA_TRACE
-      tm[2] += clock64() - m1;
-#endif
+      UT(2);
     }
-    UT(5);
-    if (sl == ns - 1) {
-      // ---- item done: accumulator -> outputs ------------------------------------
-      mbar_wait(&mdone[buf], uint32_t(p / kUBuf) & 1u, a.status);
-      tc_fence_after();
-      const int quarter = warp & 3, half = warp >> 2;
-      const int row = quarter * 32 + lane;   // TMEM lane = weight row of the item
-      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-      if (MODE == kModeGateUp) {
-        // rows 16t .. 16t+7: gate of features 8 (rb*8 + t) + 0..7; rows +8: up.
-        // h goes out as bf16 terms: hi = bf16(h), lo = bf16(h - hi)
-        __nv_bfloat16* hhi = reinterpret_cast<__nv_bfloat16*>(a.out);
-        __nv_bfloat16* hlo = hhi + (size_t)a.n_rows * a.out_ld;
-        const int t = row >> 4, r16 = row & 15, tile = cur.rb * kUTiles + t;
-        const int f = tile * 8 + (r16 & 7);
-        for (int c0 = half * 8; c0 < cur.nmma; c0 += 16) {
-          uint32_t v[8];
-          tmem_ld8(trow + c0, v);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float gv = __uint_as_float(v[j]);
-            const float uv = __shfl_down_sync(0xFFFFFFFFu, gv, 8);
-            if (r16 < 8 && tile < a.n_tiles && c0 + j < cur.ntok) {
-              const float h = silu_f(gv) * uv;
-              const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-              const size_t o = (size_t)(cur.pos0 + c0 + j) * a.out_ld + f;
-              hhi[o] = hb;
-              hlo[o] = __float2bfloat16_rn(h - __bfloat162float(hb));
-            }
-          }
-        }
-      } else {
-        const int r = cur.rb * kURows + row;   // output feature
-        for (int c0 = half * 8; c0 < cur.n16; c0 += 16) {
-          uint32_t vh[8], vl[8];
-          tmem_ld8(trow + c0, vh);
-          tmem_ld8(trow + cur.n16 + c0, vl);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (r < a.n_tiles * kTileRows && c0 + j < cur.ntok)
-              a.out[(size_t)(cur.pos0 + c0 + j) * a.out_ld + r] = __uint_as_float(vh[j]) + __uint_as_float(vl[j]);
-        }
-      }
-      tc_fence_before();
-      __syncthreads();   // accumulator read; the next item may overwrite it
-      tc_fence_after();
-      UT(6);
-    }
+    if (lane == 0 && t == 0) UT_PRINT("decode", n_stream)
   }
-  cp_async_wait<0>();
-#ifdef MOE_UMMA_TRACE
-  if (blockIdx.x == 0 && tid == 0)
-    printf("umma mode %d: %d slices; cycles per slice: mdone %lld, issue_b %lld, full %lld, decode %lld, "
-           "bwait+sync %lld, mma issue %lld, epilogue %lld, other %lld\n",
-           MODE, n_stream, tt[0] / n_stream, tt[1] / n_stream, tt[2] / n_stream, tt[3] / n_stream,
-           tt[4] / n_stream, tt[5] / n_stream, tt[6] / n_stream, tt[7] / n_stream);
-  if (blockIdx.x == 0 && tid == 0)
-    printf("  thread 0 per slice: first MMA %lld, all MMAs %lld, commit %lld\n", tm[0] / n_stream, tm[1] / n_stream,
-           tm[2] / n_stream);
-#endif
+
+  tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kUCols);
+  if (warp == kWProducer) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kUAcc * kUCols);
+  }
 }
 
 }  // namespace
@@ -422,11 +556,11 @@ int launch_umma_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& d
   if (mode == kModeGateUp) {
     MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       int(L.total)));
-    umma_routed_kernel<kModeGateUp><<<grid, kUThreads, L.total, s>>>(a, L);
+    umma_routed_kernel<kModeGateUp><<<grid, kUBlock, L.total, s>>>(a, L);
   } else {
     MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       int(L.total)));
-    umma_routed_kernel<kModeDown><<<grid, kUThreads, L.total, s>>>(a, L);
+    umma_routed_kernel<kModeDown><<<grid, kUBlock, L.total, s>>>(a, L);
   }
   return launch_status();
 }

@@ -37,6 +37,18 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
   d |= (uint64_t)1 << 46;   // descriptor version of this architecture
   return d;
 }
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: 8-row x 128-byte
+// atoms stacked along M (or N) 1024 bytes apart, the 16-byte chunk j of row r
+// of an atom stored at chunk j ^ (r % 8). The atoms must be 1024-byte
+// aligned; a K step inside the atom advances saddr by its bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;                   // leading byte offset: unused for this layout
+  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                   // descriptor version of this architecture
+  d |= (uint64_t)2 << 61;                   // layout: 128-byte swizzle
+  return d;
+}
 // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
