@@ -56,6 +56,7 @@ constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about
 constexpr int kUAcc = 2;                     // accumulators in tensor memory
 constexpr int kUCols = 128;                  // columns per accumulator = largest MMA N
 constexpr int kUMaxActive = 1024;
+constexpr int kUTable = 256;                 // items per CTA with a precomputed table entry
 constexpr uint32_t kUTileChunk = kUChunk * kUSliceKb * kUnitBytes;   // one tile's part of a chunk
 constexpr uint32_t kURawBytes = kUTiles * kUTileChunk;                  // one chunk of packed weights
 constexpr uint32_t kUABytes = kURows * kUSliceK * 2;                 // one slice of bf16 weights
@@ -68,7 +69,7 @@ constexpr int kUBlock = (kWDec + kNDec) * 32;
 constexpr int kScanThreads = 256;
 
 struct UmmaSmem {
-  uint32_t ring, a, b, iofs, bars, misc, total;
+  uint32_t ring, a, b, iofs, itab, bars, misc, total;
 };
 __host__ __device__ inline UmmaSmem umma_smem() {
   UmmaSmem m{};
@@ -83,6 +84,7 @@ __host__ __device__ inline UmmaSmem umma_smem() {
   m.a = take(kUStages * kUABytes, 1024);
   m.b = take(kUStages * kUBBytes, 1024);
   m.iofs = take((kUMaxActive + 1) * 4, 16);
+  m.itab = take(kUTable * 16, 16);
   m.bars = take((2 * kURing + 3 * kUStages + 2 * kUAcc) * 8, 8);
   m.misc = take(16, 16);   // tensor-memory address, abort flag
   m.total = at + 1024;     // slack: the swizzled buffers are aligned to 1024 in the shared window
@@ -243,6 +245,61 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   const int nch = (ns + kUChunk - 1) / kUChunk;   // raw chunks per item
   const int n_chunks = n_mine * nch;
 
+  // active expert of item it (iofs is strictly increasing)
+  auto expert_of = [&](int it) {
+    int l = 0, h = D - 1;
+    while (l < h) {
+      const int m = (l + h + 1) >> 1;
+      if (iofs[m] <= it) l = m; else h = m - 1;
+    }
+    return l;
+  };
+  // my item j: expert, row block, first row (sorted slot), rows, MMA N
+  struct Item {
+    int e, rb, pos0, ntok, nmma, n16;
+  };
+  auto item_slow = [&](int j) {
+    Item f;
+    const int it = lo + j, ai = expert_of(it), rem = it - iofs[ai];
+    const int tb = rem / nrb;
+    f.e = a.active[ai];
+    const int n_e = a.offsets[f.e + 1] - a.offsets[f.e];
+    f.rb = rem - tb * nrb;
+    f.pos0 = a.offsets[f.e] + tb * kNTok;
+    f.ntok = min(kNTok, n_e - tb * kNTok);
+    if (MODE == kModeGateUp) {
+      f.n16 = 0;
+      f.nmma = (f.ntok + 15) & ~15;
+    } else {
+      f.n16 = (f.ntok + 7) & ~7;   // hi columns [0, n16), lo columns [n16, 2 n16)
+      f.nmma = 2 * f.n16;
+    }
+    return f;
+  };
+  // the first kUTable items of the CTA, looked up once (in parallel) in the prologue
+  int4* itab = reinterpret_cast<int4*>(smem + L.itab);
+  auto item_of = [&](int j) {
+    if (j >= kUTable) return item_slow(j);
+    const int4 v = itab[j];
+    Item f;
+    f.e = v.x;
+    f.rb = v.y;
+    f.pos0 = v.z;
+    f.ntok = v.w;
+    if (MODE == kModeGateUp) {
+      f.n16 = 0;
+      f.nmma = (f.ntok + 15) & ~15;
+    } else {
+      f.n16 = (f.ntok + 7) & ~7;
+      f.nmma = 2 * f.n16;
+    }
+    return f;
+  };
+  for (int j = tid; j < n_mine && j < kUTable; j += blockDim.x) {
+    const Item f = item_slow(j);
+    itab[j] = make_int4(f.e, f.rb, f.pos0, f.ntok);
+  }
+
   if (tid == 0) {
     for (int i = 0; i < kURing; ++i) {
       mbar_init(&full_raw[i], 1);
@@ -265,38 +322,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-
-  // active expert of item it (iofs is strictly increasing)
-  auto expert_of = [&](int it) {
-    int l = 0, h = D - 1;
-    while (l < h) {
-      const int m = (l + h + 1) >> 1;
-      if (iofs[m] <= it) l = m; else h = m - 1;
-    }
-    return l;
-  };
-  // my item j: expert, row block, first row (sorted slot), rows, MMA N
-  struct Item {
-    int e, rb, pos0, ntok, nmma, n16;
-  };
-  auto item_of = [&](int j) {
-    Item f;
-    const int it = lo + j, ai = expert_of(it), rem = it - iofs[ai];
-    const int tb = rem / nrb;
-    f.e = a.active[ai];
-    const int n_e = a.offsets[f.e + 1] - a.offsets[f.e];
-    f.rb = rem - tb * nrb;
-    f.pos0 = a.offsets[f.e] + tb * kNTok;
-    f.ntok = min(kNTok, n_e - tb * kNTok);
-    if (MODE == kModeGateUp) {
-      f.n16 = 0;
-      f.nmma = (f.ntok + 15) & ~15;
-    } else {
-      f.n16 = (f.ntok + 7) & ~7;   // hi columns [0, n16), lo columns [n16, 2 n16)
-      f.nmma = 2 * f.n16;
-    }
-    return f;
-  };
 
   if (warp == kWProducer) {
     // ---- packed weights -> raw ring ----------------------------------------------
@@ -449,8 +474,18 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     constexpr int kRows = MODE == kModeGateUp ? kUCols / 16 : kUCols / 32;   // rows per thread
     const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
     const __nv_bfloat16* src1 = static_cast<const __nv_bfloat16*>(a.act_raw2);
-    int b_row[kRows];
+    int b_row[kRows], nb_row[kRows];   // source rows of this item and of the next one
     Item f{};
+    // rows of item j (requested one item ahead, so the loads are in flight meanwhile)
+    auto rows_of = [&](int j, int (&rows)[kRows]) {
+      const Item h = item_of(j);
+#pragma unroll
+      for (int m = 0; m < kRows; ++m) {
+        const int r = rr + 16 * m;
+        rows[m] = r < h.ntok ? (MODE == kModeGateUp ? a.perm[h.pos0 + r] / a.k : h.pos0 + r) : 0;
+      }
+    };
+    if (n_mine > 0) rows_of(0, nb_row);
     for (int p = 0; p < n_stream; ++p) {
       const int j = p / ns, sl = p - j * ns, st = p % kUStages;
       if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
@@ -459,10 +494,8 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         f = item_of(j);
         UT(2);
 #pragma unroll
-        for (int m = 0; m < kRows; ++m) {
-          const int r = rr + 16 * m;
-          b_row[m] = r < f.ntok ? (MODE == kModeGateUp ? a.perm[f.pos0 + r] / a.k : f.pos0 + r) : 0;
-        }
+        for (int m = 0; m < kRows; ++m) b_row[m] = nb_row[m];
+        if (j + 1 < n_mine) rows_of(j + 1, nb_row);
         UT(3);
       }
       const int kb0 = sl * kUSliceKb, nc = min(kUSliceKb, KB - kb0) * (kMxBlock / 8);
