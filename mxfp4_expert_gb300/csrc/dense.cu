@@ -7,10 +7,14 @@
 //
 // C[weight row][token] = sum_k W[row][k] * X[token][k]: the weight rows are
 // the MMA's M dimension (16 per warp), the tokens its N dimension (8 per MMA),
-// both operands K-contiguous in memory. A block computes 64 weight rows x 64
-// tokens; K goes in steps of 32 through padded shared-memory tiles (80-byte
-// rows, so the ldmatrix row reads hit distinct banks), with the next step's
-// tiles loaded into registers while the current one is multiplied.
+// both operands K-contiguous in memory. A block computes 16 * WM weight rows x
+// 64 tokens with its 4 warps arranged WM along the rows and 4 / WM along the
+// tokens: 64 rows when there are many tokens (the weight tile is reused by
+// 64 tokens), 16 rows for at most 64 tokens (4x more blocks, so the weight
+// bytes are spread over every SM). K goes in steps of 32 through padded
+// shared-memory tiles (80-byte rows, so the ldmatrix row reads hit distinct
+// banks), with the next step's tiles loaded into registers while the current
+// one is multiplied.
 //
 // In the first kernel the shared gate and up rows are interleaved 8 + 8 per
 // 16-row tile (the MMA16_GATEUP idea), so one lane holds gate and up of the
@@ -26,12 +30,10 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 64;            // weight rows per block
 constexpr int kBN = 64;            // tokens per block
-constexpr int kBK = 32;            // K per step
-constexpr int kLd = kBK + 8;       // shared-memory row, bf16 elements (80 bytes)
-constexpr int kDWarps = kBM / 16;  // each warp: 16 weight rows x 64 tokens
+constexpr int kDWarps = 4;
 constexpr int kDThreads = kDWarps * 32;
+constexpr int kSmallT = 64;        // up to this many tokens: 16-row blocks
 
 __device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -62,39 +64,58 @@ __device__ __forceinline__ const __nv_bfloat16* front_row(const FrontArgs& a, in
 
 // MODE 0: router + shared gate/up (FrontArgs). MODE 1: shared down + combine
 // (CombineArgs). Both share the tiling; P carries the mode's arguments.
-template <int MODE, typename P>
+// BK: K per step (32 for 64-row blocks; 128 for 16-row blocks when K allows,
+// where fewer and larger steps hide more of the load latency). K % BK == 0.
+template <int MODE, int WM, int BK, typename P>
 __global__ void __launch_bounds__(kDThreads)
 dense_kernel(P a, int Ep, int N, int K) {
+  constexpr int kBM = 16 * WM;              // weight rows per block
+  constexpr int kBK = BK;
+  constexpr int kLd = kBK + 8;              // shared-memory row, bf16 elements
+  constexpr int kCPR = kBK / 8;             // 16-byte chunks per tile row
+  constexpr int kRPP = kDThreads / kCPR;    // tile rows per pass of the block
+  constexpr int kNT = kBN / 8 / (kDWarps / WM);   // 8-token MMA tiles per warp
+  constexpr int kWH = (kBM + kRPP - 1) / kRPP;    // weight-tile passes
+  constexpr int kXH = kBN / kRPP;                 // token-tile passes
   __shared__ __align__(16) __nv_bfloat16 Ws[kBM * kLd];
   __shared__ __align__(16) __nv_bfloat16 Xh[kBN * kLd];
   __shared__ __align__(16) __nv_bfloat16 Xl[MODE == 1 ? kBN * kLd : 8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp % WM, wn = warp / WM;   // the warp's 16 rows and kNT token tiles
   const int n0 = blockIdx.x * kBM, t0 = blockIdx.y * kBN;
   const int T = a.T;
   bool have_w = true;
   if constexpr (MODE == 1) have_w = a.sh_down != nullptr;
 
-  // per thread: 2 chunks of 16 bytes of the weight tile and of the token tile
-  // (4 x 8 fp32 of h_sh in MODE 1), rows tid / 4 and tid / 4 + 32, column (tid % 4) * 8
-  const __nv_bfloat16* wrow[2];
-  const void* xrow[2];
-  const int cr = tid >> 2, cc = (tid & 3) * 8;
+  // per thread: 16-byte chunk column cc = (tid % kCPR) * 8 of the weight-tile
+  // rows cr + kRPP h (only rows < kBM) and of the token-tile rows cr + kRPP h
+  // (8 fp32 of h_sh in MODE 1), cr = tid / kCPR
+  const __nv_bfloat16* wrow[kWH];
+  const void* xrow[kXH];
+  const int cr = tid / kCPR, cc = (tid % kCPR) * 8;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = cr + 32 * h;
-    if constexpr (MODE == 0) {
-      wrow[h] = front_row(a, Ep, n0 + r);
-      xrow[h] = t0 + r < T ? static_cast<const void*>(a.x + (size_t)(t0 + r) * K) : nullptr;
-    } else {
-      wrow[h] = (have_w && n0 + r < N) ? a.sh_down + (size_t)(n0 + r) * K : nullptr;
-      xrow[h] = t0 + r < T ? static_cast<const void*>(a.h_sh + (size_t)(t0 + r) * K) : nullptr;
-    }
+  for (int h = 0; h < kWH; ++h) {
+    const int r = cr + kRPP * h;
+    if constexpr (MODE == 0)
+      wrow[h] = r < kBM ? front_row(a, Ep, n0 + r) : nullptr;
+    else
+      wrow[h] = (r < kBM && have_w && n0 + r < N) ? a.sh_down + (size_t)(n0 + r) * K : nullptr;
   }
-  uint4 wreg[2], xh[2], xl[2];
+#pragma unroll
+  for (int h = 0; h < kXH; ++h) {
+    const int r = cr + kRPP * h;
+    if constexpr (MODE == 0)
+      xrow[h] = t0 + r < T ? static_cast<const void*>(a.x + (size_t)(t0 + r) * K) : nullptr;
+    else
+      xrow[h] = t0 + r < T ? static_cast<const void*>(a.h_sh + (size_t)(t0 + r) * K) : nullptr;
+  }
+  uint4 wreg[kWH], xh[kXH], xl[MODE == 1 ? kXH : 1];
   auto load = [&](int k0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kWH; ++h)
       wreg[h] = wrow[h] ? ldg_nc_stream_u4(wrow[h] + k0 + cc) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int h = 0; h < kXH; ++h) {
       if constexpr (MODE == 0) {
         xh[h] = xrow[h] ? __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xrow[h]) + k0 + cc))
                         : make_uint4(0u, 0u, 0u, 0u);
@@ -121,17 +142,19 @@ dense_kernel(P a, int Ep, int N, int K) {
   };
   auto store = [&]() {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = cr + 32 * h;
-      *reinterpret_cast<uint4*>(Ws + r * kLd + cc) = wreg[h];
+    for (int h = 0; h < kWH; ++h)
+      if (cr + kRPP * h < kBM) *reinterpret_cast<uint4*>(Ws + (cr + kRPP * h) * kLd + cc) = wreg[h];
+#pragma unroll
+    for (int h = 0; h < kXH; ++h) {
+      const int r = cr + kRPP * h;
       *reinterpret_cast<uint4*>(Xh + r * kLd + cc) = xh[h];
       if constexpr (MODE == 1) *reinterpret_cast<uint4*>(Xl + r * kLd + cc) = xl[h];
     }
   };
 
-  float acc[kBN / 8][4];
+  float acc[kNT][4];
 #pragma unroll
-  for (int j = 0; j < kBN / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+  for (int j = 0; j < kNT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
 
   if (have_w) {
     load(0);
@@ -143,10 +166,10 @@ dense_kernel(P a, int Ep, int N, int K) {
 #pragma unroll
       for (int ks = 0; ks < kBK; ks += 16) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(a0, a1, a2, a3, Ws + (warp * 16 + (lane & 15)) * kLd + ks + (lane >> 4) * 8);
+        ldsm_x4(a0, a1, a2, a3, Ws + (wm * 16 + (lane & 15)) * kLd + ks + (lane >> 4) * 8);
 #pragma unroll
-        for (int j = 0; j < kBN / 8; j += 2) {
-          const int xr = j * 8 + (lane & 7) + ((lane >> 4) << 3), xc = ks + ((lane >> 3) & 1) * 8;
+        for (int j = 0; j < kNT; j += 2) {
+          const int xr = (wn * kNT + j) * 8 + (lane & 7) + ((lane >> 4) << 3), xc = ks + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(b0, b1, b2, b3, Xh + xr * kLd + xc);
           mma_bf16(acc[j], a0, a1, a2, a3, b0, b1);
@@ -161,18 +184,18 @@ dense_kernel(P a, int Ep, int N, int K) {
     }
   }
 
-  // lane (g, q): rows m = n0 + 16 warp + g (c[0], c[1]) and m + 8 (c[2], c[3]),
-  // tokens t0 + 8 j + 2 q + {0, 1}
+  // lane (g, q): rows m = n0 + 16 wm + g (c[0], c[1]) and m + 8 (c[2], c[3]),
+  // tokens t0 + 8 (wn kNT + j) + 2 q + {0, 1}
   const int g = lane >> 2, q = lane & 3;
-  const int m = n0 + warp * 16 + g;
+  const int m = n0 + wm * 16 + g;
 #pragma unroll
-  for (int j = 0; j < kBN / 8; ++j) {
+  for (int j = 0; j < kNT; ++j) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int t = t0 + j * 8 + 2 * q + u;
+      const int t = t0 + (wn * kNT + j) * 8 + 2 * q + u;
       if (t >= T) continue;
       if constexpr (MODE == 0) {
-        if (n0 + warp * 16 < Ep) {
+        if (n0 + wm * 16 < Ep) {
           if (m < a.E) a.logits[(size_t)t * a.E + m] = acc[j][u];
           if (m + 8 < a.E) a.logits[(size_t)t * a.E + m + 8] = acc[j][2 + u];
         } else if (a.sh_gate) {
@@ -203,15 +226,24 @@ int launch_front(const FrontArgs& a, const DeviceInfo& di, cudaStream_t s) {
   (void)di;
   const int Ep = (a.E + 15) / 16 * 16;
   const int N = Ep + (a.sh_gate ? 2 * a.I : 0);
-  const dim3 grid((N + kBM - 1) / kBM, (a.T + kBN - 1) / kBN);
-  dense_kernel<0, FrontArgs><<<grid, kDThreads, 0, s>>>(a, Ep, N, a.d);
+  if (a.T <= kSmallT && a.d % 128 == 0)
+    dense_kernel<0, 1, 128, FrontArgs><<<dim3((N + 15) / 16, 1), kDThreads, 0, s>>>(a, Ep, N, a.d);
+  else if (a.T <= kSmallT)
+    dense_kernel<0, 1, 32, FrontArgs><<<dim3((N + 15) / 16, 1), kDThreads, 0, s>>>(a, Ep, N, a.d);
+  else
+    dense_kernel<0, 4, 32, FrontArgs><<<dim3((N + 63) / 64, (a.T + kBN - 1) / kBN), kDThreads, 0, s>>>(a, Ep, N, a.d);
   return launch_status();
 }
 
 int launch_combine(const CombineArgs& a, const DeviceInfo& di, cudaStream_t s) {
   (void)di;
-  const dim3 grid((a.d + kBM - 1) / kBM, (a.T + kBN - 1) / kBN);
-  dense_kernel<1, CombineArgs><<<grid, kDThreads, 0, s>>>(a, 0, a.d, a.I);
+  if (a.T <= kSmallT && a.I % 128 == 0)
+    dense_kernel<1, 1, 128, CombineArgs><<<dim3((a.d + 15) / 16, 1), kDThreads, 0, s>>>(a, 0, a.d, a.I);
+  else if (a.T <= kSmallT)
+    dense_kernel<1, 1, 32, CombineArgs><<<dim3((a.d + 15) / 16, 1), kDThreads, 0, s>>>(a, 0, a.d, a.I);
+  else
+    dense_kernel<1, 4, 32, CombineArgs><<<dim3((a.d + 63) / 64, (a.T + kBN - 1) / kBN), kDThreads, 0, s>>>(a, 0, a.d,
+                                                                                                       a.I);
   return launch_status();
 }
 
