@@ -11,7 +11,7 @@
 //     since small copies are issued too slowly) into a ring of raw slots.
 //     The ring is too small to cover the HBM latency on its own, so whole
 //     items are also prefetched into L2 about 8 chunks ahead;
-//   * 8 decode warps (one tile each): raw slot -> bf16 with the E8M0 block
+//   * 16 decode warps (two per tile): raw slot -> bf16 with the E8M0 block
 //     scale applied (exact, integer and bf16-multiply instructions only), in
 //     the K-major 128-byte-swizzled operand layout the MMA reads;
 //   * 4 loader warps: the slice of the activation rows (bf16 x gathered by
@@ -64,7 +64,7 @@ constexpr uint32_t kUBBytes = kUCols * kUSliceK * 2;                 // one slic
 
 // warp roles
 constexpr int kWProducer = 0, kWMma = 1, kWEpi = 2, kNEpi = 4, kWLoad = kWEpi + kNEpi, kNLoad = 4,
-              kWDec = kWLoad + kNLoad, kNDec = kUTiles;
+              kWDec = kWLoad + kNLoad, kDecPerTile = 2, kNDec = kUTiles * kDecPerTile;
 constexpr int kUBlock = (kWDec + kNDec) * 32;
 constexpr int kScanThreads = 256;
 
@@ -141,19 +141,31 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Bounded mbarrier wait that also gives up at once when another role of the
-// CTA has timed out (*abort set).
+// mbarrier.try_wait with an explicit suspend-time limit: the thread sleeps in
+// hardware until the phase completes or about `ns` nanoseconds pass, instead
+// of spinning (a spinning warp takes issue slots from the decode warps)
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded mbarrier wait that also gives up when another role of the CTA has
+// timed out (*abort set; seen within one suspend period).
 __device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_for(bar, parity, 100000u)) {
     if (*abort) return false;
     if (clock64() - t0 > kSpinBudget) {
       *abort = 1;
       if (status) atomicOr(status, MOE_DEV_TIMEOUT);
       return false;
     }
-    __nanosleep(20);
   }
   return true;
 }
@@ -519,9 +531,10 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     cp_async_wait_all();   // nothing lands after the CTA's shared memory goes away
     if (lt == 0) UT_PRINT("loader", n_stream)
   } else {
-    // ---- raw ring -> bf16 weights (decode warp t decodes tile t of the item) ----------
+    // ---- raw ring -> bf16 weights (decode warp dw: tile dw % 8 of the item, the
+    // slice's 32-wide K-blocks u = dw / 8, dw / 8 + 2, ...) ----------------------------
     UT_DECL
-    const int t = warp - kWDec;
+    const int dw = warp - kWDec, t = dw % kUTiles;
     const int g = lane >> 2, q = lane & 3;
     int tile = 0;
     for (int p = 0; p < n_stream; ++p) {
@@ -539,7 +552,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       const uint8_t* raw = ring + (size_t)s * kURawBytes + (size_t)t * kUTileChunk + (size_t)sub * kUSliceKb * kUnitBytes;
       uint8_t* ab = abuf + (size_t)st * kUABytes;
 #pragma unroll
-      for (int u = 0; u < kUSliceKb; ++u) {
+      for (int u = dw / kUTiles; u < kUSliceKb; u += kDecPerTile) {
         const int r0 = t * kTileRows + g, r1 = r0 + 8;
         uint2 c0 = make_uint2(0u, 0u), c1 = c0, c2 = c0, c3 = c0;
         if (u < nkb && tile < a.n_tiles) {
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       }
       UT(2);
     }
-    if (lane == 0 && t == 0) UT_PRINT("decode", n_stream)
+    if (lane == 0 && dw == 0) UT_PRINT("decode", n_stream)
   }
 
   tc_fence_before();
