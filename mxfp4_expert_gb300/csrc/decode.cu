@@ -77,15 +77,31 @@ __device__ __forceinline__ long long dclk() { return 0; }
 constexpr int kWarps = 15;                  // compute warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp that issues the bulk copies
 constexpr int kComputeThreads = kWarps * 32;
-constexpr int kGroupWarps = 3;    // warps that share one routed gate/up tile (K split in three)
-constexpr int kGroups = kWarps / kGroupWarps;   // tiles in flight per CTA
+// Warps that share one routed gate/up tile (K split among them), and tiles in
+// flight per CTA. At T = 1 a CTA holds 5 or 6 tiles: 3 groups of 5 warps take
+// two short rounds for either count, where 5 groups of 3 would need a second
+// full-length round for a sixth tile. At T = 2..4 (about 20 tiles per CTA)
+// 5 groups of 3 keep more tiles in flight.
+template <int T>
+struct GroupCfg {
+  static constexpr int kWarpsPer = T == 1 ? 5 : 3;
+  static constexpr int kCount = kWarps / kWarpsPer;
+};
+constexpr int kGroupSlots = kWarps;   // groups x warps per group, for every T
 constexpr int kRowsPerLoad = 4;   // bf16 rows per load: router rows, or 2 shared features x (gate, up)
 constexpr int kMaxKbPerWarp = 8;  // routed gate/up: d <= kWarps * 8 * 32 = 3840
 constexpr int kMergeChunks = 16;  // top-k: E <= 16 chunks of 32 experts
-#ifndef MOE_DECODE_UNROLL
-#define MOE_DECODE_UNROLL 6
+// gate/up MMA items per warp issued back to back (no branches in between):
+// 8 at T = 1 (16 K-blocks per warp and tile), 6 otherwise (27 per warp);
+// a build may fix it with MOE_DECODE_UNROLL
+template <int T>
+__host__ __device__ constexpr int unroll_for() {
+#ifdef MOE_DECODE_UNROLL
+  return MOE_DECODE_UNROLL;
+#else
+  return T == 1 ? 8 : 6;
 #endif
-constexpr int kUnroll = MOE_DECODE_UNROLL;   // gate/up MMA items per warp issued back to back (no branches in between)
+}
 constexpr int kHTermBytes = 64;   // h of one (slot, K-block): 2 e4m3 terms x 32 features
 constexpr int kHGroups = 4;       // 8-feature groups per K-block, one exponent each
 
@@ -108,9 +124,10 @@ __device__ __forceinline__ int csync_count(bool v) {
   return int(r);
 }
 
-// Barrier among the kGroupWarps warps of group gid (ids 2.. are free).
+// Barrier among the GW warps of group gid (ids 2.. are free).
+template <int GW>
 __device__ __forceinline__ void group_sync(int gid) {
-  asm volatile("bar.sync %0, %1;" ::"r"(2 + gid), "n"(kGroupWarps * 32) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + gid), "n"(GW * 32) : "memory");
 }
 
 __device__ __forceinline__ float dot8_bf16(uint4 w, uint4 x) {
@@ -205,7 +222,7 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int
   s.bars = take(8u * uint32_t(2 * stages + 1), 8);   // full[S], empty[S], routing
   const uint32_t nch = uint32_t((E + 31) / 32), kk = uint32_t(k < 32 ? k : 32);
   // gate/up partials: per group, two tiles in turn, one row per warp
-  const uint32_t red_b = uint32_t(kGroups * 2 * kGroupWarps * red_floats(T)) * 4u;
+  const uint32_t red_b = uint32_t(2 * kGroupSlots * red_floats(T)) * 4u;
   const uint32_t cand_b = uint32_t(T) * nch * kk * 8u;
   s.red = take(red_b > cand_b ? red_b : cand_b, 16);
   const uint32_t xs_b = align_up(uint32_t(T) * d * 2, 16);
@@ -268,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   trace_put(17, (unsigned long long)clock64());
   long long tacc[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};   // debug builds: cycle sums of thread 0
   auto trace_add = [&](int point, long long v) { tacc[point - 20] += v; };
+  constexpr int kGroupWarps = GroupCfg<T>::kWarpsPer, kGroups = GroupCfg<T>::kCount;
+  constexpr int kUnroll = unroll_for<T>();
   constexpr int kPairs = (T + 1) / 2;
   constexpr int kRF = 32 * kPairs;
   const int d = a.d, I = a.I, E = a.E, k = a.k;
@@ -643,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       trace_add(24, dclk() - c1);
     } else if (i < s.bGU) {
       // ---- routed gate/up tile: 8 gate + 8 up rows of one active expert -------
-      // Tile jb belongs to warp group jb % kGroups; its 3 warps split K, and
+      // Tile jb belongs to warp group jb % kGroups; its warps split K, and
       // the group's first warp adds the 3 partials (in warp order) and writes
       // the tile's 8 features of h per slot as the B operand of the down MMA:
       // 2 e4m3 terms with one exponent for the 8 features.
@@ -664,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
         float acc[kPairs][2];
 #pragma unroll
         for (int p = 0; p < kPairs; ++p) acc[p][0] = acc[p][1] = 0.0f;
-        // my K-blocks gw, gw+3, ...: groups of kUnroll without branches (a
+        // my K-blocks gw, gw + kGroupWarps, ...: groups of kUnroll without branches (a
         // K-block past the end is clamped and weighted 0)
         for (int kb0 = gw; kb0 < KBd; kb0 += kUnroll * kGroupWarps) {
 #pragma unroll
@@ -700,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             gbuf[gw * kRF + p * 32 + 16 + g * 2 + (q >> 1)] = v1;   // up row g
           }
         }
-        group_sync(gid);
+        group_sync<kGroupWarps>(gid);
         if (gw == 0) {
           uint8_t* hT = reinterpret_cast<uint8_t*>(a.h);
           float* hF = reinterpret_cast<float*>(hT + (size_t)T * k * KBi * kHTermBytes);
