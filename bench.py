@@ -429,7 +429,10 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": us_per_layer, "unit": "us/layer", "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1xe4m3->f32 (mma.sync), bf16 router/shared, f32 accumulate",
+        "vs_baseline": None,
+        "dtype": ("e2m1->bf16 x bf16->f32 (tcgen05 routed experts), bf16 router/shared (mma.sync), f32 accumulate"
+                  if path == mx.MOE_PATH_PREFILL_TC else
+                  "e2m1xe4m3->f32 (mma.sync), bf16 router/shared, f32 accumulate"),
         "data": "synthetic",
         "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, E={w.E}, k={w.k}, I={w.I}, shared=1",
                    "weight_sets_cycled": n_sets, "layers_per_step": n_sets,
