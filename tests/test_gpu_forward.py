@@ -113,6 +113,22 @@ def test_small_layers(mx, name, T, d, I, E, k, routing):
     check_layer(w, 0, layer, x, bias, out)
 
 
+def test_tc_items_beyond_table(mx):
+    """tcgen05 path with more work items per CTA than its shared-memory item
+    table holds (256): E=1024, k=32, ~130 rows per expert, so the down pass
+    has about 49K items (d/128 row blocks x ceil(rows/64) token blocks per
+    expert) and the items past the table are looked up on the fly."""
+    w = wl.Workload("tc_items", T=4160, d=2048, I=32, E=1024, k=32, sets=1, routing="natural", seed=11)
+    assert mx.moe_query_path(mx.moe_shape(w.d, w.I, w.E, w.k, True), w.T) == mx.MOE_PATH_PREFILL_TC
+    layer, x, bias = build(mx, w)
+    out = run(mx, layer, x, bias, w.T, w.E, w.k)
+    counts = np.bincount(out[2].cpu().numpy().ravel(), minlength=w.E)
+    items_down = int(sum((w.d // 128) * ((c + 63) // 64) for c in counts if c > 0))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert items_down > 256 * sms, (items_down, sms)
+    check_layer(w, 0, layer, x, bias, out, tokens=range(0, w.T, 347))
+
+
 def test_no_shared_expert(mx):
     from mxfp4_expert_gb300 import synthetic
     w = wl.Workload("noshared", T=4, d=256, I=64, E=16, k=2, sets=1, routing="natural", seed=5)
