@@ -64,8 +64,9 @@ __device__ __forceinline__ const __nv_bfloat16* front_row(const FrontArgs& a, in
 
 // MODE 0: router + shared gate/up (FrontArgs). MODE 1: shared down + combine
 // (CombineArgs). Both share the tiling; P carries the mode's arguments.
-// BK: K per step (32 for 64-row blocks; 128 for 16-row blocks when K allows,
-// where fewer and larger steps hide more of the load latency). K % BK == 0.
+// BK: K per step (128 for 16-row blocks and 64 for the router + shared
+// gate/up with 64-row blocks when K allows, else 32: fewer and larger steps
+// hide more of the load latency). K % BK == 0.
 template <int MODE, int WM, int BK, typename P>
 __global__ void __launch_bounds__(kDThreads)
 dense_kernel(P a, int Ep, int N, int K) {
@@ -230,6 +231,8 @@ int launch_front(const FrontArgs& a, const DeviceInfo& di, cudaStream_t s) {
     dense_kernel<0, 1, 128, FrontArgs><<<dim3((N + 15) / 16, 1), kDThreads, 0, s>>>(a, Ep, N, a.d);
   else if (a.T <= kSmallT)
     dense_kernel<0, 1, 32, FrontArgs><<<dim3((N + 15) / 16, 1), kDThreads, 0, s>>>(a, Ep, N, a.d);
+  else if (a.d % 64 == 0)
+    dense_kernel<0, 4, 64, FrontArgs><<<dim3((N + 63) / 64, (a.T + kBN - 1) / kBN), kDThreads, 0, s>>>(a, Ep, N, a.d);
   else
     dense_kernel<0, 4, 32, FrontArgs><<<dim3((N + 63) / 64, (a.T + kBN - 1) / kBN), kDThreads, 0, s>>>(a, Ep, N, a.d);
   return launch_status();
@@ -241,7 +244,7 @@ int launch_combine(const CombineArgs& a, const DeviceInfo& di, cudaStream_t s) {
     dense_kernel<1, 1, 128, CombineArgs><<<dim3((a.d + 15) / 16, 1), kDThreads, 0, s>>>(a, 0, a.d, a.I);
   else if (a.T <= kSmallT)
     dense_kernel<1, 1, 32, CombineArgs><<<dim3((a.d + 15) / 16, 1), kDThreads, 0, s>>>(a, 0, a.d, a.I);
-  else
+  else   // (64-wide steps are slower here: the h_sh hi/lo split doubles the staged registers)
     dense_kernel<1, 4, 32, CombineArgs><<<dim3((a.d + 63) / 64, (a.T + kBN - 1) / kBN), kDThreads, 0, s>>>(a, 0, a.d,
                                                                                                        a.I);
   return launch_status();
