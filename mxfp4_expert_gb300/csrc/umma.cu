@@ -16,11 +16,9 @@
 //     the K-major 128-byte-swizzled operand layout the MMA reads;
 //   * 4 loader warps: the slice of the activation rows (bf16 x gathered by
 //     token; for the down projection h as two bf16 terms, hi and lo, in
-//     separate columns) copied with cp.async into the same layout; each
-//     thread's copies arrive on the stage's barrier when they land
-//     (cp.async.mbarrier.arrive.noinc), so a loader never waits for its own
-//     copies, and the MMA thread fences the generic -> async proxy after it
-//     has seen the barrier complete;
+//     separate columns) copied with cp.async into the same layout; a loader
+//     announces slice p once its copies have landed (it waits for them two
+//     slices later) and it has made them visible to the async proxy;
 //   * MMA (one thread): tcgen05.mma kind::f16, M = 128, N = the item's column
 //     count, K = 16, into one of two fp32 accumulators in tensor memory; each
 //     slice's MMAs are committed to the barrier that frees its operand stage,
@@ -53,6 +51,8 @@ constexpr int kUStages = 5;                  // operand stages (bf16 weights + a
 constexpr int kUChunk = 4;                   // slices per raw weight copy
 constexpr int kURing = 3;                    // raw weight chunks in flight
 constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about this many chunks ahead
+constexpr int kULag = 2;                     // activation slices a loader keeps in flight
+static_assert(kUStages > kULag, "a loader announces slice p - kULag only after it has claimed slice p's stage");
 constexpr int kUAcc = 2;                     // accumulators in tensor memory
 constexpr int kUCols = 128;                  // columns per accumulator = largest MMA N
 constexpr int kUMaxActive = 1024;
@@ -134,12 +134,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                "r"(valid ? 16 : 0)
                : "memory");
 }
-// arrive on *bar once every cp.async issued so far by this thread has landed
-// (does not add to the barrier's expected count)
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // mbarrier.try_wait with an explicit suspend-time limit: the thread sleeps in
 // hardware until the phase completes or about `ns` nanoseconds pass, instead
@@ -319,7 +316,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     }
     for (int i = 0; i < kUStages; ++i) {
       mbar_init(&a_full[i], kNDec);
-      mbar_init(&b_full[i], kNLoad * 32);
+      mbar_init(&b_full[i], kNLoad);
       mbar_init(&op_empty[i], 1);
     }
     for (int i = 0; i < kUAcc; ++i) {
@@ -401,7 +398,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
             break;
           }
           UT(0);
-          fence_async_smem();   // the loaders' cp.async writes -> visible to the tensor cores
           tc_fence_after();
           UT(3);
           const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
@@ -487,6 +483,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
     const __nv_bfloat16* src1 = static_cast<const __nv_bfloat16*>(a.act_raw2);
     int b_row[kRows], nb_row[kRows];   // source rows of this item and of the next one
+    int pend = 0;                       // first slice not yet announced
     Item f{};
     // rows of item j (requested one item ahead, so the loads are in flight meanwhile)
     auto rows_of = [&](int j, int (&rows)[kRows]) {
@@ -525,10 +522,24 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           }
         }
       }
-      cp_async_arrive_noinc(&b_full[st]);
+      cp_async_commit();
+      // announce slice p - kULag once its copies (not the later ones) have landed
+      if (p - pend >= kULag) {
+        cp_async_wait<kULag>();
+        fence_async_smem();   // generic-proxy writes -> visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
+        ++pend;
+      }
       UT(1);
     }
-    cp_async_wait_all();   // nothing lands after the CTA's shared memory goes away
+    cp_async_wait<0>();   // nothing lands after the CTA's shared memory goes away
+    if (!*abort) {
+      fence_async_smem();
+      __syncwarp();
+      for (; pend < n_stream; ++pend)
+        if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
+    }
     if (lt == 0) UT_PRINT("loader", n_stream)
   } else {
     // ---- raw ring -> bf16 weights (decode warp dw: tile dw % 8 of the item, the
