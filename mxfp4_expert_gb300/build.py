@@ -2,7 +2,7 @@
 
 Each .cu file compiles in its own nvcc process (in parallel); the objects are
 linked into ``mxfp4_expert_gb300/libmoe_mxfp4.so`` with the CUDA runtime linked
-statically, so the library only needs the driver at run time.
+statically, so the library only needs the CUDA driver at run time.
 """
 from __future__ import annotations
 

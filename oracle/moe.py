@@ -20,7 +20,7 @@ experts plus one shared expert; §3: moe_intermediate_size 768; hidden size
                       The shared expert enters with weight 1 (the pages give
                       no gate or scaling for it).
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 the router is a bias-free linear map unless a bias is supplied; a supplied
 bias is added before both selection and weights; the softmax/top-k/renormalise
 order is as above; the expert body is SwiGLU; there is no routed scaling
