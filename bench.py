@@ -75,6 +75,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_us_per_layer(ms_max, calls, ws):
+    """Whole-job time per layer: every one of the ws replicas ran `calls`
+    layer calls in the slowest rank's ms_max milliseconds."""
+    return ms_max * 1e3 / (calls * ws)
+
+
 def max_over_ranks(v, ws, device):
     if ws == 1:
         return v
@@ -366,7 +372,7 @@ def run_ours(args, w):
     clocks = sampler.stop() if not args.profile else None
     ms = max_over_ranks(ms, ws, dev)
     calls = steps * n_sets
-    us_per_layer = ms * 1e3 / (calls * ws)
+    us_per_layer = job_us_per_layer(ms, calls, ws)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # per-stage durations of the last replayed cycle (events recorded inside the graph)
