@@ -131,7 +131,8 @@ typedef struct moe_layer {
 
 /* Kernel paths moe_forward can take (moe_query_path). */
 typedef enum moe_path {
-  MOE_PATH_DECODE_MMA = 1,   /* per-stage kernels: router GEMV, top-k + sort,
+  MOE_PATH_DECODE_MMA = 1,   /* T < 32 where the single-launch kernel does not
+                                apply: per-stage kernels: router GEMV, top-k + sort,
                                 MXFP4 expert GEMVs on e4m3 mma.sync, combine */
   MOE_PATH_DECODE_FUSED = 2, /* T <= 4: one cooperative persistent kernel per
                                 call (router, top-k, shared and routed experts,
