@@ -359,16 +359,21 @@ def run_ours(args, w):
         time.sleep(0.3)
     barrier(ws)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the total and the per-step spread
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    e0, e1 = evs[0], evs[-1]
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(steps):
+        for i in range(steps):
             g.replay()
-        e1.record(stream)
+            evs[i + 1].record(stream)
     e1.synchronize()
     torch.cuda.synchronize()
     barrier(ws)
     ms = e0.elapsed_time(e1)
+    step_us = np.array([evs[i].elapsed_time(evs[i + 1]) * 1e3 / n_sets for i in range(steps)])
+    step_pct = {"p10": float(np.percentile(step_us, 10)), "p50": float(np.percentile(step_us, 50)),
+                "p90": float(np.percentile(step_us, 90))}
     clocks = sampler.stop() if not args.profile else None
     ms = max_over_ranks(ms, ws, dev)
     calls = steps * n_sets
@@ -449,6 +454,7 @@ def run_ours(args, w):
         "pct_of_hbm_peak": 100.0 * eff_gbs / peak,
         "algorithmic_bytes_per_layer": algo_bytes,
         "stage_us": stage_mean,
+        "step_us_per_layer": step_pct,   # this rank's per-step spread (each step = n_sets layer calls)
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes},
