@@ -324,9 +324,12 @@ def run_ours(args, w):
         for s in range(n_sets):
             if copies is not None:
                 xs[s].copy_(copies[0][s], non_blocking=True)
-            mx.moe_forward(layers[s], xs[s], biases[s], y=ys[s], workspace=work[s], idx_out=idxs[s],
-                           dev_status=status, stage_events=events[s] if with_events else None,
-                           stream=stream)
+            if with_events:
+                mx.moe_forward_profiled(layers[s], xs[s], events[s], biases[s], y=ys[s], workspace=work[s],
+                                        idx_out=idxs[s], dev_status=status, stream=stream)
+            else:
+                mx.moe_forward(layers[s], xs[s], biases[s], y=ys[s], workspace=work[s], idx_out=idxs[s],
+                               dev_status=status, stream=stream)
             if copies is not None:
                 copies[1][s].copy_(ys[s], non_blocking=True)
 

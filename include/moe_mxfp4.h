@@ -154,6 +154,12 @@ size_t moe_packed_bytes(int n_mat, int N, int K, int layout);
 int moe_describe_packed(int n_mat, int N, int K, int layout, moe_packed_desc* out);
 
 /* Quantise fp32 weights to MXFP4 and write them in `layout`.
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §2
+ * (the routed experts of Ling-3.0-flash are served in MXFP4, the baseline
+ * running FlashInfer's MXFP4 MoE kernel); the pages do not define the format,
+ * so the element, scale and rounding rule are those of the OCP Microscaling
+ * Formats (MX) v1.0 specification, §5 (E2M1 elements, E8M0 scale per 32) and
+ * §6.3 (conversion). The call is an offline step, done once per weight set.
  *   w_dev       fp32 [n_mat][N][K] row-major (device)
  *   packed_dev  output, packed_bytes >= moe_packed_bytes(...) (device, 16-B aligned)
  *   desc_out    host, may be NULL
@@ -162,7 +168,9 @@ int moe_describe_packed(int n_mat, int N, int K, int layout, moe_packed_desc* ou
  * Rule (OCP MX v1.0, §6.3): per 32-block, s = clamp(floor(log2 amax) - 2 +
  * 127, 0, 254) (amax = 0 -> 0); codes = RNE(v * 2^(127-s)) onto the E2M1
  * grid, ties to even mantissa, saturating at 6, sign kept (-0 -> code 8).
- * A block with inf/NaN gets scale 255, its non-finite elements code 0. */
+ * A block with inf/NaN gets scale 255, its non-finite elements code 0.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, bad layout),
+ * MOE_ERR_UNSUPPORTED_SHAPE (N % 16, K % 32), MOE_ERR_BUFFER_TOO_SMALL. */
 int moe_pack_mxfp4(const float* w_dev, int n_mat, int N, int K, int layout,
                    void* packed_dev, size_t packed_bytes, moe_packed_desc* desc_out,
                    int* dev_status, moe_stream_t stream);
@@ -176,13 +184,22 @@ int moe_unpack_mxfp4(const void* packed_dev, const moe_packed_desc* desc,
 /* ---- routing ------------------------------------------------------------ */
 
 /* Top-k selection and renormalised softmax weights from fp32 logits.
- *   logits_dev      fp32 [T][E]
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §2
+ * (each MoE layer sends a token to 8 of its 512 routed experts) and page
+ * "NVIDIA three-layer optimisation speeds up MoE inference on DGX Spark by
+ * 42.5%", its background section on sparse activation (a gating network
+ * scores every expert and only the top-k highest-scoring ones run). The
+ * pages give neither the tie rule nor the weight normalisation; the reading
+ * here is a softmax over the k selected keys, equal keys to the lower index.
+ *   logits_dev      fp32 [T][E] (device)
  *   bias_dev        fp32, NULL for none; bias_row_stride 0: one row [E]
  *                   for all tokens, >= E: row t at bias_dev + t*stride
- *   idx_dev         int32 [T][k], slots in descending key order
- *   w_dev           fp32 [T][k]
+ *   idx_dev         int32 [T][k], slots in descending key order (device)
+ *   w_dev           fp32 [T][k] (device)
  * Keys are logit + bias in fp32 (round-to-nearest-even); -0 ranks as +0, NaN
- * ranks as -inf; equal keys go to the lower expert index. E <= 1024, k <= 32. */
+ * ranks as -inf; equal keys go to the lower expert index. E <= 1024, k <= 32.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, T < 1, stride in (0, E)),
+ * MOE_ERR_UNSUPPORTED_SHAPE (E > 1024, k > 32 or k > E). */
 int moe_route_topk(const float* logits_dev, int T, int E, int k,
                    const float* bias_dev, int bias_row_stride,
                    int32_t* idx_dev, float* w_dev, moe_stream_t stream);
@@ -221,26 +238,47 @@ size_t moe_workspace_bytes(const moe_shape* shape, int T);
 int moe_query_path(const moe_shape* shape, int T);
 
 /* The layer over T tokens.
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §1
+ * (at batch 1, decode is bound by reading weights), §2 (8 of 512 routed
+ * experts plus one shared expert per token), §3 (moe_intermediate_size 768)
+ * and §5 (a 4-token verify window touches up to 32 distinct experts); the
+ * per-token formula is the one at the top of this file.
  *   L             host struct with device weight pointers and descriptors
- *   x_dev         bf16 [T][d];  y_dev bf16 [T][d] (may not alias x)
+ *   x_dev         bf16 [T][d] (device, 16-B aligned);  y_dev bf16 [T][d]
+ *                 (device; may not alias x)
  *   bias_dev      fp32 router bias as in moe_route_topk (NULL: none)
  *   logits_out    fp32 [T][E] router logits before bias (NULL: not returned)
  *   idx_out       int32 [T][k]; w_out fp32 [T][k] (NULL: not returned)
- *   workspace_dev >= moe_workspace_bytes(&L->shape, T) bytes, zero-filled
- *                 before its first use (see moe_workspace_bytes)
+ *   workspace_dev >= moe_workspace_bytes(&L->shape, T) bytes (device, 256-B
+ *                 aligned), zero-filled before its first use (see
+ *                 moe_workspace_bytes)
  *   dev_status    device int (may be NULL)
- *   stage_events  NULL, or n_stage_events cudaEvent_t handles (host array,
- *                 caller-created): event 0 is recorded on `stream` before the
- *                 first kernel and event i after stage i (stages listed by
- *                 moe_stage_names), for per-stage timing; extra events are
- *                 left untouched.
- * Activations must satisfy |x| < 2^100 and expert outputs stay finite. */
+ * Activations must satisfy |x| < 2^100 and expert outputs stay finite.
+ * Errors (nothing enqueued): MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_BAD_DESCRIPTOR (a packed buffer's descriptor does not match the
+ * shape: refused, never reinterpreted), MOE_ERR_WORKSPACE_TOO_SMALL,
+ * MOE_ERR_NO_DEVICE; MOE_ERR_CUDA if a launch fails. */
 int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
                 const float* bias_dev, int bias_row_stride,
                 float* logits_out, int32_t* idx_out, float* w_out,
                 void* workspace_dev, size_t workspace_bytes, int* dev_status,
-                void* const* stage_events, int n_stage_events,
                 moe_stream_t stream);
+
+/* Profiling hook: moe_forward that also records caller-created CUDA events
+ * at the boundaries of its stages, for per-stage timing. Same arguments and
+ * result as moe_forward, plus
+ *   stage_events  host array of n_stage_events cudaEvent_t handles: event 0
+ *                 is recorded on `stream` before the first kernel and event i
+ *                 after stage i (stages listed by moe_stage_names); extra
+ *                 events are left untouched. Under stream capture the records
+ *                 become external event nodes, so graph replays time them.
+ * The kernels launched are exactly moe_forward's. */
+int moe_forward_profiled(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                         const float* bias_dev, int bias_row_stride,
+                         float* logits_out, int32_t* idx_out, float* w_out,
+                         void* workspace_dev, size_t workspace_bytes, int* dev_status,
+                         void* const* stage_events, int n_stage_events,
+                         moe_stream_t stream);
 
 /* Size in bytes of the scratch array inside the library that
  * moe_forward_static_scratch uses instead of a caller's workspace. */
@@ -261,7 +299,9 @@ int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
  * is part of the library's device image (one per device). It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
- * Arguments are those of moe_forward without workspace and stage events.
+ * Arguments are those of moe_forward without the workspace. Every check of
+ * moe_forward is made before anything is enqueued: a call that returns an
+ * error has enqueued nothing.
  *
  *   - Set-up: the first call on each device, with that device current, looks
  *     up the array's device address (cudaGetSymbolAddress) and keeps it.
@@ -275,7 +315,7 @@ int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
  *     one stream or order them with events.
  *   - Returns MOE_ERR_WORKSPACE_TOO_SMALL, with nothing enqueued, when
  *     moe_workspace_bytes(&L->shape, T) > MOE_STATIC_SCRATCH_BYTES (at
- *     d = 2560, I = 768, E = 512, k = 8 that is T > 16). Larger calls need
+ *     d = 2560, I = 768, E = 512, k = 8 that is T > 30). Larger calls need
  *     moe_forward with a workspace of their own. */
 int moe_forward_static_scratch(const moe_layer* L, const void* x_dev, int T, void* y_dev,
                                const float* bias_dev, int bias_row_stride,
@@ -297,7 +337,7 @@ int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want, long long
 /* Static text for a moe_status value. */
 const char* moe_status_string(int status);
 
-/* Library version, e.g. "moe_mxfp4 1.0 sm_103a". */
+/* Library version, e.g. "moe_mxfp4 1.1 sm_103a". */
 const char* moe_version(void);
 
 #ifdef __cplusplus

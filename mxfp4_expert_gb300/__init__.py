@@ -19,12 +19,14 @@ __all__ = [
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
-    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_profiled", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
-# MOE_MXFP4_LIB may name another build of the same library (e.g. a debug build).
-LIB_PATH = os.environ.get("MOE_MXFP4_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
-                                                           "libmoe_mxfp4.so")
+# The in-tree build, and only it: there is no way to point the binding at
+# another library.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp4.so")
+# Version string the library must report (moe_version); anything else is refused.
+EXPECTED_VERSION = "moe_mxfp4 1.1 sm_103a"
 
 MOE_LAYOUT_MMA16 = 1
 MOE_LAYOUT_MMA16_GATEUP = 2
@@ -77,8 +79,9 @@ def _load():
         "moe_sort_by_expert": (i32, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
         "moe_workspace_bytes": (sz, [ctypes.POINTER(moe_shape), i32]),
         "moe_query_path": (i32, [ctypes.POINTER(moe_shape), i32]),
-        "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
-                                ctypes.POINTER(ctypes.c_void_p), i32, vp]),
+        "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]),
+        "moe_forward_profiled": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
+                                         ctypes.POINTER(ctypes.c_void_p), i32, vp]),
         "moe_forward_static_scratch": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, vp]),
         "moe_stage_names": (ctypes.c_char_p, [i32]),
         "moe_selftest_bounded_wait": (i32, [vp, ctypes.c_uint32, ctypes.c_longlong, vp, vp]),
@@ -88,6 +91,9 @@ def _load():
     for name, (res, args) in sig.items():
         f = getattr(L, name)
         f.restype, f.argtypes = res, args
+    got = L.moe_version().decode()
+    if got != EXPECTED_VERSION:
+        raise ImportError(f"{LIB_PATH} reports version {got!r}, this binding needs {EXPECTED_VERSION!r}; rebuild it")
     return L
 
 
@@ -261,38 +267,86 @@ class Layer:
         return moe_workspace_bytes(self.shape, T)
 
 
+def _forward_args(layer: Layer, x, bias, y, logits_out, idx_out, w_out, dev_status):
+    """Checks shared by the forward calls; returns (T, bias row stride).
+
+    The C library can only check pointers and sizes it is given; these checks
+    make sure every tensor is large enough for what the kernels write or read,
+    and that all of them live on the current device."""
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(y, torch.bfloat16, "y")
+    if x.dim() != 2 or x.shape[1] != layer.d:
+        raise ValueError(f"x must be [T, {layer.d}], got {tuple(x.shape)}")
+    if y.shape != x.shape:
+        raise ValueError(f"y must have x's shape {tuple(x.shape)}, got {tuple(y.shape)}")
+    T, E, k = x.shape[0], layer.shape.n_experts, layer.shape.top_k
+    dev = torch.cuda.current_device()
+    stride = 0
+    if bias is not None:
+        _cuda(bias, torch.float32, "bias")
+        if bias.dim() == 1:
+            if bias.numel() != E:
+                raise ValueError(f"bias must have {E} entries")
+        elif bias.dim() == 2 and bias.shape[0] >= T and bias.shape[1] == E:
+            stride = E
+        else:
+            raise ValueError(f"bias must be [{E}] or [T, {E}], got {tuple(bias.shape)}")
+    for name, t, dtype, n in (("logits_out", logits_out, torch.float32, T * E),
+                              ("idx_out", idx_out, torch.int32, T * k),
+                              ("w_out", w_out, torch.float32, T * k),
+                              ("dev_status", dev_status, torch.int32, 1)):
+        if t is not None:
+            _cuda(t, dtype, name)
+            if t.numel() < n:
+                raise ValueError(f"{name} needs at least {n} elements, got {t.numel()}")
+    for name, t in (("x", x), ("y", y), ("bias", bias), ("logits_out", logits_out), ("idx_out", idx_out),
+                    ("w_out", w_out), ("dev_status", dev_status)):
+        if t is not None and t.device.index != dev:
+            raise ValueError(f"{name} is on cuda:{t.device.index}, the current device is cuda:{dev}")
+    return T, stride
+
+
 def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
                 y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                 logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
                 w_out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
-                stage_events=None, stream=None):
+                stream=None):
     """y = layer(x) for bf16 x [T, d]; returns y (bf16 [T, d]).
 
     workspace: uint8 device tensor of layer.workspace_bytes(T) bytes, zero-filled
     before its first use (it carries synchronisation counters between calls);
     allocated with zeros when omitted.
-
-    stage_events: optional list of torch.cuda.Event (enable_timing=True); see
-    moe_stage_names for what each boundary marks.
     """
-    _cuda(x, torch.bfloat16, "x")
-    T = x.shape[0]
-    stride = 0
-    if bias is not None:
-        _cuda(bias, torch.float32, "bias")
-        stride = 0 if bias.dim() == 1 else bias.shape[1]
+    return _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, None, stream)
+
+
+def moe_forward_profiled(layer: Layer, x: torch.Tensor, stage_events, bias: torch.Tensor | None = None,
+                         y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
+                         w_out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                         stream=None):
+    """moe_forward that also records `stage_events` (torch.cuda.Event with
+    enable_timing=True) at its stage boundaries; see moe_stage_names."""
+    return _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, list(stage_events),
+                    stream)
+
+
+def _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, stage_events, stream):
     if y is None:
+        _cuda(x, torch.bfloat16, "x")
         y = torch.empty_like(x)
+    T, stride = _forward_args(layer, x, bias, y, logits_out, idx_out, w_out, dev_status)
     if workspace is None:
         workspace = torch.zeros(layer.workspace_bytes(T), dtype=torch.uint8, device=x.device)
-    ev_arr, n_ev = None, 0
-    if stage_events:
+    _cuda(workspace, torch.uint8, "workspace")
+    args = (ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride, _p(logits_out), _p(idx_out), _p(w_out),
+            _p(workspace), workspace.numel(), _p(dev_status))
+    if stage_events is None:
+        _check(lib.moe_forward(*args, _s(stream)), "moe_forward")
+    else:
         n_ev = len(stage_events)
         ev_arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in stage_events])
-    _check(lib.moe_forward(ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride, _p(logits_out),
-                           _p(idx_out), _p(w_out), _p(workspace), workspace.numel(), _p(dev_status),
-                           ev_arr, n_ev, _s(stream)),
-           "moe_forward")
+        _check(lib.moe_forward_profiled(*args, ev_arr, n_ev, _s(stream)), "moe_forward_profiled")
     return y
 
 
@@ -305,14 +359,10 @@ def moe_forward_static_scratch(layer: Layer, x: torch.Tensor, y: torch.Tensor, b
     for it. y (bf16 [T, d]) is the caller's. Calls on one device share that
     array, so calls that may overlap in time must be ordered by the caller;
     the first call on a device should come before any stream capture.
+    Every tensor is checked (shape, size, dtype, current device) before the
+    call, so a wrong buffer raises instead of letting a kernel run past it.
     """
-    _cuda(x, torch.bfloat16, "x")
-    _cuda(y, torch.bfloat16, "y")
-    T = x.shape[0]
-    stride = 0
-    if bias is not None:
-        _cuda(bias, torch.float32, "bias")
-        stride = 0 if bias.dim() == 1 else bias.shape[1]
+    T, stride = _forward_args(layer, x, bias, y, logits_out, idx_out, w_out, dev_status)
     _check(lib.moe_forward_static_scratch(ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride,
                                           _p(logits_out), _p(idx_out), _p(w_out), _p(dev_status), _s(stream)),
            "moe_forward_static_scratch")

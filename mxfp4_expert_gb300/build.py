@@ -49,14 +49,10 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=(), out_path: str = LIB_PATH,
-          build_dir: str = BUILD_DIR) -> str:
-    """Compile every CUDA source and link the shared library; returns its path.
-
-    extra_flags / out_path / build_dir allow a separately built variant (for
-    example with a debug define) next to the default library.
-    """
+def build(verbose: bool = False, force: bool = False) -> str:
+    """Compile every CUDA source and link the shared library; returns its path."""
     nvcc = _nvcc()
+    build_dir, out_path = BUILD_DIR, LIB_PATH
     os.makedirs(build_dir, exist_ok=True)
     hdrs = _headers()
     objs, jobs = [], []
@@ -64,7 +60,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags=(), out_path: 
         obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, __file__] + hdrs):
-            jobs.append([nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj])
+            jobs.append([nvcc, *NVCC_FLAGS, "-c", src, "-o", obj])
 
     def run(cmd):
         if verbose:

@@ -137,17 +137,18 @@ extern "C" int moe_query_path(const moe_shape* shape, int T) {
   return select_path(*shape, T, di);
 }
 
-extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
-                           const float* bias_dev, int bias_row_stride, float* logits_out,
-                           int32_t* idx_out, float* w_out, void* workspace_dev,
-                           size_t workspace_bytes, int* dev_status, void* const* stage_events,
-                           int n_stage_events, moe_stream_t stream) {
+namespace moe {
+namespace {
+
+// Every argument check of a forward call, done before anything is enqueued.
+// On MOE_OK, *ws holds the workspace plan and *di the current device.
+int validate_forward(const moe_layer* L, const void* x_dev, int T, const void* y_dev, int bias_row_stride,
+                     const void* workspace_dev, size_t workspace_bytes, Workspace* ws, DeviceInfo* di) {
   MOE_CHECK_ARG(L && x_dev && y_dev && workspace_dev, MOE_ERR_INVALID_ARG);
-  MOE_CHECK_ARG(n_stage_events >= 0 && (stage_events || n_stage_events == 0), MOE_ERR_INVALID_ARG);
   int st = check_shape(&L->shape, T);
   if (st != MOE_OK) return st;
   const moe_shape& sh = L->shape;
-  const int d = sh.d_model, I = sh.d_ff, E = sh.n_experts, k = sh.top_k;
+  const int d = sh.d_model, I = sh.d_ff, E = sh.n_experts;
   MOE_CHECK_ARG(L->router_w && L->gate_up && L->down, MOE_ERR_INVALID_ARG);
   MOE_CHECK_ARG(!sh.has_shared || (L->shared_gate && L->shared_up && L->shared_down), MOE_ERR_INVALID_ARG);
   MOE_CHECK_ARG(bias_row_stride == 0 || bias_row_stride >= E, MOE_ERR_INVALID_ARG);
@@ -160,12 +161,20 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
   MOE_CHECK_ARG(!sh.has_shared || (aligned(L->shared_gate, 16) && aligned(L->shared_up, 16) &&
                                    aligned(L->shared_down, 16)),
                 MOE_ERR_INVALID_ARG);
-  const Workspace ws = plan(sh, T);
-  MOE_CHECK_ARG(workspace_bytes >= ws.total, MOE_ERR_WORKSPACE_TOO_SMALL);
-  DeviceInfo di;
-  st = current_device(&di);
-  if (st != MOE_OK) return st;
+  *ws = plan(sh, T);
+  MOE_CHECK_ARG(workspace_bytes >= ws->total, MOE_ERR_WORKSPACE_TOO_SMALL);
+  return current_device(di);
+}
 
+// The kernel sequence of one validated forward call on `stream`; stage_events
+// as in moe_forward_profiled (n_stage_events 0: none).
+int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, const float* bias_dev,
+                    int bias_row_stride, float* logits_out, int32_t* idx_out, float* w_out, void* workspace_dev,
+                    int* dev_status, void* const* stage_events, int n_stage_events, moe_stream_t stream,
+                    const Workspace& ws, const DeviceInfo& di) {
+  int st = MOE_OK;
+  const moe_shape& sh = L->shape;
+  const int d = sh.d_model, I = sh.d_ff, E = sh.n_experts, k = sh.top_k;
   cudaStream_t s = (cudaStream_t)stream;
   void* B = workspace_dev;
   float* logits = logits_out ? logits_out : at<float>(B, ws.logits);
@@ -335,6 +344,35 @@ extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y
   return mark();
 }
 
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                           const float* bias_dev, int bias_row_stride, float* logits_out,
+                           int32_t* idx_out, float* w_out, void* workspace_dev,
+                           size_t workspace_bytes, int* dev_status, moe_stream_t stream) {
+  Workspace ws;
+  DeviceInfo di;
+  const int st = validate_forward(L, x_dev, T, y_dev, bias_row_stride, workspace_dev, workspace_bytes, &ws, &di);
+  if (st != MOE_OK) return st;
+  return enqueue_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, workspace_dev,
+                         dev_status, nullptr, 0, stream, ws, di);
+}
+
+extern "C" int moe_forward_profiled(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                                    const float* bias_dev, int bias_row_stride, float* logits_out,
+                                    int32_t* idx_out, float* w_out, void* workspace_dev,
+                                    size_t workspace_bytes, int* dev_status, void* const* stage_events,
+                                    int n_stage_events, moe_stream_t stream) {
+  MOE_CHECK_ARG(n_stage_events >= 0 && (stage_events || n_stage_events == 0), MOE_ERR_INVALID_ARG);
+  Workspace ws;
+  DeviceInfo di;
+  const int st = validate_forward(L, x_dev, T, y_dev, bias_row_stride, workspace_dev, workspace_bytes, &ws, &di);
+  if (st != MOE_OK) return st;
+  return enqueue_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, workspace_dev,
+                         dev_status, stage_events, n_stage_events, stream, ws, di);
+}
+
 namespace moe {
 namespace {
 // Scratch of moe_forward_static_scratch: part of this library's device image,
@@ -342,18 +380,50 @@ namespace {
 // a device uses the same bytes.
 static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
 
-// Device address of g_static_scratch on device `dev` (the current device),
-// looked up the first time that device calls and cached afterwards.
+// Identity of the calling thread's current CUDA context (0 if it has none).
+// A device's primary context gets a new identity when it is destroyed and
+// created again (cudaDeviceReset), which invalidates device addresses.
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);                  // cuCtxGetCurrent
+  using GetId = int (*)(void*, unsigned long long*);   // cuCtxGetId
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+    (void)cudaGetLastError();
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Device address of g_static_scratch on device `dev` (the current device).
+// It is looked up with cudaGetSymbolAddress the first time the device calls,
+// and again whenever the device's context has changed since (after a
+// cudaDeviceReset the old address is no longer valid).
 int static_scratch_address(int dev, void** out) {
   static std::mutex mu;
   static void* cache[64] = {};
+  static unsigned long long cache_ctx[64] = {};
   if (dev < 0 || dev >= 64) return MOE_ERR_NO_DEVICE;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!cache[dev] || ctx == 0 || ctx != cache_ctx[dev]) {
     void* p = nullptr;
     MOE_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_scratch));
     if (!p) return MOE_ERR_CUDA;
     cache[dev] = p;
+    cache_ctx[dev] = current_context_id();   // the lookup made the context current if it was not
   }
   *out = cache[dev];
   return MOE_OK;
@@ -368,19 +438,22 @@ extern "C" int moe_forward_static_scratch(const moe_layer* L, const void* x_dev,
   MOE_CHECK_ARG(L && x_dev && y_dev, MOE_ERR_INVALID_ARG);
   int st = check_shape(&L->shape, T);
   if (st != MOE_OK) return st;
-  const Workspace ws = plan(L->shape, T);
-  if (ws.total > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (plan(L->shape, T).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo di;
   if ((st = current_device(&di))) return st;
   void* scratch = nullptr;
   if ((st = static_scratch_address(di.device, &scratch))) return st;
+  // every check of moe_forward, before anything is enqueued
+  Workspace ws;
+  st = validate_forward(L, x_dev, T, y_dev, bias_row_stride, scratch, MOE_STATIC_SCRATCH_BYTES, &ws, &di);
+  if (st != MOE_OK) return st;
   // The synchronisation counters at the head of the workspace must read zero
   // when the call's kernels start; clear them on the call's own stream so a
   // call never depends on how an earlier one ended.
   MOE_CUDA_TRY(cudaMemsetAsync(static_cast<char*>(scratch) + ws.state, 0,
                                decode_state_bytes(L->shape.n_experts, L->shape.d_ff), (cudaStream_t)stream));
-  return moe_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, scratch,
-                     MOE_STATIC_SCRATCH_BYTES, dev_status, nullptr, 0, stream);
+  return enqueue_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, scratch,
+                         dev_status, nullptr, 0, stream, ws, di);
 }
 
 extern "C" const char* moe_stage_names(int path) {
@@ -405,7 +478,7 @@ extern "C" const char* moe_status_string(int status) {
   }
 }
 
-extern "C" const char* moe_version(void) { return "moe_mxfp4 1.0 sm_103a"; }
+extern "C" const char* moe_version(void) { return "moe_mxfp4 1.1 sm_103a"; }
 
 namespace moe {
 namespace {
@@ -427,13 +500,3 @@ extern "C" int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want
   wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag_dev, want, budget_cycles, dev_status);
   return launch_status();
 }
-
-#ifdef MOE_DECODE_TRACE
-namespace moe {
-int decode_trace_copy(unsigned long long* host, int n_cta);
-}
-// Debug builds only: phase timestamps of the last single-launch decode call.
-extern "C" int moe_debug_decode_trace(unsigned long long* host, int n_cta) {
-  return moe::decode_trace_copy(host, n_cta);
-}
-#endif

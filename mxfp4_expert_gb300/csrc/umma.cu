@@ -31,9 +31,6 @@
 // ends the other roles' waits at once, and the kernel drains its own copies
 // and MMAs before it frees tensor memory and returns.
 #include <cuda_runtime.h>
-#ifdef MOE_UMMA_TRACE
-#include <cstdio>
-#endif
 
 #include "common.cuh"
 #include "host_util.h"
@@ -166,20 +163,6 @@ __device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile i
   }
   return true;
 }
-
-// debug build only: cycles per slice spent in up to four sections of a role
-#ifdef MOE_UMMA_TRACE
-#define UT_DECL long long ut_acc[4] = {0, 0, 0, 0}; long long ut_t = clock64();
-#define UT(i) do { const long long _t = clock64(); ut_acc[i] += _t - ut_t; ut_t = _t; } while (0)
-#define UT_PRINT(role, n)                                                                                  \
-  if (blockIdx.x == 0)                                                                                     \
-    printf("  %-9s cycles per slice: %6lld %6lld %6lld %6lld\n", role, ut_acc[0] / (n), ut_acc[1] / (n), \
-           ut_acc[2] / (n), ut_acc[3] / (n));
-#else
-#define UT_DECL
-#define UT(i) do { } while (0)
-#define UT_PRINT(role, n) (void)0;
-#endif
 
 template <int MODE>
 __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, UmmaSmem L) {
@@ -335,7 +318,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   if (warp == kWProducer) {
     // ---- packed weights -> raw ring ----------------------------------------------
     if (lane == 0) {
-      UT_DECL
       int issued = 0, pf_next = 0;
       const int pf_items = (kUPrefetchChunks + nch - 1) / nch;
       const uint8_t* wm = nullptr;
@@ -346,9 +328,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       for (int c = 0; c < n_chunks; ++c) {
         const int j = c / nch, cc = c - j * nch, s = c % kURing;
         if (c >= kURing && !uwait(&empty_raw[s], uint32_t(c / kURing - 1) & 1u, abort, a.status)) break;
-        UT(0);
         if (cc == 0) {
-          UT(0);
           const Item f = item_of(j);
           nt = min(kUTiles, a.n_tiles - f.rb * kUTiles);
           wm = item_base(f);
@@ -358,7 +338,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
             const int gt = min(kUTiles, a.n_tiles - g.rb * kUTiles);
             prefetch_l2(item_base(g), uint32_t(gt) * KB * kUnitBytes);
           }
-          UT(2);
         }
         const int kb0 = cc * kUChunk * kUSliceKb, nkb = min(kUChunk * kUSliceKb, KB - kb0);
         uint8_t* dst = ring + (size_t)s * kURawBytes;
@@ -367,24 +346,19 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           bulk_g2s(dst + (size_t)t * kUTileChunk, wm + ((uint64_t)t * KB + kb0) * kUnitBytes,
                    uint32_t(nkb) * kUnitBytes, &full_raw[s]);
         issued = c + 1;
-        UT(1);
       }
       if (*abort)   // copies still in flight land before the CTA's shared memory goes away
         for (int c = issued > kURing ? issued - kURing : 0; c < issued; ++c)
           mbar_wait(&full_raw[c % kURing], uint32_t(c / kURing) & 1u, a.status);
-      UT_PRINT("producer", n_stream)
     }
   } else if (warp == kWMma) {
     // ---- tcgen05.mma issue -----------------------------------------------------------
     if (lane == 0) {
-      UT_DECL
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
       bool ok = true;
       for (int j = 0; j < n_mine && ok; ++j) {
-        UT(0);
         const Item f = item_of(j);
-        UT(2);
         const int ab = j % kUAcc;
         if (j >= kUAcc && !uwait(&acc_empty[ab], uint32_t(j / kUAcc - 1) & 1u, abort, a.status)) break;
         tc_fence_after();
@@ -397,9 +371,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
             ok = false;
             break;
           }
-          UT(0);
           tc_fence_after();
-          UT(3);
           const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
           const uint32_t as = smem_addr(abuf + (size_t)st * kUABytes);
           const uint32_t bs = smem_addr(bbuf + (size_t)st * kUBBytes);
@@ -409,25 +381,20 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           last = &op_empty[st];
           last_par = par;
           if (sl == ns - 1) umma_commit(&acc_full[ab]);
-          UT(1);
         }
       }
       // every MMA has finished before tensor memory is freed
       if (last) mbar_wait(last, last_par, a.status);
-      UT_PRINT("mma", n_stream)
     }
   } else if (warp < kWLoad) {
     // ---- epilogue: accumulator -> outputs --------------------------------------------
-    UT_DECL
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;   // TMEM lane = weight row of the item
     for (int j = 0; j < n_mine; ++j) {
       const int ab = j % kUAcc;
       if (!uwait(&acc_full[ab], uint32_t(j / kUAcc) & 1u, abort, a.status)) break;
-      UT(0);
       tc_fence_after();
       const Item f = item_of(j);
-      UT(2);
       const uint32_t trow = tmem + uint32_t(ab * kUCols) + ((uint32_t)(quarter * 32) << 16);
       if (MODE == kModeGateUp) {
         // rows 16t .. 16t+7: gate of features 8 (rb*8 + t) + 0..7; rows +8: up.
@@ -469,15 +436,12 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
-      UT(1);
     }
-    if (lane == 0 && warp == kWEpi) UT_PRINT("epilogue", n_stream)
   } else if (warp < kWDec) {
     // ---- activation rows -> operand stage (cp.async) --------------------------------
     // Thread lt copies 16-byte column c = lt % 8 of rows lt / 8 + 16 m. Gate/up:
     // the rows are tokens (x rows gathered through perm). Down: the rows are
     // sorted slots, hi terms to B rows r and lo terms to B rows n16 + r.
-    UT_DECL
     const int lt = tid - kWLoad * 32, c = lt & 7, rr = lt >> 3;
     constexpr int kRows = MODE == kModeGateUp ? kUCols / 16 : kUCols / 32;   // rows per thread
     const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
@@ -498,14 +462,11 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     for (int p = 0; p < n_stream; ++p) {
       const int j = p / ns, sl = p - j * ns, st = p % kUStages;
       if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
-      UT(0);
       if (sl == 0) {
         f = item_of(j);
-        UT(2);
 #pragma unroll
         for (int m = 0; m < kRows; ++m) b_row[m] = nb_row[m];
         if (j + 1 < n_mine) rows_of(j + 1, nb_row);
-        UT(3);
       }
       const int kb0 = sl * kUSliceKb, nc = min(kUSliceKb, KB - kb0) * (kMxBlock / 8);
       uint8_t* bb = bbuf + (size_t)st * kUBBytes;
@@ -531,7 +492,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
         ++pend;
       }
-      UT(1);
     }
     cp_async_wait<0>();   // nothing lands after the CTA's shared memory goes away
     if (!*abort) {
@@ -540,11 +500,9 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       for (; pend < n_stream; ++pend)
         if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
     }
-    if (lt == 0) UT_PRINT("loader", n_stream)
   } else {
     // ---- raw ring -> bf16 weights (decode warp dw: tile dw % 8 of the item, the
     // slice's 32-wide K-blocks u = dw / 8, dw / 8 + 2, ...) ----------------------------
-    UT_DECL
     const int dw = warp - kWDec, t = dw % kUTiles;
     const int g = lane >> 2, q = lane & 3;
     int tile = 0;
@@ -552,12 +510,9 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       const int j = p / ns, sl = p - j * ns, st = p % kUStages;
       const int cc = sl / kUChunk, sub = sl - cc * kUChunk, c = j * nch + cc, s = c % kURing;
       if (sub == 0 && !uwait(&full_raw[s], uint32_t(c / kURing) & 1u, abort, a.status)) break;
-      UT(0);
       if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
-      UT(1);
       if (sl == 0) {
         tile = item_of(j).rb * kUTiles + t;
-        UT(3);
       }
       const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
       const uint8_t* raw = ring + (size_t)s * kURawBytes + (size_t)t * kUTileChunk + (size_t)sub * kUSliceKb * kUnitBytes;
@@ -590,9 +545,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         mbar_arrive(&a_full[st]);
         if (sub == kUChunk - 1 || sl == ns - 1) mbar_arrive(&empty_raw[s]);   // chunk consumed
       }
-      UT(2);
     }
-    if (lane == 0 && dw == 0) UT_PRINT("decode", n_stream)
   }
 
   tc_fence_before();

@@ -131,7 +131,21 @@ class Expert:
         return cls(gu[:I], gu[I:], dn)
 
 
-def moe_layer(x, router_w, experts, shared, k: int, bias=None, idx=None, logits_f32=None):
+def expert_outputs(x_rows, gate_up_f32, down_f32) -> np.ndarray:
+    """One routed expert applied to some token rows, in fp64.
+
+    The expert's fp32 weights (gate_up [2I, d], down [d, I]) are quantised
+    with the MX rule (Expert.from_fp32), then out = Wd (silu(Wg x) * (Wu x))
+    for every row of x_rows [n, d]. This is step 4 of the layer on its own,
+    so that callers can evaluate many experts in separate processes and hand
+    the results to moe_layer(expert_out=...).
+    """
+    e = Expert.from_fp32(gate_up_f32, down_f32)
+    return swiglu_ffn(as_f64(x_rows), e.gate, e.up, e.down)
+
+
+def moe_layer(x, router_w, experts, shared, k: int, bias=None, idx=None, logits_f32=None,
+              expert_out=None):
     """The whole layer in fp64.
 
     x          [T, d] (bf16 values)
@@ -142,6 +156,9 @@ def moe_layer(x, router_w, experts, shared, k: int, bias=None, idx=None, logits_
     idx        optional [T, k] routing to use instead of the oracle's own
                (the GPU-reported indices, after they were checked)
     logits_f32 optional fp32 logits to rank; default: fp32(oracle fp64 logits)
+    expert_out optional mapping (t, j) -> out_{idx[t, j]}(x_t) [d] from
+               expert_outputs(); used instead of `experts` (which may then be
+               None). The weights and the sum below are the same either way.
 
     Returns dict(logits fp64 [T,E], idx [T,k], weights fp64 [T,k], y fp64 [T,d]).
     Weights are computed from the oracle's fp64 logits (plus bias) at the
@@ -164,8 +181,12 @@ def moe_layer(x, router_w, experts, shared, k: int, bias=None, idx=None, logits_
         ex = np.exp(kv - kv.max())
         wts[t] = ex / ex.sum()
         for j in range(k):
-            ex_ = experts[int(idx[t, j])]
-            y[t] += wts[t, j] * swiglu_ffn(x[t:t + 1], ex_.gate, ex_.up, ex_.down)[0]
+            if expert_out is not None:
+                out = np.asarray(expert_out[(t, j)], dtype=np.float64)
+            else:
+                ex_ = experts[int(idx[t, j])]
+                out = swiglu_ffn(x[t:t + 1], ex_.gate, ex_.up, ex_.down)[0]
+            y[t] += wts[t, j] * out
     if shared is not None:
         sg, su, sd = (as_f64(a) for a in shared)
         y += swiglu_ffn(x, sg, su, sd)

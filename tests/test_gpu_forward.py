@@ -4,15 +4,19 @@ Per call: (1) the GPU's router logits are within 1e-5 * sum_j |x_j Wr_j| of
 the oracle's fp64 logits; (2) the GPU's indices equal the oracle's ranking of
 the GPU's own fp32 logits (plus bias) and the weights agree to 2e-6;
 (3) y (bf16) against the oracle's fp64 layer output computed with those
-indices: relative L2 <= 5e-3 and, per element, |err| <= 2e-2 * rms(y_ref)
-plus half a bf16 ulp of y_ref (the rounding of the bf16 output itself).
-Full-size workloads are checked on every token where the oracle is cheap
-(T = 1, 4) and on sampled tokens otherwise (T = 64, 4096).
+indices: relative L2 <= 5e-3 and max |err| <= 2e-2 * rms(y_ref) per element.
+The one exception to the per-element bound is an element whose GPU value is
+exactly y_ref rounded to the nearest bf16 (no bf16 output can be closer);
+such elements are counted, and the Ling-shape workloads require none.
+Workloads are checked on every token, except prefill (T = 4096), which is
+checked on at least 256 tokens chosen so that every expert is some checked
+token's choice.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle_par
 import workloads as wl
 from oracle import moe as omoe
 
@@ -39,7 +43,9 @@ def run(mx, layer, x, bias, T, E, k):
     return y, logits, idx, w
 
 
-def check_layer(w, set_idx, layer, x, bias, out, tokens=None, device="cuda"):
+def check_layer(w, set_idx, layer, x, bias, out, tokens=None, device="cuda", strict=False):
+    """Checks (1)-(3) on `tokens` (default: all). Returns (rel-L2, max|err|/rms,
+    elements that needed the bf16-rounding exception); strict=True requires none."""
     y, logits, idx, wts = out
     tokens = list(range(w.T)) if tokens is None else list(tokens)
     xs = x[tokens].cpu()
@@ -60,29 +66,26 @@ def check_layer(w, set_idx, layer, x, bias, out, tokens=None, device="cuda"):
     assert np.array_equal(gi, ri)
     assert np.all(np.abs(wts.cpu().numpy()[tokens] - rw) <= 2e-6)
     # (3) y with the oracle's expert values at those indices
-    needed = sorted(set(gi.ravel().tolist()))
-    experts = {}
-    for e in needed:
-        gu, dn = wl.gen_expert(w, set_idx, e, device)
-        experts[e] = omoe.Expert.from_fp32(gu.cpu().numpy(), dn.cpu().numpy())
     shared = tuple(t.cpu() for t in wl.gen_shared(w, set_idx, device))
-    ref = omoe.moe_layer(xs, router, experts, shared, w.k, bias=b, idx=gi)
+    if not layer.shape.has_shared:
+        shared = None
+    ref = oracle_par.reference_layer(w, set_idx, xs, router, shared, b, gi, device)
     yg = y.float().cpu().numpy().astype(np.float64)[tokens]
     yr = ref["y"]
     rel = np.linalg.norm(yg - yr) / np.linalg.norm(yr)
     rms = np.sqrt(np.mean(yr ** 2))
     err = np.abs(yg - yr)
     assert rel <= REL_L2, rel
-    # y is bf16: no result can be closer than half a bf16 ulp of the exact value
-    assert np.all(err <= MAX_ABS * rms + 0.5 * bf16_ulp(yr)), (err.max(), rms)
-    return rel, err.max() / rms
-
-
-def bf16_ulp(v):
-    """Spacing of bf16 numbers (8 significant bits) at |v|; 0 at v = 0."""
-    a = np.abs(np.asarray(v, dtype=np.float64))
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    return np.where(a > 0, np.exp2(e - 7), 0.0)
+    within = err <= MAX_ABS * rms
+    rounded = yg == oracle_par.bf16_rne(yr)
+    bad = ~(within | rounded)
+    assert not bad.any(), (int(bad.sum()), float(err.max() / rms))
+    n_exc = int(np.sum(~within))
+    if strict:
+        assert n_exc == 0, n_exc
+    print(f"{w.name} set {set_idx}: {len(tokens)} tokens, rel-L2 {rel:.2e}, max|err|/rms {err.max() / rms:.2e}, "
+          f"bf16-rounding exceptions {n_exc}")
+    return rel, err.max() / rms, n_exc
 
 
 def build(mx, w, set_idx=0):
@@ -150,7 +153,7 @@ def test_ling_t1(mx):
     for s in (0, 1):
         layer, x, bias = build(mx, w, s)
         out = run(mx, layer, x, bias, w.T, w.E, w.k)
-        check_layer(w, s, layer, x, bias, out)
+        check_layer(w, s, layer, x, bias, out, strict=True)
         del layer
         torch.cuda.empty_cache()
 
@@ -162,26 +165,62 @@ def test_mtp_t4(mx):
         out = run(mx, layer, x, bias, w.T, w.E, w.k)
         D, sets = wl.mtp_expert_sets(w, s)
         assert len(set(out[2].cpu().numpy().ravel().tolist())) == D
-        check_layer(w, s, layer, x, bias, out)
+        check_layer(w, s, layer, x, bias, out, strict=True)
         del layer
         torch.cuda.empty_cache()
 
 
-def test_zipf_t64_sampled(mx):
+@pytest.mark.parametrize("T", [8, 16])
+def test_ling_shape_per_stage_mma(mx, T):
+    """Ling shapes at 5 <= T < 32 (the per-stage e4m3 mma.sync path), every token."""
+    w = wl.get("ling_t1", name=f"ling_t{T}", T=T, sets=1)
+    layer, x, bias = build(mx, w, 0)
+    assert mx.moe_query_path(layer.shape, T) == mx.MOE_PATH_DECODE_MMA
+    out = run(mx, layer, x, bias, w.T, w.E, w.k)
+    check_layer(w, 0, layer, x, bias, out, strict=True)
+
+
+def test_zipf_t64(mx):
+    """T = 64 with Zipf(1.1) expert popularity: every token."""
     w = wl.get("zipf_t64")
     layer, x, bias = build(mx, w, 0)
     out = run(mx, layer, x, bias, w.T, w.E, w.k)
     D = len(set(out[2].cpu().numpy().ravel().tolist()))
     assert 100 <= D <= 220
-    check_layer(w, 0, layer, x, bias, out, tokens=[0, 17, 40, 63])
+    check_layer(w, 0, layer, x, bias, out, strict=True)
+
+
+def covering_tokens(idx, E, at_least):
+    """Tokens such that every expert in [0, E) is the choice of one of them
+    (greedy set cover over the tokens' top-k sets), topped up with evenly
+    spaced tokens to `at_least`; sorted."""
+    T = idx.shape[0]
+    sets = [set(r.tolist()) for r in idx]
+    left, chosen = set(range(E)), set()
+    while left:
+        t = max(range(T), key=lambda i: (len(sets[i] & left), -i))
+        if not sets[t] & left:
+            break
+        chosen.add(t)
+        left -= sets[t]
+    assert not left, f"experts never chosen: {sorted(left)[:8]}"
+    for t in np.linspace(0, T - 1, at_least).astype(int):
+        if len(chosen) >= at_least:
+            break
+        chosen.add(int(t))
+    return sorted(chosen)
 
 
 @pytest.mark.slow
-def test_prefill_t4096_sampled(mx):
+def test_prefill_t4096(mx):
+    """T = 4096: at least 256 tokens that between them choose all 512 experts,
+    so every expert's work items on the grouped-GEMM path are checked."""
     w = wl.get("prefill_t4096")
     layer, x, bias = build(mx, w, 0)
     out = run(mx, layer, x, bias, w.T, w.E, w.k)
-    check_layer(w, 0, layer, x, bias, out, tokens=[0, 1, 2047, 4095])
+    toks = covering_tokens(out[2].cpu().numpy(), w.E, 256)
+    assert len(toks) >= 256
+    check_layer(w, 0, layer, x, bias, out, tokens=toks, strict=True)
 
 
 def test_deterministic(mx):

@@ -96,6 +96,34 @@ def test_experts_from_fp32_use_the_mx_values():
     assert np.array_equal(e.down, mxfp4.fake_quantize(dn))
 
 
+def test_expert_outputs_path_matches_triple_loop():
+    """moe_layer(expert_out=...) with per-(token, slot) outputs from
+    expert_outputs() gives the triple loop's layer (the path the full-size
+    GPU parity checks use to spread the oracle over processes)."""
+    rng = np.random.default_rng(6)
+    T, d, I, E, k = 3, 64, 32, 8, 2
+    x = rng.standard_normal((T, d))
+    wr = rng.standard_normal((E, d)) * 0.1
+    raw = {e: ((rng.standard_normal((2 * I, d)) * 0.05).astype(np.float32),
+               (rng.standard_normal((d, I)) * 0.05).astype(np.float32)) for e in range(E)}
+    experts = {e: moe.Expert.from_fp32(*raw[e]) for e in range(E)}
+    shared = tuple(rng.standard_normal(s) * 0.05 for s in [(I, d), (I, d), (d, I)])
+    idx = moe.moe_layer(x, wr, experts, shared, k=k)["idx"]
+    outs = {}
+    for e in set(idx.ravel().tolist()):
+        pairs = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        rows = moe.expert_outputs(x[[t for t, _ in pairs]], *raw[e])
+        outs.update({p: rows[i] for i, p in enumerate(pairs)})
+    out = moe.moe_layer(x, wr, None, shared, k=k, idx=idx, expert_out=outs)
+    ref = triple_loop_layer(x, wr, experts, shared, k=k)
+    assert np.allclose(out["y"], ref, rtol=1e-11, atol=1e-12)
+    # a wrong pairing (slots of one token swapped) is visible
+    bad = dict(outs)
+    bad[(0, 0)], bad[(0, 1)] = outs[(0, 1)], outs[(0, 0)]
+    wrong = moe.moe_layer(x, wr, None, shared, k=k, idx=idx, expert_out=bad)["y"]
+    assert _rel(wrong, ref) > 1e-3
+
+
 # planted mistakes: each plausible bug must change the result beyond tolerance ----
 
 def _rel(a, b):

@@ -211,3 +211,19 @@ def test_planted_mistake_is_caught(make):
     mutant = make()
     results = [pin(mutant) for pin in PINS]
     assert not all(results), "a planted mistake passed every pin"
+
+
+def test_bf16_rounding_helper_matches_torch():
+    """The parity tests' bf16 rounding (fp64 -> nearest bf16, ties to even)
+    agrees with torch's fp32 -> bf16 conversion on fp32 inputs, including
+    exact ties and values next to them."""
+    import torch
+    import oracle_par
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(20000) * np.exp2(rng.integers(-20, 20, 20000))).astype(np.float32)
+    bits = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x3F808001, 0x3F807FFF, 0x00008000, 0x7F7E8000],
+                    dtype=np.uint32).view(np.float32)   # ties at even / odd mantissas, neighbours, subnormal, large (below the bf16 maximum)
+    v = np.concatenate([v, bits])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle_par.bf16_rne(v.astype(np.float64))
+    assert np.array_equal(got, ref)

@@ -69,6 +69,81 @@ def test_static_scratch_matches_moe_forward_twice(mx, name, T):
         _compare(mx, layer, _x(w, call, T), None, w)
 
 
+def test_static_scratch_ling_limit(mx):
+    """At the Ling shape the 4 MiB array holds the workspace of up to 30
+    tokens: T = 30 runs (and matches moe_forward), T = 31 is refused with
+    MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued."""
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS["ling_t1"]
+    layer = synthetic.build_layer(w, 0)
+    assert mx.moe_workspace_bytes(layer.shape, 30) <= mx.STATIC_SCRATCH_BYTES
+    assert mx.moe_workspace_bytes(layer.shape, 31) > mx.STATIC_SCRATCH_BYTES
+    _compare(mx, layer, _x(w, 0, 30), None, w)
+    x = _x(w, 1, 31)
+    y = torch.full_like(x, 7.0)
+    with pytest.raises(mx.MoeError) as ei:
+        mx.moe_forward_static_scratch(layer, x, y)
+    assert ei.value.status == -4
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+
+
+def test_static_scratch_allocates_nothing(mx):
+    """A warmed-up call changes neither the device's free memory nor the
+    caching allocator's reserved bytes."""
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS["ling_t1"]
+    layer = synthetic.build_layer(w, 0)
+    x = _x(w, 2, 4)
+    y = torch.empty_like(x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mx.moe_forward_static_scratch(layer, x, y, dev_status=st)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    res0 = torch.cuda.memory_reserved()
+    for _ in range(3):
+        mx.moe_forward_static_scratch(layer, x, y, dev_status=st)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0 and torch.cuda.memory_reserved() == res0
+    assert int(st.item()) == 0
+
+
+def test_static_scratch_after_a_timed_out_wait(mx):
+    """Each call clears the counters it needs, so it does not depend on how an
+    earlier kernel ended: after a bounded wait that gave up (a flag nothing
+    sets), the next call still matches moe_forward."""
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS["ling_t1"]
+    layer = synthetic.build_layer(w, 0)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mx.moe_selftest_bounded_wait(flag, 1, 2_000_000, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & mx.DEV_TIMEOUT
+    _compare(mx, layer, _x(w, 3, 1), None, w)
+
+
+def test_static_scratch_checks_buffers(mx):
+    """Buffers too small for what the kernels write, or of the wrong width, are
+    refused by the binding before the library is called."""
+    from mxfp4_expert_gb300 import synthetic
+    w = wl.WORKLOADS["tiny"]
+    layer = synthetic.build_layer(w, 0)
+    x = _x(w, 0, 2)
+    with pytest.raises(ValueError):
+        mx.moe_forward_static_scratch(layer, x, torch.empty((1, w.d), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        mx.moe_forward_static_scratch(layer, x[:, :256].contiguous(), torch.empty((2, 256), dtype=torch.bfloat16,
+                                                                                 device="cuda"))
+    with pytest.raises(ValueError):
+        mx.moe_forward_static_scratch(layer, x, torch.empty_like(x),
+                                      logits_out=torch.empty(w.E, dtype=torch.float32, device="cuda"))
+    with pytest.raises(ValueError):
+        mx.moe_forward_static_scratch(layer, x, torch.empty_like(x),
+                                      idx_out=torch.empty(w.k, dtype=torch.int32, device="cuda"))
+
+
 def test_static_scratch_rejects_too_large(mx):
     from mxfp4_expert_gb300 import synthetic
     w = wl.WORKLOADS["tiny"]
