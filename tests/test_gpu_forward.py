@@ -12,6 +12,8 @@ Workloads are checked on every token, except prefill (T = 4096), which is
 checked on at least 256 tokens chosen so that every expert is some checked
 token's choice.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -173,7 +175,7 @@ def test_mtp_t4(mx):
 @pytest.mark.parametrize("T", [8, 16])
 def test_ling_shape_per_stage_mma(mx, T):
     """Ling shapes at 5 <= T < 32 (the per-stage e4m3 mma.sync path), every token."""
-    w = wl.get("ling_t1", name=f"ling_t{T}", T=T, sets=1)
+    w = dataclasses.replace(wl.WORKLOADS["ling_t1"], name=f"ling_t{T}", T=T, sets=1)
     layer, x, bias = build(mx, w, 0)
     assert mx.moe_query_path(layer.shape, T) == mx.MOE_PATH_DECODE_MMA
     out = run(mx, layer, x, bias, w.T, w.E, w.k)
