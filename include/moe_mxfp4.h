@@ -138,9 +138,10 @@ typedef enum moe_path {
                                 call (router, top-k, shared and routed experts,
                                 combine), one CTA per SM */
   MOE_PATH_PREFILL_TC = 3    /* T >= 32: per-stage kernels with the routed
-                                experts as grouped GEMMs on the tcgen05 tensor
-                                cores (MXFP4 decoded to bf16 in shared memory,
-                                fp32 accumulators in tensor memory) */
+                                experts as grouped GEMMs on block-scaled tcgen05
+                                MMAs (MXFP4 weights as E4M3 codes with E8M0
+                                scales, activations as E4M3 terms with E8M0
+                                scales, fp32 accumulators in tensor memory) */
 } moe_path;
 
 /* ---- packing ------------------------------------------------------------ */
@@ -279,6 +280,35 @@ int moe_forward_profiled(const moe_layer* L, const void* x_dev, int T, void* y_d
                          void* workspace_dev, size_t workspace_bytes, int* dev_status,
                          void* const* stage_events, int n_stage_events,
                          moe_stream_t stream);
+
+/* The layer with 8-bit activations (W4A8): before each routed-expert GEMM the
+ * activations (x for gate/up, h for down) are quantised to MXFP8 - E4M3
+ * elements with one E8M0 scale per 32, OCP MX v1.0 rule s = floor(log2 amax)
+ * - 8 + 127, round to nearest even, saturate at 448 - and the GEMMs run on
+ * block-scaled tcgen05 MMAs. Router and shared expert stay bf16.
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §2
+ * (the baseline runs the W4A8 configuration of the FlashInfer MXFP4 MoE
+ * kernel). The pages do not define the 8-bit format; MXFP8 E4M3 is the reading.
+ * Arguments, workspace and errors as moe_forward; any T >= 1 (the call always
+ * takes the per-stage tcgen05 path, MOE_PATH_PREFILL_TC). */
+int moe_forward_w4a8(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                     const float* bias_dev, int bias_row_stride,
+                     float* logits_out, int32_t* idx_out, float* w_out,
+                     void* workspace_dev, size_t workspace_bytes, int* dev_status,
+                     moe_stream_t stream);
+
+/* Quantise activation rows to MXFP8, the operation moe_forward_w4a8 applies
+ * to x and to h: per row and 32-element block, s = clamp(floor(log2 amax) - 8
+ * + 127, 0, 254) (amax = 0 -> 0), elements RNE(v * 2^(127 - s)) to E4M3,
+ * saturating at 448 (OCP MX v1.0, §6.3, with E4M3's emax 8).
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §2
+ * (W4A8: 8-bit activations against 4-bit weights).
+ *   src_dev      bf16 (src_is_bf16 = 1) or fp32 (0) [rows][K] (device, 16-B aligned)
+ *   codes_dev    uint8 [rows][K] E4M3 codes (device, 16-B aligned)
+ *   scales_dev   uint8 [rows][K/32] E8M0 scale bytes (device)
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE (K % 32 != 0). */
+int moe_quant_mxfp8(const void* src_dev, int src_is_bf16, int rows, int K, uint8_t* codes_dev,
+                    uint8_t* scales_dev, moe_stream_t stream);
 
 /* Size in bytes of the scratch array inside the library that
  * moe_forward_static_scratch uses instead of a caller's workspace. */

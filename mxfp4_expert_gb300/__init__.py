@@ -19,7 +19,7 @@ __all__ = [
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
-    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_profiled", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_profiled", "moe_forward_w4a8", "moe_quant_mxfp8", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
 # The in-tree build, and only it: there is no way to point the binding at
@@ -80,6 +80,8 @@ def _load():
         "moe_workspace_bytes": (sz, [ctypes.POINTER(moe_shape), i32]),
         "moe_query_path": (i32, [ctypes.POINTER(moe_shape), i32]),
         "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]),
+        "moe_quant_mxfp8": (i32, [vp, i32, i32, i32, vp, vp, vp]),
+        "moe_forward_w4a8": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]),
         "moe_forward_profiled": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
                                          ctypes.POINTER(ctypes.c_void_p), i32, vp]),
         "moe_forward_static_scratch": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, vp]),
@@ -320,6 +322,30 @@ def moe_forward(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
     return _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, None, stream)
 
 
+def moe_forward_w4a8(layer: Layer, x: torch.Tensor, bias: torch.Tensor | None = None,
+                     y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
+                     w_out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                     stream=None):
+    """The layer with MXFP8 activations before each routed-expert GEMM (W4A8),
+    on the block-scaled tcgen05 path for any T; otherwise as moe_forward."""
+    return _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, None, stream,
+                    entry="moe_forward_w4a8")
+
+
+def moe_quant_mxfp8(src: torch.Tensor, stream=None):
+    """bf16 or fp32 [rows, K] -> (E4M3 codes uint8 [rows, K], E8M0 scales uint8 [rows, K/32])."""
+    if src.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("src must be bf16 or fp32")
+    _cuda(src, src.dtype, "src")
+    rows, K = src.shape
+    codes = torch.empty((rows, K), dtype=torch.uint8, device=src.device)
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=src.device)
+    _check(lib.moe_quant_mxfp8(_p(src), 1 if src.dtype == torch.bfloat16 else 0, rows, K, _p(codes), _p(scales),
+                               _s(stream)), "moe_quant_mxfp8")
+    return codes, scales
+
+
 def moe_forward_profiled(layer: Layer, x: torch.Tensor, stage_events, bias: torch.Tensor | None = None,
                          y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                          logits_out: torch.Tensor | None = None, idx_out: torch.Tensor | None = None,
@@ -331,7 +357,8 @@ def moe_forward_profiled(layer: Layer, x: torch.Tensor, stage_events, bias: torc
                     stream)
 
 
-def _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, stage_events, stream):
+def _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_status, stage_events, stream,
+             entry="moe_forward"):
     if y is None:
         _cuda(x, torch.bfloat16, "x")
         y = torch.empty_like(x)
@@ -342,7 +369,7 @@ def _forward(layer, x, bias, y, workspace, logits_out, idx_out, w_out, dev_statu
     args = (ctypes.byref(layer.struct), _p(x), T, _p(y), _p(bias), stride, _p(logits_out), _p(idx_out), _p(w_out),
             _p(workspace), workspace.numel(), _p(dev_status))
     if stage_events is None:
-        _check(lib.moe_forward(*args, _s(stream)), "moe_forward")
+        _check(getattr(lib, entry)(*args, _s(stream)), entry)
     else:
         n_ev = len(stage_events)
         ev_arr = (ctypes.c_void_p * n_ev)(*[e.cuda_event for e in stage_events])

@@ -37,10 +37,13 @@ int current_device(DeviceInfo* out) {
 
 namespace {
 
+// Tokens from which the routed experts run as tcgen05 grouped GEMMs.
+constexpr int kPrefillMinT = 32;
+
 // Workspace sections of one forward call (byte offsets from the base).
 struct Workspace {
   size_t state, logits, idx, w, sort_ws, counts, offsets, perm, inv, active, n_active, status;
-  size_t x_b, x_e, h_sh, h, h_b, h_e, part, total;
+  size_t x_b, x_e, h_sh, h, h_b, h_e, part, xq, xs, hq, hs, total;
 };
 
 Workspace plan(const moe_shape& sh, int T) {
@@ -53,7 +56,7 @@ Workspace plan(const moe_shape& sh, int T) {
     at += round_up(bytes, 256);
     return here;
   };
-  o.state = take(decode_state_bytes(int(E), int(I)));   // persists across calls
+  o.state = take(decode_state_bytes(T, int(E)));   // persists across calls
   o.logits = take(size_t(T) * E * 4);
   o.idx = take(slots * 4);
   o.w = take(slots * 4);
@@ -72,6 +75,11 @@ Workspace plan(const moe_shape& sh, int T) {
   o.h_b = take(slots * (I / 32) * kActRowKbBytes);
   o.h_e = take(slots * decode_he_stride(int(I)) * 2);
   o.part = take(slots * d * 4);
+  // activations of the tcgen05 path as E4M3 terms (up to 2) + E8M0 scales
+  o.xq = take(size_t(T) * 2 * d);
+  o.xs = take(size_t(T) * (d / 32));
+  o.hq = take(slots * 2 * I);
+  o.hs = take(slots * (I / 32));
   o.total = at;
   return o;
 }
@@ -108,9 +116,6 @@ extern "C" size_t moe_workspace_bytes(const moe_shape* shape, int T) {
   return plan(*shape, T).total;
 }
 
-// Tokens from which the routed experts run as tcgen05 grouped GEMMs.
-constexpr int kPrefillMinT = 32;
-
 // Path for (shape, T) on the current device: the single-launch decode kernel
 // when T <= 4 and the shape fits it; the per-stage kernels with tcgen05
 // routed GEMMs from kPrefillMinT tokens; else the per-stage kernels.
@@ -121,9 +126,8 @@ static int select_path(const moe_shape& sh, int T, const DeviceInfo& di) {
   probe.I = sh.d_ff;
   probe.E = sh.n_experts;
   probe.k = sh.top_k;
-  int stages;
-  uint32_t slot, smem;
-  if (T <= kDecodeMaxT && decode_plan(probe, di, &stages, &slot, &smem) == MOE_OK) return MOE_PATH_DECODE_FUSED;
+  uint32_t smem;
+  if (T <= kDecodeMaxT && decode_plan(probe, di, &smem) == MOE_OK) return MOE_PATH_DECODE_FUSED;
   if (T >= kPrefillMinT) return MOE_PATH_PREFILL_TC;
   return MOE_PATH_DECODE_MMA;
 }
@@ -171,7 +175,7 @@ int validate_forward(const moe_layer* L, const void* x_dev, int T, const void* y
 int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, const float* bias_dev,
                     int bias_row_stride, float* logits_out, int32_t* idx_out, float* w_out, void* workspace_dev,
                     int* dev_status, void* const* stage_events, int n_stage_events, moe_stream_t stream,
-                    const Workspace& ws, const DeviceInfo& di) {
+                    const Workspace& ws, const DeviceInfo& di, bool act_mxfp8 = false) {
   int st = MOE_OK;
   const moe_shape& sh = L->shape;
   const int d = sh.d_model, I = sh.d_ff, E = sh.n_experts, k = sh.top_k;
@@ -200,7 +204,8 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
   };
   if ((st = mark())) return st;
 
-  if (select_path(sh, T, di) == MOE_PATH_DECODE_FUSED) {
+  const int path = act_mxfp8 ? MOE_PATH_PREFILL_TC : select_path(sh, T, di);
+  if (path == MOE_PATH_DECODE_FUSED) {
     DecodeArgs da{};
     da.T = T;
     da.d = d;
@@ -224,14 +229,14 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
     da.w_out = w_out;
     da.y = static_cast<__nv_bfloat16*>(y_dev);
     da.state = at<DecodeState>(B, ws.state);
-    da.h = at<float>(B, ws.h);
+    da.h = at<uint8_t>(B, ws.h);   // decode_h_bytes(T, k, I) <= slots * I * 4
     da.h_sh = at<float>(B, ws.h_sh);
     da.status = status;
     if ((st = launch_decode(da, di, s))) return st;
     return mark();
   }
 
-  const bool tc = select_path(sh, T, di) == MOE_PATH_PREFILL_TC;
+  const bool tc = path == MOE_PATH_PREFILL_TC;
   // 1. activations -> e4m3 B-operand terms (the tcgen05 path reads x as bf16)
   if (!tc) {
     if ((st = launch_act_split(x, true, T, d, at<uint8_t>(B, ws.x_b), at<int16_t>(B, ws.x_e), di, s))) return st;
@@ -258,8 +263,14 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
   if ((st = mark())) return st;
   const int max_active = T * k < E ? T * k : E;
   if (tc) {
-    // routed gate/up (x rows as bf16) -> h as bf16 hi + lo terms; routed down
-    // (both terms as separate columns) -> part [slots][d]; both on tcgen05
+    // x -> E4M3 terms with E8M0 scales per 32 (MXFP8 for the 8-bit-activation
+    // call, else two terms of bf16 precision); routed gate/up on block-scaled
+    // tcgen05 MMAs -> h fp32 [slots][I]; h -> E4M3 terms; routed down -> part
+    // [slots][d]; shared down + combine
+    const int qmode = act_mxfp8 ? kQuantMxfp8 : kQuantSplit2;
+    const int nterms = act_mxfp8 ? 1 : 2;
+    if ((st = launch_act_quant(x, true, T, d, qmode, at<uint8_t>(B, ws.xq), at<uint8_t>(B, ws.xs), s))) return st;
+    if ((st = mark())) return st;
     RoutedArgs ua{};
     ua.w = static_cast<const uint8_t*>(L->gate_up);
     ua.mat_bytes = L->gate_up_desc.bytes_per_mat;
@@ -270,20 +281,25 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
     ua.offsets = offsets;
     ua.perm = perm;
     ua.k = k;
-    ua.act_raw = x;
-    ua.n_rows = T * k;
-    ua.out = at<float>(B, ws.h);   // written as bf16 hi [slots][I], then lo [slots][I]
+    ua.act_q = at<uint8_t>(B, ws.xq);
+    ua.act_s = at<uint8_t>(B, ws.xs);
+    ua.act_terms = nterms;
+    ua.out = at<float>(B, ws.h);
     ua.out_ld = I;
     ua.status = status;
     if ((st = launch_umma_routed(kModeGateUp, ua, di, s))) return st;
+    if ((st = mark())) return st;
+    if ((st = launch_act_quant(at<float>(B, ws.h), false, T * k, I, qmode, at<uint8_t>(B, ws.hq),
+                               at<uint8_t>(B, ws.hs), s)))
+      return st;
     if ((st = mark())) return st;
     RoutedArgs ud = ua;
     ud.w = static_cast<const uint8_t*>(L->down);
     ud.mat_bytes = L->down_desc.bytes_per_mat;
     ud.n_tiles = d / kTileRows;
     ud.KB = I / kMxBlock;
-    ud.act_raw = at<__nv_bfloat16>(B, ws.h);
-    ud.act_raw2 = at<__nv_bfloat16>(B, ws.h) + (size_t)T * k * I;
+    ud.act_q = at<uint8_t>(B, ws.hq);
+    ud.act_s = at<uint8_t>(B, ws.hs);
     ud.out = at<float>(B, ws.part);
     ud.out_ld = d;
     if ((st = launch_umma_routed(kModeDown, ud, di, s))) return st;
@@ -373,6 +389,18 @@ extern "C" int moe_forward_profiled(const moe_layer* L, const void* x_dev, int T
                          dev_status, stage_events, n_stage_events, stream, ws, di);
 }
 
+extern "C" int moe_forward_w4a8(const moe_layer* L, const void* x_dev, int T, void* y_dev,
+                                const float* bias_dev, int bias_row_stride, float* logits_out,
+                                int32_t* idx_out, float* w_out, void* workspace_dev,
+                                size_t workspace_bytes, int* dev_status, moe_stream_t stream) {
+  Workspace ws;
+  DeviceInfo di;
+  const int st = validate_forward(L, x_dev, T, y_dev, bias_row_stride, workspace_dev, workspace_bytes, &ws, &di);
+  if (st != MOE_OK) return st;
+  return enqueue_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, workspace_dev,
+                         dev_status, nullptr, 0, stream, ws, di, true);
+}
+
 namespace moe {
 namespace {
 // Scratch of moe_forward_static_scratch: part of this library's device image,
@@ -451,16 +479,30 @@ extern "C" int moe_forward_static_scratch(const moe_layer* L, const void* x_dev,
   // when the call's kernels start; clear them on the call's own stream so a
   // call never depends on how an earlier one ended.
   MOE_CUDA_TRY(cudaMemsetAsync(static_cast<char*>(scratch) + ws.state, 0,
-                               decode_state_bytes(L->shape.n_experts, L->shape.d_ff), (cudaStream_t)stream));
+                               decode_state_bytes(T, L->shape.n_experts), (cudaStream_t)stream));
   return enqueue_forward(L, x_dev, T, y_dev, bias_dev, bias_row_stride, logits_out, idx_out, w_out, scratch,
                          dev_status, nullptr, 0, stream, ws, di);
+}
+
+extern "C" int moe_quant_mxfp8(const void* src_dev, int src_is_bf16, int rows, int K, uint8_t* codes_dev,
+                               uint8_t* scales_dev, moe_stream_t stream) {
+  MOE_CHECK_ARG(src_dev && codes_dev && scales_dev && rows >= 0 && K > 0, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(src_is_bf16 == 0 || src_is_bf16 == 1, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(K % 32 == 0, MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK_ARG(aligned(src_dev, 16) && aligned(codes_dev, 16), MOE_ERR_INVALID_ARG);
+  DeviceInfo di;
+  const int st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return launch_act_quant(src_dev, src_is_bf16 != 0, rows, K, kQuantMxfp8, codes_dev, scales_dev,
+                          (cudaStream_t)stream);
 }
 
 extern "C" const char* moe_stage_names(int path) {
   if (path == MOE_PATH_DECODE_FUSED) return "decode_fused";
   if (path == MOE_PATH_DECODE_MMA)
     return "act_split_x,router_shared_gateup,topk,sort,routed_gateup,act_split_h,routed_down,combine";
-  if (path == MOE_PATH_PREFILL_TC) return "router_shared_gateup,topk,sort,routed_gateup,routed_down,combine";
+  if (path == MOE_PATH_PREFILL_TC)
+    return "router_shared_gateup,topk,sort,quant_x,routed_gateup,quant_h,routed_down,combine";
   return nullptr;
 }
 

@@ -10,17 +10,15 @@ namespace moe {
 
 constexpr int kDecodeMaxT = 4;        // tokens per call on this path
 constexpr int kDecodeMaxTiles = 4;    // 16-row output tiles per CTA
-constexpr int kDecodeMaxStages = 16;
-constexpr int kDecodeStateWords = 16; // header words before the per-block counters
+constexpr int kDecodeStateWords = 16; // synchronisation words at the head of the workspace
 
 // Synchronisation words at the start of the workspace (zero before the
 // first call; the last CTA of every call puts them back to zero).
 struct DecodeState {
-  unsigned long long bar;  // CTAs past their router rows
-  uint32_t done;           // CTAs finished (compared modulo the grid size; never reset)
-  uint32_t shcnt;          // CTAs whose shared gate/up slice is written
-  uint32_t gudone;         // CTAs whose routed gate/up items are written
-  uint32_t pad[11];
+  uint32_t routed;   // CTAs whose router logits and shared gate/up features are written
+  uint32_t done;     // CTAs finished (compared modulo the grid size; never reset)
+  uint32_t gudone;   // CTAs whose routed gate/up features are written
+  uint32_t pad[13];
 };
 static_assert(sizeof(DecodeState) == kDecodeStateWords * 4, "state header size");
 
@@ -41,19 +39,20 @@ struct DecodeArgs {
   float* w_out;         // [T][k] or null
   __nv_bfloat16* y;     // [T][d]
   DecodeState* state;
-  float* h;             // [T*k][I] routed SwiGLU outputs, exchanged between CTAs
+  uint8_t* h;           // routed SwiGLU outputs as e4m3 terms + group factors, exchanged between CTAs
   float* h_sh;          // [T][I]
   int* status;
-  int stages;           // set by launch_decode
-  uint32_t slot_bytes;  // set by launch_decode
 };
 
-size_t decode_state_bytes(int E, int I);
-// Row stride (elements) of the h exponent array: I/32 rounded up to 8.
+// Bytes of the cross-call state (the counters above).
+size_t decode_state_bytes(int T, int E);
+// Row stride (elements) of the per-stage path's h exponent array: I/32 rounded up to 8.
 uint32_t decode_he_stride(int I);
-// MOE_OK if the shape/T can take this path on this device.
-int decode_plan(const DecodeArgs& a, const DeviceInfo& di, int* stages, uint32_t* slot_bytes,
-                uint32_t* smem_bytes);
-int launch_decode(DecodeArgs a, const DeviceInfo& di, cudaStream_t s);
+// Bytes of the routed-h exchange area the single-launch kernel uses.
+size_t decode_h_bytes(int T, int k, int I);
+// MOE_OK if the shape/T can take this path on this device; *smem_bytes is the
+// dynamic shared memory of the launch.
+int decode_plan(const DecodeArgs& a, const DeviceInfo& di, uint32_t* smem_bytes);
+int launch_decode(const DecodeArgs& a, const DeviceInfo& di, cudaStream_t s);
 
 }  // namespace moe

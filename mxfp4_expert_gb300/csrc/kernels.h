@@ -24,6 +24,12 @@ int launch_sort(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_
 int launch_act_split(const void* src, bool src_bf16, int rows, int K, uint8_t* act_b,
                      int16_t* act_e, const DeviceInfo& di, cudaStream_t s);
 
+// quant.cu: activation rows (bf16 or fp32) [rows][K] -> E4M3 terms
+// q [rows][nterms][K] and E8M0 scales [rows][K/32] (see quant.cu).
+enum QuantMode { kQuantMxfp8 = 0, kQuantSplit2 = 1 };
+int launch_act_quant(const void* src, bool src_bf16, int rows, int K, int mode, uint8_t* q, uint8_t* scales,
+                     cudaStream_t s);
+
 enum RoutedMode { kModeGateUp = 0, kModeDown = 1 };
 
 struct RoutedArgs {
@@ -38,20 +44,21 @@ struct RoutedArgs {
   int k;
   const uint8_t* act_b;     // B-operand rows (e4m3 terms)
   const int16_t* act_e;
-  const void* act_raw;      // tensor-core path: x (bf16 [T][K]) for gate/up; h hi terms (bf16 [slots][K]) for down
-  const void* act_raw2;     // tensor-core path, down: h lo terms (bf16 [slots][K])
-  int n_rows;               // tensor-core path: slots (rows of h)
+  const uint8_t* act_q;     // tensor-core path: activation rows as E4M3 terms [rows][act_terms][K]
+                            // (gate/up: x rows by token; down: h rows by sorted slot)
+  const uint8_t* act_s;     // tensor-core path: their E8M0 scales [rows][K/32]
+  int act_terms;            // tensor-core path: 1 (MXFP8) or 2 (two-term split)
   int act_by_token;         // 1: activation row = perm[slot] / k; 0: = slot
   int max_items;            // upper bound on n_active * n_tiles (grid sizing)
   float* out;               // gate/up: h [slots][N/2]; down: part [slots][N]
-                            // (tensor-core gate/up: h as bf16 hi [slots][N/2] then lo [slots][N/2])
   int out_ld;
   int* status;
 };
 int launch_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
 
-// umma.cu: the same routed GEMMs on tcgen05 (bf16 operands decoded from
-// MXFP4 in shared memory, fp32 accumulator in tensor memory), for large T.
+// umma.cu: the same routed GEMMs on tcgen05 block-scaled MMAs (E4M3-coded
+// MXFP4 weights x E4M3 activation terms, E8M0 scales in tensor memory, fp32
+// accumulator in tensor memory), for large T.
 int launch_umma_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
 
 // dense.cu

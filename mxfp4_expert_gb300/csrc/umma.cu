@@ -1,32 +1,40 @@
-// Routed-expert GEMMs on the 5th-generation tensor cores (tcgen05), for large
-// token counts (prefill): gate/up with SwiGLU, and down.
+// Routed-expert GEMMs on the 5th-generation tensor cores (tcgen05) with
+// block-scaled MMAs, for large token counts (prefill): gate/up with SwiGLU,
+// and down.
+//
+// Every MMA is tcgen05.mma.kind::mxf8f6f4.block_scale: A = 128 weight rows x
+// K 32 as E4M3 codes, B = activation rows x K 32 as E4M3 codes, each with one
+// E8M0 scale per row and 32-wide K-block, read by the tensor core from tensor
+// memory; fp32 accumulation in tensor memory. The MXFP4 weights enter exactly:
+// an E2M1 code re-encoded as E4M3 is 2^-6 times its value (E2M1's subnormal
+// maps onto E4M3's), so the A scale byte is the block's E8M0 scale + 6. The
+// activations arrive pre-quantised (quant.cu): MXFP8 for the 8-bit-activation
+// call, or two E4M3 terms sharing one E8M0 scale (bf16 precision), which the
+// MMA reads as separate B rows and the epilogue adds.
 //
 // Work items are (active expert, block of 128 weight rows = 8 packed 16-row
-// tiles, block of that expert's rows / tokens), split into contiguous ranges
-// per CTA (one CTA per SM, persistent). Along K an item goes in slices of two
-// 32-wide K-blocks. The CTA is a pipeline of warp roles that meet only at
-// mbarriers (no block-wide barrier per slice):
+// tiles, block of up to 128 B rows of that expert's tokens / slots), split
+// into contiguous ranges per CTA (one CTA per SM, persistent). Along K an
+// item goes in slices of four 32-wide K-blocks (one 128-byte swizzle row of
+// E4M3). The CTA is a pipeline of warp roles that meet only at mbarriers:
 //   * producer (one thread): 1-D bulk copies of the packed MXFP4 bytes of a
-//     chunk of 4 slices (8 tiles x 8 units of 272 bytes; one copy per tile,
-//     since small copies are issued too slowly) into a ring of raw slots.
-//     The ring is too small to cover the HBM latency on its own, so whole
+//     chunk of 2 slices (one copy per tile) into a ring of raw slots; whole
 //     items are also prefetched into L2 about 8 chunks ahead;
-//   * 16 decode warps (two per tile): raw slot -> bf16 with the E8M0 block
-//     scale applied (exact, integer and bf16-multiply instructions only), in
-//     the K-major 128-byte-swizzled operand layout the MMA reads;
-//   * 4 loader warps: the slice of the activation rows (bf16 x gathered by
-//     token; for the down projection h as two bf16 terms, hi and lo, in
-//     separate columns) copied with cp.async into the same layout; a loader
-//     announces slice p once its copies have landed (it waits for them two
-//     slices later) and it has made them visible to the async proxy;
-//   * MMA (one thread): tcgen05.mma kind::f16, M = 128, N = the item's column
-//     count, K = 16, into one of two fp32 accumulators in tensor memory; each
-//     slice's MMAs are committed to the barrier that frees its operand stage,
-//     the item's last slice also to the accumulator's "full" barrier;
+//   * 16 decode warps (two per tile): raw slot -> E4M3 codes (two logic
+//     operations per 4 codes) in the K-major 128-byte-swizzled layout the MMA
+//     reads, and the A scale bytes in the layout tcgen05.cp copies;
+//   * 4 loader warps: the slice of the activation rows (x gathered by token,
+//     or h by slot; each term a block of B rows) copied with cp.async, and
+//     their B scale bytes; a loader announces slice p once its copies have
+//     landed (it waits for them two slices later) and it has made them
+//     visible to the async proxy;
+//   * MMA (one thread): tcgen05.cp of the slice's A and B scales into tensor
+//     memory, then one MMA per K-block (M = 128, N = the item's B rows) into
+//     one of two accumulators; each slice's work is committed to the barrier
+//     that frees its stage, the item's last slice also to the accumulator's;
 //   * 4 epilogue warps (one per 32-lane quarter of tensor memory): tcgen05.ld,
-//     then SwiGLU of the gate and up rows of a tile (8 lanes apart) written as
-//     bf16 hi and lo terms, or for the down pass the sum of the hi and lo
-//     columns; then the accumulator is released to the next item but one.
+//     the terms of a row added, then SwiGLU of the gate and up rows of a tile
+//     (8 lanes apart) to fp32 h, or for the down pass the fp32 outputs per slot.
 // Every wait is bounded; a timeout sets MOE_DEV_TIMEOUT and an abort flag that
 // ends the other roles' waits at once, and the kernel drains its own copies
 // and MMAs before it frees tensor memory and returns.
@@ -41,23 +49,26 @@ namespace moe {
 namespace {
 
 constexpr int kURows = 128;                  // weight rows per item (MMA M)
-constexpr int kUTiles = kURows / kTileRows;  // packed tiles per item (one per decode warp)
-constexpr int kUSliceKb = 2;                 // 32-wide K-blocks per slice
+constexpr int kUTiles = kURows / kTileRows;  // packed tiles per item (one per decode warp pair)
+constexpr int kUSliceKb = 4;                 // 32-wide K-blocks per slice: one 128-byte row of E4M3
 constexpr int kUSliceK = kUSliceKb * kMxBlock;
-constexpr int kUStages = 5;                  // operand stages (bf16 weights + activations)
-constexpr int kUChunk = 4;                   // slices per raw weight copy
+constexpr int kUStages = 4;                  // operand stages (weights + activations + scales)
+constexpr int kUChunk = 2;                   // slices per raw weight copy
 constexpr int kURing = 3;                    // raw weight chunks in flight
 constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about this many chunks ahead
 constexpr int kULag = 2;                     // activation slices a loader keeps in flight
 static_assert(kUStages > kULag, "a loader announces slice p - kULag only after it has claimed slice p's stage");
 constexpr int kUAcc = 2;                     // accumulators in tensor memory
-constexpr int kUCols = 128;                  // columns per accumulator = largest MMA N
+constexpr int kUCols = 128;                  // B rows per item = largest MMA N
+constexpr int kUSfCols = 8;                  // tensor-memory columns of one stage's scales (A: 4, B: 4)
+constexpr uint32_t kUTmemCols = 512;         // 2 x 128 accumulator + 4 x 8 scale columns, as a power of two
 constexpr int kUMaxActive = 1024;
 constexpr int kUTable = 256;                 // items per CTA with a precomputed table entry
 constexpr uint32_t kUTileChunk = kUChunk * kUSliceKb * kUnitBytes;   // one tile's part of a chunk
 constexpr uint32_t kURawBytes = kUTiles * kUTileChunk;                  // one chunk of packed weights
-constexpr uint32_t kUABytes = kURows * kUSliceK * 2;                 // one slice of bf16 weights
-constexpr uint32_t kUBBytes = kUCols * kUSliceK * 2;                 // one slice of bf16 activations
+constexpr uint32_t kUABytes = kURows * kUSliceK;                     // one slice of E4M3 weights
+constexpr uint32_t kUBBytes = kUCols * kUSliceK;                     // one slice of E4M3 activations
+constexpr uint32_t kUSfBytes = 512;                                  // scales of 128 rows x 4 K-blocks
 
 // warp roles
 constexpr int kWProducer = 0, kWMma = 1, kWEpi = 2, kNEpi = 4, kWLoad = kWEpi + kNEpi, kNLoad = 4,
@@ -66,7 +77,7 @@ constexpr int kUBlock = (kWDec + kNDec) * 32;
 constexpr int kScanThreads = 256;
 
 struct UmmaSmem {
-  uint32_t ring, a, b, iofs, itab, bars, misc, total;
+  uint32_t ring, a, b, sfa, sfb, iofs, itab, bars, misc, total;
 };
 __host__ __device__ inline UmmaSmem umma_smem() {
   UmmaSmem m{};
@@ -80,6 +91,8 @@ __host__ __device__ inline UmmaSmem umma_smem() {
   m.ring = take(kURing * kURawBytes, 128);
   m.a = take(kUStages * kUABytes, 1024);
   m.b = take(kUStages * kUBBytes, 1024);
+  m.sfa = take(kUStages * kUSfBytes, 128);
+  m.sfb = take(kUStages * kUSfBytes, 128);
   m.iofs = take((kUMaxActive + 1) * 4, 16);
   m.itab = take(kUTable * 16, 16);
   m.bars = take((2 * kURing + 3 * kUStages + 2 * kUAcc) * 8, 8);
@@ -88,42 +101,17 @@ __host__ __device__ inline UmmaSmem umma_smem() {
   return m;
 }
 
-// byte offset of element (row r, k < 64) in a K-major operand with 128-byte
-// swizzle: row r in atom r / 8 (1024 bytes each), line r % 8 (128 bytes), its
-// 16-byte chunk k / 8 stored at chunk (k / 8) ^ (r % 8)
-__device__ __forceinline__ uint32_t sw128_off(int r, int k) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((k >> 3) ^ (r & 7)) << 4) + (k & 7) * 2);
+// byte offset of the byte element (row r, k < 128) in a K-major operand with
+// 128-byte swizzle: row r in atom r / 8 (1024 bytes each), line r % 8 (128
+// bytes), its 16-byte chunk k / 16 stored at chunk (k / 16) ^ (r % 8)
+__device__ __forceinline__ uint32_t sw128_off8(int r, int k) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((k >> 4) ^ (r & 7)) << 4) + (k & 15));
 }
-
-// E2M1 -> bf16 without conversion instructions. Input: four codes in the
-// byte form of decode_rowlo (sign in bit 7, the 3 magnitude bits e1 e0 m in
-// bits 4..2 of each byte). The magnitude bits are moved to bf16 bits 8..6
-// and the sign to bit 15: that bf16 number is the E2M1 value times 2^-126
-// (the E2M1 subnormal 0.5 lands on the bf16 subnormal 2^-127). One exact bf16
-// multiply by 2^(s-1) then gives value * 2^(s-127); block scales s > 128
-// (2^(s-1) not a bf16) take a second multiply.
-__device__ __forceinline__ uint32_t e2m1_pair_raw(uint32_t b, uint32_t sel) {
-  const uint32_t p = __byte_perm(b, 0u, sel);   // two code bytes into the high bytes of the halves
-  return (p & 0x80008000u) | ((p >> 4) & 0x01C001C0u);
-}
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  const __nv_bfloat162 r =
-      __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-// the two factors of block scale s (E8M0), as bf16 pairs: 2^(min(s,128)-1)
-// and 2^(s-min(s,128))
-__device__ __forceinline__ uint32_t scale_f1(uint32_t s) { return ((min(s, 128u) + 126u) << 7) * 0x10001u; }
-__device__ __forceinline__ uint32_t scale_f2(uint32_t s) { return ((s - min(s, 128u) + 127u) << 7) * 0x10001u; }
-__device__ __forceinline__ uint2 e2m1x4_to_bf16x4(uint32_t b, uint32_t f1, uint32_t f2, bool big) {
-  uint32_t lo = bf16x2_mul(e2m1_pair_raw(b, 0x1404u), f1);   // codes 0, 1
-  uint32_t hi = bf16x2_mul(e2m1_pair_raw(b, 0x3424u), f1);   // codes 2, 3
-  if (big) {
-    lo = bf16x2_mul(lo, f2);
-    hi = bf16x2_mul(hi, f2);
-  }
-  return make_uint2(lo, hi);
-}
+// byte offset of the scale of row r (< 128) and K-block kb (< 4) of a slice in
+// the 512-byte block that tcgen05.cp .32x128b.warpx4 copies: 32 lines of 16
+// bytes, line r % 32 holding rows r % 32 + 32 j (j = 0..3) at bytes 4 j + kb.
+// The tensor core reads the scale of row r from column r / 32, byte kb.
+__device__ __forceinline__ uint32_t sf_off(int r, int kb) { return (uint32_t)((r & 31) * 16 + (r >> 5) * 4 + kb); }
 
 // 16-byte asynchronous global -> shared copy; zero-filled when !valid
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -172,6 +160,8 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   uint8_t* ring = smem + L.ring;
   uint8_t* abuf = smem + L.a;
   uint8_t* bbuf = smem + L.b;
+  uint8_t* sfabuf = smem + L.sfa;
+  uint8_t* sfbbuf = smem + L.sfb;
   int* iofs = reinterpret_cast<int*>(smem + L.iofs);
   uint64_t* full_raw = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty_raw = full_raw + kURing;
@@ -186,8 +176,9 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int D = *a.n_active, KB = a.KB, K = KB * kMxBlock;
   const int nrb = (a.n_tiles + kUTiles - 1) / kUTiles;
-  // tokens per item: gate/up columns are tokens; down columns are hi and lo terms of h
-  constexpr int kNTok = MODE == kModeGateUp ? kUCols : kUCols / 2;
+  // B rows per item: every term of a token (gate/up) or slot (down) is a B row
+  const int nterms = a.act_terms;
+  const int kNTok = kUCols / nterms;
   const int ns = (KB + kUSliceKb - 1) / kUSliceKb;   // slices per item
 
   // iofs[i] = items of the active experts before i (nrb per block of kNTok rows)
@@ -246,9 +237,14 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     }
     return l;
   };
-  // my item j: expert, row block, first row (sorted slot), rows, MMA N
+  // my item j: expert, row block, first row (sorted slot), rows, MMA N, and
+  // the B rows of one term (term t occupies B rows [t n16, t n16 + ntok))
   struct Item {
     int e, rb, pos0, ntok, nmma, n16;
+  };
+  auto geometry = [&](Item& f) {
+    f.n16 = nterms == 2 ? (f.ntok + 7) & ~7 : (f.ntok + 15) & ~15;
+    f.nmma = nterms * f.n16;
   };
   auto item_slow = [&](int j) {
     Item f;
@@ -259,13 +255,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     f.rb = rem - tb * nrb;
     f.pos0 = a.offsets[f.e] + tb * kNTok;
     f.ntok = min(kNTok, n_e - tb * kNTok);
-    if (MODE == kModeGateUp) {
-      f.n16 = 0;
-      f.nmma = (f.ntok + 15) & ~15;
-    } else {
-      f.n16 = (f.ntok + 7) & ~7;   // hi columns [0, n16), lo columns [n16, 2 n16)
-      f.nmma = 2 * f.n16;
-    }
+    geometry(f);
     return f;
   };
   // the first kUTable items of the CTA, looked up once (in parallel) in the prologue
@@ -278,13 +268,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     f.rb = v.y;
     f.pos0 = v.z;
     f.ntok = v.w;
-    if (MODE == kModeGateUp) {
-      f.n16 = 0;
-      f.nmma = (f.ntok + 15) & ~15;
-    } else {
-      f.n16 = (f.ntok + 7) & ~7;
-      f.nmma = 2 * f.n16;
-    }
+    geometry(f);
     return f;
   };
   for (int j = tid; j < n_mine && j < kUTable; j += blockDim.x) {
@@ -309,7 +293,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     *abort = 0;
     mbar_fence_init();
   }
-  if (warp == kWProducer) tmem_alloc(tslot, kUAcc * kUCols);
+  if (warp == kWProducer) tmem_alloc(tslot, kUTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -363,7 +347,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         if (j >= kUAcc && !uwait(&acc_empty[ab], uint32_t(j / kUAcc - 1) & 1u, abort, a.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(ab * kUCols);
-        const uint32_t idesc = umma_idesc_bf16(kURows, f.nmma);
         for (int sl = 0; sl < ns; ++sl) {
           const int p = j * ns + sl, st = p % kUStages;
           const uint32_t par = uint32_t(p / kUStages) & 1u;
@@ -375,8 +358,13 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
           const uint32_t as = smem_addr(abuf + (size_t)st * kUABytes);
           const uint32_t bs = smem_addr(bbuf + (size_t)st * kUBBytes);
-          for (int kk = 0; kk < nkb * 2; ++kk)   // K = 16 steps: 32 bytes into the swizzle atoms
-            umma_bf16(d, umma_desc_sw128(as + 32 * kk), umma_desc_sw128(bs + 32 * kk), idesc, sl > 0 || kk > 0);
+          // this slice's scales into tensor memory (in issue order before its MMAs)
+          const uint32_t sfa = tmem + uint32_t(kUAcc * kUCols + st * kUSfCols), sfb = sfa + 4;
+          tmem_cp_sf(sfa, umma_desc_sf(smem_addr(sfabuf + (size_t)st * kUSfBytes)));
+          tmem_cp_sf(sfb, umma_desc_sf(smem_addr(sfbbuf + (size_t)st * kUSfBytes)));
+          for (int kb = 0; kb < nkb; ++kb)   // K = 32 steps: 32 bytes into the swizzle rows
+            umma_mx(d, umma_desc_sw128(as + 32 * kb), umma_desc_sw128(bs + 32 * kb),
+                    umma_idesc_mx_e4m3(kURows, f.nmma, kb, kb), sfa, sfb, sl > 0 || kb > 0);
           umma_commit(&op_empty[st]);
           last = &op_empty[st];
           last_par = par;
@@ -398,26 +386,19 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       const uint32_t trow = tmem + uint32_t(ab * kUCols) + ((uint32_t)(quarter * 32) << 16);
       if (MODE == kModeGateUp) {
         // rows 16t .. 16t+7: gate of features 8 (rb*8 + t) + 0..7; rows +8: up.
-        // h goes out as bf16 terms: hi = bf16(h), lo = bf16(h - hi)
-        __nv_bfloat16* hhi = reinterpret_cast<__nv_bfloat16*>(a.out);
-        __nv_bfloat16* hlo = hhi + (size_t)a.n_rows * a.out_ld;
+        // h goes out as fp32 [slot][I] (row = sorted slot)
         const int t = row >> 4, r16 = row & 15, tile = f.rb * kUTiles + t;
         const int fe = tile * 8 + (r16 & 7);
         const bool st_ok = r16 < 8 && tile < a.n_tiles;
-        for (int c0 = 0; c0 < f.nmma; c0 += 8) {
-          uint32_t v[8];
+        for (int c0 = 0; c0 < f.n16; c0 += 8) {
+          uint32_t v[8], v2[8];
           tmem_ld8(trow + c0, v);
+          if (nterms == 2) tmem_ld8(trow + f.n16 + c0, v2);
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const float gv = __uint_as_float(v[jj]);
+            const float gv = __uint_as_float(v[jj]) + (nterms == 2 ? __uint_as_float(v2[jj]) : 0.0f);
             const float uv = __shfl_down_sync(0xFFFFFFFFu, gv, 8);
-            if (st_ok && c0 + jj < f.ntok) {
-              const float h = silu_f(gv) * uv;
-              const __nv_bfloat16 hb = __float2bfloat16_rn(h);
-              const size_t o = (size_t)(f.pos0 + c0 + jj) * a.out_ld + fe;
-              hhi[o] = hb;
-              hlo[o] = __float2bfloat16_rn(h - __bfloat162float(hb));
-            }
+            if (st_ok && c0 + jj < f.ntok) a.out[(size_t)(f.pos0 + c0 + jj) * a.out_ld + fe] = silu_f(gv) * uv;
           }
         }
       } else {
@@ -426,11 +407,12 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         for (int c0 = 0; c0 < f.n16; c0 += 8) {
           uint32_t vh[8], vl[8];
           tmem_ld8(trow + c0, vh);
-          tmem_ld8(trow + f.n16 + c0, vl);
+          if (nterms == 2) tmem_ld8(trow + f.n16 + c0, vl);
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj)
             if (st_ok && c0 + jj < f.ntok)
-              a.out[(size_t)(f.pos0 + c0 + jj) * a.out_ld + r] = __uint_as_float(vh[jj]) + __uint_as_float(vl[jj]);
+              a.out[(size_t)(f.pos0 + c0 + jj) * a.out_ld + r] =
+                  __uint_as_float(vh[jj]) + (nterms == 2 ? __uint_as_float(vl[jj]) : 0.0f);
         }
       }
       tc_fence_before();
@@ -438,51 +420,60 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   } else if (warp < kWDec) {
-    // ---- activation rows -> operand stage (cp.async) --------------------------------
-    // Thread lt copies 16-byte column c = lt % 8 of rows lt / 8 + 16 m. Gate/up:
-    // the rows are tokens (x rows gathered through perm). Down: the rows are
-    // sorted slots, hi terms to B rows r and lo terms to B rows n16 + r.
+    // ---- activation rows -> operand stage (cp.async), and their scales -------------
+    // B row r of an item is term r / n16 of its activation row r % n16 (gate/up:
+    // the token of sorted slot pos0 + r % n16; down: the slot itself). Thread lt
+    // copies 16-byte chunk c = lt % 8 of B rows lt / 8 + 16 m, and writes the
+    // scale bytes of B row lt.
     const int lt = tid - kWLoad * 32, c = lt & 7, rr = lt >> 3;
-    constexpr int kRows = MODE == kModeGateUp ? kUCols / 16 : kUCols / 32;   // rows per thread
-    const __nv_bfloat16* src0 = static_cast<const __nv_bfloat16*>(a.act_raw);
-    const __nv_bfloat16* src1 = static_cast<const __nv_bfloat16*>(a.act_raw2);
-    int b_row[kRows], nb_row[kRows];   // source rows of this item and of the next one
-    int pend = 0;                       // first slice not yet announced
+    constexpr int kRows = kUCols / 16;   // B rows per thread
+    int b_src[kRows], nb_src[kRows];     // (activation row * nterms + term), or -1 for padding
+    int s_src = -1, ns_src = -1;         // activation row of B row lt, or -1
+    int pend = 0;                        // first slice not yet announced
     Item f{};
     // rows of item j (requested one item ahead, so the loads are in flight meanwhile)
-    auto rows_of = [&](int j, int (&rows)[kRows]) {
+    auto rows_of = [&](int j, int (&src)[kRows], int& ssrc) {
       const Item h = item_of(j);
+      auto act_row = [&](int r) -> int {
+        if (r >= h.nmma) return -1;
+        const int tt = r / h.n16, jj = r - tt * h.n16;
+        if (jj >= h.ntok) return -1;
+        const int ar = MODE == kModeGateUp ? a.perm[h.pos0 + jj] / a.k : h.pos0 + jj;
+        return ar * nterms + tt;
+      };
 #pragma unroll
-      for (int m = 0; m < kRows; ++m) {
-        const int r = rr + 16 * m;
-        rows[m] = r < h.ntok ? (MODE == kModeGateUp ? a.perm[h.pos0 + r] / a.k : h.pos0 + r) : 0;
-      }
+      for (int m = 0; m < kRows; ++m) src[m] = act_row(rr + 16 * m);
+      const int v = act_row(lt);
+      ssrc = v < 0 ? -1 : v / nterms;
     };
-    if (n_mine > 0) rows_of(0, nb_row);
+    if (n_mine > 0) rows_of(0, nb_src, ns_src);
     for (int p = 0; p < n_stream; ++p) {
       const int j = p / ns, sl = p - j * ns, st = p % kUStages;
       if (p >= kUStages && !uwait(&op_empty[st], uint32_t(p / kUStages - 1) & 1u, abort, a.status)) break;
       if (sl == 0) {
         f = item_of(j);
 #pragma unroll
-        for (int m = 0; m < kRows; ++m) b_row[m] = nb_row[m];
-        if (j + 1 < n_mine) rows_of(j + 1, nb_row);
+        for (int m = 0; m < kRows; ++m) b_src[m] = nb_src[m];
+        s_src = ns_src;
+        if (j + 1 < n_mine) rows_of(j + 1, nb_src, ns_src);
       }
-      const int kb0 = sl * kUSliceKb, nc = min(kUSliceKb, KB - kb0) * (kMxBlock / 8);
+      const int kb0 = sl * kUSliceKb, nkb = min(kUSliceKb, KB - kb0), nc = nkb * (kMxBlock / 16);
       uint8_t* bb = bbuf + (size_t)st * kUBBytes;
-      const int nrow = MODE == kModeGateUp ? f.nmma : f.n16;
       if (c < nc) {
 #pragma unroll
         for (int m = 0; m < kRows; ++m) {
           const int r = rr + 16 * m;
-          if (r < nrow) {
-            const bool valid = r < f.ntok;
-            const size_t o = (size_t)b_row[m] * K + kb0 * kMxBlock + c * 8;
-            cp_async16(bb + sw128_off(r, c * 8), src0 + o, valid);
-            if (MODE == kModeDown) cp_async16(bb + sw128_off(f.n16 + r, c * 8), src1 + o, valid);
+          if (r < f.nmma) {
+            const bool valid = b_src[m] >= 0;
+            const size_t o = (size_t)(valid ? b_src[m] : 0) * K + kb0 * kMxBlock + c * 16;
+            cp_async16(bb + sw128_off8(r, c * 16), a.act_q + o, valid);
           }
         }
       }
+      uint8_t* sb = sfbbuf + (size_t)st * kUSfBytes;
+#pragma unroll
+      for (int i = 0; i < kUSliceKb; ++i)
+        sb[sf_off(lt, i)] = (s_src >= 0 && i < nkb) ? a.act_s[(size_t)s_src * KB + kb0 + i] : uint8_t(127);
       cp_async_commit();
       // announce slice p - kULag once its copies (not the later ones) have landed
       if (p - pend >= kULag) {
@@ -501,8 +492,8 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
     }
   } else {
-    // ---- raw ring -> bf16 weights (decode warp dw: tile dw % 8 of the item, the
-    // slice's 32-wide K-blocks u = dw / 8, dw / 8 + 2, ...) ----------------------------
+    // ---- raw ring -> E4M3 weights and A scales (decode warp dw: tile dw % 8 of
+    // the item, the slice's 32-wide K-blocks u = dw / 8, dw / 8 + 2) ---------------
     const int dw = warp - kWDec, t = dw % kUTiles;
     const int g = lane >> 2, q = lane & 3;
     int tile = 0;
@@ -517,27 +508,31 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
       const uint8_t* raw = ring + (size_t)s * kURawBytes + (size_t)t * kUTileChunk + (size_t)sub * kUSliceKb * kUnitBytes;
       uint8_t* ab = abuf + (size_t)st * kUABytes;
+      uint8_t* sa = sfabuf + (size_t)st * kUSfBytes;
 #pragma unroll
       for (int u = dw / kUTiles; u < kUSliceKb; u += kDecPerTile) {
         const int r0 = t * kTileRows + g, r1 = r0 + 8;
-        uint2 c0 = make_uint2(0u, 0u), c1 = c0, c2 = c0, c3 = c0;
+        uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 0u, slo = 0u, shi = 0u;
         if (u < nkb && tile < a.n_tiles) {
           const uint8_t* unit = raw + (size_t)u * kUnitBytes;
           const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
           const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          const uint32_t slo = sc16 & 0xFFu, shi = sc16 >> 8;   // block scales of rows g and g+8
-          const bool big = __any_sync(0xFFFFFFFFu, (slo | shi) > 128u);
-          const uint32_t f1lo = scale_f1(slo), f2lo = scale_f2(slo), f1hi = scale_f1(shi), f2hi = scale_f2(shi);
-          c0 = e2m1x4_to_bf16x4(decode_rowlo(wv.x), f1lo, f2lo, big);   // row g,   k 4q .. 4q+3
-          c1 = e2m1x4_to_bf16x4(decode_rowhi(wv.x), f1hi, f2hi, big);   // row g+8
-          c2 = e2m1x4_to_bf16x4(decode_rowlo(wv.y), f1lo, f2lo, big);   // row g,   k 16+4q ..
-          c3 = e2m1x4_to_bf16x4(decode_rowhi(wv.y), f1hi, f2hi, big);   // row g+8
+          c0 = decode_rowlo(wv.x);   // row g,   k 4q .. 4q+3: E4M3 = 2^-6 x the E2M1 value
+          c1 = decode_rowhi(wv.x);   // row g+8
+          c2 = decode_rowlo(wv.y);   // row g,   k 16+4q ..
+          c3 = decode_rowhi(wv.y);   // row g+8
+          slo = min((sc16 & 0xFFu) + 6u, 255u);   // A scale: 2^(s-127) x 2^6
+          shi = min((sc16 >> 8) + 6u, 255u);
         }
         const int k0 = u * kMxBlock + 4 * q;
-        *reinterpret_cast<uint2*>(ab + sw128_off(r0, k0)) = c0;
-        *reinterpret_cast<uint2*>(ab + sw128_off(r1, k0)) = c1;
-        *reinterpret_cast<uint2*>(ab + sw128_off(r0, k0 + 16)) = c2;
-        *reinterpret_cast<uint2*>(ab + sw128_off(r1, k0 + 16)) = c3;
+        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r0, k0)) = c0;
+        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r1, k0)) = c1;
+        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r0, k0 + 16)) = c2;
+        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r1, k0 + 16)) = c3;
+        if (q == 0) {
+          sa[sf_off(r0, u)] = uint8_t(slo);
+          sa[sf_off(r1, u)] = uint8_t(shi);
+        }
       }
       fence_async_smem();
       __syncwarp();
@@ -553,7 +548,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   if (warp == kWProducer) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kUAcc * kUCols);
+    tmem_dealloc(tmem, kUTmemCols);
   }
 }
 

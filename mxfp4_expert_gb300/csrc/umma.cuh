@@ -1,7 +1,8 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05): tensor
-// memory (TMEM) allocation, the shared-memory matrix descriptor, the
-// instruction descriptor of a bf16 x bf16 -> fp32 MMA, the MMA itself, its
-// completion signal, and TMEM -> register loads.
+// memory (TMEM) allocation, shared-memory matrix descriptors, the instruction
+// descriptor of a block-scaled E4M3 x E4M3 -> fp32 MMA, the MMA itself, the
+// copy of scale factors into TMEM, the completion signal, and TMEM -> register
+// loads.
 #pragma once
 
 #include "common.cuh"
@@ -49,20 +50,40 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                   // layout: 128-byte swizzle
   return d;
 }
-// Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Shared-memory descriptor of a 512-byte scale block for tcgen05.cp: 32 lines
+// of 16 bytes, no swizzle (8-line core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t umma_desc_sf(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Instruction descriptor of a block-scaled MMA (kind::mxf8f6f4): fp32
+// accumulator, E4M3 A and B (format 0), both K-major, E8M0 scales (bit 23),
+// M x N, and which byte of the 32-bit scale words the A and B scales of this
+// K-block are (sf_a at bits 29-30, sf_b at bits 4-5).
+__host__ __device__ constexpr uint32_t umma_idesc_mx_e4m3(int M, int N, int sf_a, int sf_b) {
+  return ((uint32_t)(sf_b & 3) << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         ((uint32_t)(sf_a & 3) << 29);
 }
 
 // ---- MMA ----------------------------------------------------------------------
-// One thread: D[tmem] (+)= A * B^T for one K=16 step (kind::f16, cta_group::1).
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          bool accumulate) {
+// One thread: D[tmem] (+)= (A x scale_A) * (B x scale_B)^T for one K = 32 step
+// (kind::mxf8f6f4, block_scale, one scale per 32 elements, cta_group::1).
+__device__ __forceinline__ void umma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t tmem_sfa, uint32_t tmem_sfb, bool accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(tmem_sfa), "r"(tmem_sfb), "r"(accumulate ? 1u : 0u)
       : "memory");
+}
+// One thread: copy a 512-byte scale block (32 lines x 16 bytes) from shared
+// memory to 4 tensor-memory columns, the same in each of the 4 lane quarters.
+__device__ __forceinline__ void tmem_cp_sf(uint32_t tmem_col, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem_col), "l"(sdesc) : "memory");
 }
 // One thread: arrive on *bar once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

@@ -40,7 +40,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import mxfp4
+from . import mxfp4, mxfp8
 
 
 def as_f64(t) -> np.ndarray:
@@ -131,7 +131,7 @@ class Expert:
         return cls(gu[:I], gu[I:], dn)
 
 
-def expert_outputs(x_rows, gate_up_f32, down_f32) -> np.ndarray:
+def expert_outputs(x_rows, gate_up_f32, down_f32, act_mxfp8: bool = False) -> np.ndarray:
     """One routed expert applied to some token rows, in fp64.
 
     The expert's fp32 weights (gate_up [2I, d], down [d, I]) are quantised
@@ -139,9 +139,20 @@ def expert_outputs(x_rows, gate_up_f32, down_f32) -> np.ndarray:
     for every row of x_rows [n, d]. This is step 4 of the layer on its own,
     so that callers can evaluate many experts in separate processes and hand
     the results to moe_layer(expert_out=...).
+
+    act_mxfp8: the 8-bit-activation (W4A8) mode — x is replaced by its MXFP8
+    value (mxfp8.fake_quantize, per 32 along d) before the gate/up products,
+    and h by its MXFP8 value (per 32 along I) before the down product; every
+    product and sum is still exact fp64. Page "3 ways to speed up MoE
+    inference on NVIDIA DGX Spark", §2 (the W4A8 baseline configuration).
     """
     e = Expert.from_fp32(gate_up_f32, down_f32)
-    return swiglu_ffn(as_f64(x_rows), e.gate, e.up, e.down)
+    x = as_f64(x_rows)
+    if not act_mxfp8:
+        return swiglu_ffn(x, e.gate, e.up, e.down)
+    xq = mxfp8.fake_quantize(x)
+    h = silu(xq @ e.gate.T) * (xq @ e.up.T)
+    return mxfp8.fake_quantize(h) @ e.down.T
 
 
 def moe_layer(x, router_w, experts, shared, k: int, bias=None, idx=None, logits_f32=None,

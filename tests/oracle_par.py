@@ -34,11 +34,12 @@ def _pool():
     return _POOL
 
 
-def reference_layer(w, set_idx, x_rows, router, shared, bias_rows, idx, device="cuda"):
+def reference_layer(w, set_idx, x_rows, router, shared, bias_rows, idx, device="cuda", act_mxfp8=False):
     """oracle.moe.moe_layer for the given token rows at the given (already
     checked) routing, with the experts evaluated in parallel processes.
 
-    x_rows [n, d] (torch bf16 on the CPU), idx [n, k] int; returns moe_layer's dict.
+    x_rows [n, d] (torch bf16 on the CPU), idx [n, k] int; act_mxfp8: the
+    oracle's 8-bit-activation mode for the routed experts. Returns moe_layer's dict.
     """
     idx = np.asarray(idx)
     n, k = idx.shape
@@ -52,7 +53,7 @@ def reference_layer(w, set_idx, x_rows, router, shared, bias_rows, idx, device="
     for e in experts:
         gu, dn = wl.gen_expert(w, set_idx, e, device)
         rows = xs[[t for t, _ in pairs_of[e]]]
-        jobs.append((rows, gu.cpu().numpy(), dn.cpu().numpy()))
+        jobs.append((rows, gu.cpu().numpy(), dn.cpu().numpy(), act_mxfp8))
     if len(jobs) > 4:
         results = _pool().starmap(omoe.expert_outputs, jobs, chunksize=1)
     else:

@@ -260,7 +260,7 @@ def test_paths(mx):
     assert mx.moe_query_path(s, 4096) == mx.MOE_PATH_PREFILL_TC
     assert mx.moe_stage_names(mx.MOE_PATH_DECODE_FUSED) == ["decode_fused"]
     assert len(mx.moe_stage_names(mx.MOE_PATH_DECODE_MMA)) == 8
-    assert len(mx.moe_stage_names(mx.MOE_PATH_PREFILL_TC)) == 6
+    assert len(mx.moe_stage_names(mx.MOE_PATH_PREFILL_TC)) == 8
 
 
 def test_fused_workspace_reuse_matches_fresh(mx):

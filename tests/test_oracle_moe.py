@@ -124,6 +124,45 @@ def test_expert_outputs_path_matches_triple_loop():
     assert _rel(wrong, ref) > 1e-3
 
 
+def _loops_w4a8(x, gu, dn, quant):
+    """Pure-Python loops for one expert in the MXFP8-activation mode; the only
+    library calls are the pinned quantisers (mxfp4 for the weights, `quant`
+    for the activations)."""
+    G, U, Dn = (mxfp4.fake_quantize(m) for m in (gu[: len(gu) // 2], gu[len(gu) // 2:], dn))
+    xq = quant(x)
+    out = []
+    for t in range(len(x)):
+        h = []
+        for i in range(len(G)):
+            g = sum(float(G[i][j]) * float(xq[t][j]) for j in range(len(x[0])))
+            u = sum(float(U[i][j]) * float(xq[t][j]) for j in range(len(x[0])))
+            h.append(g / (1.0 + math.exp(-g)) * u)
+        hq = quant(np.array([h]))[0]
+        out.append([sum(float(Dn[r][i]) * float(hq[i]) for i in range(len(h))) for r in range(len(Dn))])
+    return np.array(out)
+
+
+def test_expert_outputs_w4a8_matches_loops():
+    """The MXFP8-activation mode quantises x before gate/up and h before down,
+    nothing else; planted variants (only x, only h, neither) are caught."""
+    from oracle import mxfp8
+    rng = np.random.default_rng(8)
+    T, d, I = 3, 64, 32
+    x = rng.standard_normal((T, d))
+    gu = (rng.standard_normal((2 * I, d)) * 0.05).astype(np.float32)
+    dn = (rng.standard_normal((d, I)) * 0.05).astype(np.float32)
+    got = moe.expert_outputs(x, gu, dn, act_mxfp8=True)
+    ref = _loops_w4a8(x, gu, dn, mxfp8.fake_quantize)
+    assert np.allclose(got, ref, rtol=1e-11, atol=1e-12)
+    ident = lambda a: np.asarray(a, dtype=np.float64)   # noqa: E731
+    plain = moe.expert_outputs(x, gu, dn)
+    assert np.allclose(plain, _loops_w4a8(x, gu, dn, ident), rtol=1e-11, atol=1e-12)
+    only_x = _loops_w4a8(x, gu, dn, lambda a: mxfp8.fake_quantize(a) if np.shape(a)[1] == d else ident(a))
+    only_h = _loops_w4a8(x, gu, dn, lambda a: mxfp8.fake_quantize(a) if np.shape(a)[1] == I else ident(a))
+    for bad in (plain, only_x, only_h):
+        assert _rel(bad, got) > 1e-3
+
+
 # planted mistakes: each plausible bug must change the result beyond tolerance ----
 
 def _rel(a, b):
