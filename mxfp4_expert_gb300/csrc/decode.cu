@@ -145,7 +145,7 @@ __device__ __forceinline__ void load_batch(UnitBatch& b, const uint8_t* base, in
 // terms of every slot (phase 5); region cg holds the gate/up partials.
 struct Smem {
   uint32_t ov, xs, xb, xfa, hbs, hfa, gpart, rpart, hsh, dpart, yacc, sel_e, sel_w, act, act_n, act_slot, act_tok,
-      first, gtab, dtab, misc, total;
+      first, gtab, dtab, misc, dnbar, dnw, dnw_bytes, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -188,8 +188,21 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int
   s.gtab = take(kMaxGuItems * 8, 8);
   s.dtab = take(kMaxDnItems * 8, 8);
   s.misc = take(16 * 4, 8);
+  s.dnbar = take(8, 8);
+  s.dnw = align_up(at, 128);
+  s.dnw_bytes = 0;   // set on the host when the down units fit (stage_down_units)
   s.total = at;
   return s;
+}
+// Room for the down units of up to 16 (output tile, expert) pairs of a CTA in
+// shared memory, if the device has it: then they are bulk-copied there during
+// the gate/up phase.
+inline void stage_down_units(Smem& s, int I, size_t smem_optin) {
+  const uint32_t bytes = 16u * uint32_t(I / kMxBlock) * kUnitBytes;
+  if (size_t(s.dnw) + bytes + 1024 <= smem_optin) {
+    s.dnw_bytes = bytes;
+    s.total = s.dnw + bytes;
+  }
 }
 
 template <int T>
@@ -229,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   int2* gtab = reinterpret_cast<int2*>(sm + L.gtab);
   int2* dtab = reinterpret_cast<int2*>(sm + L.dtab);
   int* misc = reinterpret_cast<int*>(sm + L.misc);
+  uint64_t* dnbar = reinterpret_cast<uint64_t*>(sm + L.dnbar);
+  uint8_t* dnw = sm + L.dnw;
   DecodeState* st = a.state;
 
   // ---- 0. next launch, routing-independent prefetch, previous kernel ---------
@@ -247,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  if (tid == 0) {
+    mbar_init(dnbar, 1);
+    mbar_fence_init();
+  }
+
   // ---- 1. x; router rows and shared gate/up rows ------------------------------
   #pragma unroll 1
   for (int j = tid; j < T * d / 8; j += kThreads)
@@ -264,34 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     const int n8 = d / 8;
     const uint4* x4 = reinterpret_cast<const uint4*>(xs);
     uint4 w[kRowVec];
-    // the first batch of this warp's first row is requested before x is split
-    if (warp < n_rows) {
-      const uint4* r4 = row_ptr(warp);
-#pragma unroll
-      for (int m = 0; m < kRowVec; ++m) {
-        const int j = lane + 32 * m;
-        w[m] = j < n8 ? ldg_nc_stream_u4(r4 + j) : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    // x -> e4m3 terms (B operand of the routed gate/up MMAs)
-    #pragma unroll 1
-    for (int u = warp; u < T * KBd; u += kWarps) {
-      const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
-      const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
-      if (lane == 0) xfa[u] = act_factor(ex, 1.0f);
-    }
     for (int it = warp; it < n_rows; it += kWarps) {
       const uint4* r4 = row_ptr(it);
       float acc[T];
 #pragma unroll
       for (int t = 0; t < T; ++t) acc[t] = 0.0f;
       for (int j0 = 0; j0 < n8; j0 += 32 * kRowVec) {
-        if (it != warp || j0 != 0) {
 #pragma unroll
-          for (int m = 0; m < kRowVec; ++m) {
-            const int j = j0 + lane + 32 * m;
-            w[m] = j < n8 ? ldg_nc_stream_u4(r4 + j) : make_uint4(0u, 0u, 0u, 0u);
-          }
+        for (int m = 0; m < kRowVec; ++m) {
+          const int j = j0 + lane + 32 * m;
+          w[m] = j < n8 ? ldg_nc_stream_u4(r4 + j) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int m = 0; m < kRowVec; ++m) {
@@ -326,64 +328,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   __syncthreads();
   if (warp == kWarps - 1 && lane == 0) red_release_add(&st->routed, 1u);
 
-  // ---- 2. routing: every CTA's logits (and h_sh) are in; warp t < T ranks token t
+  // ---- 2. x -> e4m3 terms (B operand of the routed gate/up MMAs) while the
+  // other CTAs finish their rows; then every CTA's logits (and h_sh) are in
+#pragma unroll 1
+  for (int u = warp; u < T * KBd; u += kWarps) {
+    const float v = __bfloat162float(xs[(size_t)u * kMxBlock + lane]);
+    const int ex = split_block(v, lane, xb + (size_t)u * kActRowKbBytes);
+    if (lane == 0) xfa[u] = act_factor(ex, 1.0f);
+  }
   if (tid == 0) wait_geq_u32(&st->routed, uint32_t(G), a.status);
   __syncthreads();
-  if (warp < T) {
-    const int t = warp;
-    uint32_t key[kPL];
-#pragma unroll
-    for (int i = 0; i < kPL; ++i) {
-      const int e = i * 32 + lane;
-      key[i] = 0u;
+  {
+    // top-k, stage 1 (all warps): the best min(k, 32) of every (token,
+    // 32-expert chunk), by key descending, equal keys -> lower expert index
+    const int nch = (E + 31) / 32, kk = k < 32 ? k : 32;
+    uint32_t* ckey = reinterpret_cast<uint32_t*>(sm + L.gpart);
+    uint32_t* cidx = ckey + T * nch * kk;
+#pragma unroll 1
+    for (int task = warp; task < T * nch; task += kWarps) {
+      const int t = task / nch, e = (task - t * nch) * 32 + lane;
+      uint32_t key = 0u;
       if (e < E) {
-        float x = __ldcg(a.logits + (size_t)t * E + e);
-        if (a.bias) x = __fadd_rn(x, a.bias[(size_t)t * a.bias_stride + e]);
-        key[i] = rank_key(x);
+        float v = __ldcg(a.logits + (size_t)t * E + e);
+        if (a.bias) v = __fadd_rn(v, a.bias[(size_t)t * a.bias_stride + e]);
+        key = rank_key(v);
+      }
+#pragma unroll 1
+      for (int r = 0; r < kk; ++r) {
+        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, key);
+        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, (mx != 0u && key == mx) ? uint32_t(e) : 0xFFFFFFFFu);
+        if (lane == 0) {
+          ckey[task * kk + r] = mx;
+          cidx[task * kk + r] = win;
+        }
+        if (uint32_t(e) == win) key = 0u;
       }
     }
-    // k rounds: warp maximum, ties to the lowest expert index
-    uint32_t bk = 0u, be = 0xFFFFFFFFu;
-#pragma unroll
-    for (int i = 0; i < kPL; ++i)
-      if (key[i] > bk) {
-        bk = key[i];
-        be = uint32_t(i * 32 + lane);
-      }
-    uint32_t my_e = 0u, my_key = 0u;
+    __syncthreads();
+    // stage 2: one warp per token merges the sorted chunk lists; lane c holds
+    // the head of chunk c
+    if (warp < T) {
+      const int t = warp;
+      const uint32_t* lk = ckey + (size_t)(t * nch + lane) * kk;
+      const uint32_t* li = cidx + (size_t)(t * nch + lane) * kk;
+      int ptr = 0;
+      uint32_t hk = lane < nch ? lk[0] : 0u, hi = lane < nch ? li[0] : 0xFFFFFFFFu;
+      uint32_t my_e = 0u, my_key = 0u;
 #pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, bk);
-      const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, bk == wmax ? be : 0xFFFFFFFFu);
-      if (lane == r) {
-        my_e = emin;
-        my_key = wmax;
-      }
-      if (lane == int(emin & 31u)) {
-        const int slot = int(emin >> 5);
-        bk = 0u;
-        be = 0xFFFFFFFFu;
-#pragma unroll
-        for (int i = 0; i < kPL; ++i) {
-          if (i == slot) key[i] = 0u;
-          if (key[i] > bk) {
-            bk = key[i];
-            be = uint32_t(i * 32 + lane);
-          }
+      for (int r = 0; r < k; ++r) {
+        const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, hk);
+        const uint32_t emin = __reduce_min_sync(0xFFFFFFFFu, hk == wmax ? hi : 0xFFFFFFFFu);
+        if (lane == r) {
+          my_e = emin;
+          my_key = wmax;
+        }
+        if (hk == wmax && hi == emin) {
+          ++ptr;
+          hk = ptr < kk ? lk[ptr] : 0u;
+          hi = ptr < kk ? li[ptr] : 0xFFFFFFFFu;
         }
       }
-    }
-    const float v = rank_value(my_key);
-    const float v0 = __shfl_sync(0xFFFFFFFFu, v, 0);
-    const float ex = lane < k ? expf(v - v0) : 0.0f;
-    const float sum = warp_sum(ex);
-    if (lane < k) {
-      const float w = ex / sum;
-      sel_e[t * k + lane] = int(my_e);
-      sel_w[t * k + lane] = w;
-      if (c == 0) {
-        if (a.idx_out) a.idx_out[t * k + lane] = int(my_e);
-        if (a.w_out) a.w_out[t * k + lane] = w;
+      const float v = rank_value(my_key);
+      const float v0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+      const float ex = lane < k ? expf(v - v0) : 0.0f;
+      const float sum = warp_sum(ex);
+      if (lane < k) {
+        const float w = ex / sum;
+        sel_e[t * k + lane] = int(my_e);
+        sel_w[t * k + lane] = w;
+        if (c == 0) {
+          if (a.idx_out) a.idx_out[t * k + lane] = int(my_e);
+          if (a.w_out) a.w_out[t * k + lane] = w;
+        }
       }
     }
   }
@@ -391,42 +407,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   // ---- active experts (ascending) with their slots, and this CTA's gate/up
   // range, by warp 0 alone -----------------------------------------------------------
   if (warp == 0) {
+    // slot j = lane + 32 m holds expert ev[m]; every slot is compared with
+    // every other through shuffles (no shared-memory round trips)
     const int n = T * k;
-    int D = 0;
-    #pragma unroll 1
-    for (int j = lane; j < n; j += 32) {
-      const int e = sel_e[j];
-      int f = 1;
-      #pragma unroll 1
-      for (int i = 0; i < j; ++i) f &= sel_e[i] != e ? 1 : 0;
-      first[j] = f;
+    int ev[4], fst[4], rank[4], pos[4], cnt[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j = lane + 32 * m;
+      ev[m] = j < n ? sel_e[j] : 0x7FFFFFFF;
+      fst[m] = j < n ? 1 : 0;
+      rank[m] = pos[m] = cnt[m] = 0;
     }
-    __syncwarp();
-    #pragma unroll 1
-    for (int j0 = 0; j0 < n; j0 += 32) {
-      const int j = j0 + lane;
-      int f = 0;
-      if (j < n) {
-        // the rank of e among the distinct experts counts first occurrences
-        // of smaller ids; pos is the slot's place among e's slots
-        const int e = sel_e[j];
-        int rank = 0, pos = 0, cnt = 0;
-        #pragma unroll 1
-        for (int i = 0; i < n; ++i) {
-          const int ei = sel_e[i];
-          rank += (first[i] && ei < e) ? 1 : 0;
-          pos += (i < j && ei == e) ? 1 : 0;
-          cnt += ei == e ? 1 : 0;
-        }
-        f = first[j];
-        act_slot[rank * kDecodeMaxT + pos] = j;
-        act_tok[rank * kDecodeMaxT + pos] = j / k;
-        if (f) {
-          act[rank] = e;
-          act_n[rank] = cnt;
+    auto slot_e = [&](int i) {
+      const int a0 = __shfl_sync(0xFFFFFFFFu, ev[0], i & 31), a1 = __shfl_sync(0xFFFFFFFFu, ev[1], i & 31);
+      const int a2 = __shfl_sync(0xFFFFFFFFu, ev[2], i & 31), a3 = __shfl_sync(0xFFFFFFFFu, ev[3], i & 31);
+      return i < 32 ? a0 : (i < 64 ? a1 : (i < 96 ? a2 : a3));
+    };
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+      const int ei = slot_e(i);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int j = lane + 32 * m;
+        if (ei == ev[m]) {
+          ++cnt[m];
+          if (i < j) {
+            ++pos[m];
+            fst[m] = 0;
+          }
         }
       }
-      D += __popc(__ballot_sync(0xFFFFFFFFu, f != 0));
+    }
+    // rank of an expert among the distinct ones: first occurrences of smaller ids
+    int D = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) D += __popc(__ballot_sync(0xFFFFFFFFu, fst[m] != 0));
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+      const int ei = slot_e(i);
+      const int f0_ = __shfl_sync(0xFFFFFFFFu, fst[0], i & 31), f1_ = __shfl_sync(0xFFFFFFFFu, fst[1], i & 31);
+      const int f2_ = __shfl_sync(0xFFFFFFFFu, fst[2], i & 31), f3_ = __shfl_sync(0xFFFFFFFFu, fst[3], i & 31);
+      const int fi = i < 32 ? f0_ : (i < 64 ? f1_ : (i < 96 ? f2_ : f3_));
+#pragma unroll
+      for (int m = 0; m < 4; ++m) rank[m] += (fi && ei < ev[m]) ? 1 : 0;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int j = lane + 32 * m;
+      if (j < n) {
+        act_slot[rank[m] * kDecodeMaxT + pos[m]] = j;
+        act_tok[rank[m] * kDecodeMaxT + pos[m]] = j / k;
+        if (fst[m]) {
+          act[rank[m]] = ev[m];
+          act_n[rank[m]] = cnt[m];
+        }
+      }
     }
     if (lane < 2) {
       // gate/up tiles: contiguous ranges, balanced by bytes together with each
@@ -457,12 +492,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   __syncthreads();
   const int D = misc[0], i0 = misc[1], i1 = misc[2] > misc[1] ? misc[2] : misc[1];
 
-  // the down units of this CTA's output tiles into L2, one active expert per
-  // warp; they are read after the h exchange
-  if (ntl > 0 && lane == 0)
+  // this CTA's gate/up tiles into L2 (one prefetch per tile, spread over the
+  // warps); the down units of its output tiles for every active expert into
+  // shared memory when they fit (bulk copies, one per expert, by the last
+  // warp; read after the h exchange), else into L2
+  const bool dn_staged = L.dnw_bytes > 0 && uint32_t(D * ntl) * U_dn <= L.dnw_bytes && ntl > 0;
+  if (lane == 0) {
 #pragma unroll 1
-    for (int ai = warp; ai < D; ai += kWarps)
-      prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
+    for (int gt = i0 + warp; gt < i1; gt += kWarps) {
+      const int ai = gt / NTg;
+      prefetch_l2(a.gate_up + (size_t)act[ai] * a.gu_mat + (size_t)(gt - ai * NTg) * U_gu, U_gu);
+    }
+    if (ntl > 0 && !dn_staged)
+#pragma unroll 1
+      for (int ai = warp; ai < D; ai += kWarps)
+        prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
+    if (dn_staged && warp == kWarps - 1) {
+      mbar_arrive_expect_tx(dnbar, uint32_t(D * ntl) * U_dn);
+#pragma unroll 1
+      for (int ai = 0; ai < D; ++ai)
+        bulk_g2s(dnw + (size_t)ai * ntl * U_dn, a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn,
+                 uint32_t(ntl) * U_dn, dnbar);
+    }
+  }
 
   // ---- 3. routed gate/up: items (tile, K-range of kU units) --------------------
   {
@@ -604,7 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   dn_table(0);
   __syncthreads();
   UnitBatch dcur, dnxt;
-  if (warp < min(n_dn, kMaxDnItems)) load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
+  if (!dn_staged && warp < min(n_dn, kMaxDnItems))
+    load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
 
   if (a.has_shared && ntl > 0) {
     #pragma unroll 1
@@ -652,6 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     for (int j = tid; j < n16; j += kThreads)
       reinterpret_cast<uint4*>(hbs)[j] = __ldcg(reinterpret_cast<const uint4*>(a.h) + j);
     __syncthreads();
+    if (dn_staged) mbar_wait(dnbar, 0u, a.status);   // the down units are in shared memory
     // B columns of a down MMA: 4 groups of 8 features x 2 terms; lane (g, q)
     // holds the C columns of group q, so the quad sum adds the groups
     const int grp = g >> 1;
@@ -662,16 +716,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       if (rb > 0) {
         dn_table(rb);
         __syncthreads();
-        if (rb + warp < round_end) load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
+        if (!dn_staged && rb + warp < round_end)
+          load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
       }
 #pragma unroll 1
       for (int it = rb + warp; it < round_end; it += kWarps) {
-        if (it + kWarps < round_end) {
+        const int meta = dtab[it - rb].y;
+        const int kb0 = (meta >> 4) & 255, n = meta & 15, ai = meta >> 12;
+        if (dn_staged) {
+          // this item's units from shared memory: expert rank ai, tile it / per_tile
+          const uint8_t* base = dnw + (size_t)(ai * ntl + it / per_tile) * U_dn + (size_t)kb0 * kUnitBytes;
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const uint8_t* unit = base + (size_t)(u < n ? u : 0) * kUnitBytes;
+            dcur.w[u] = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            dcur.s[u] = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
+          }
+        } else if (it + kWarps < round_end) {
           const int2 nx = dtab[it + kWarps - rb];
           load_batch(dnxt, a.down + uint32_t(nx.x), 0, nx.y & 15, lane);
         }
-        const int meta = dtab[it - rb].y;
-        const int kb0 = (meta >> 4) & 255, n = meta & 15, ai = meta >> 12;
         const int nt = act_n[ai];
         const int* slots = act_slot + ai * kDecodeMaxT;
         const int* toks = act_tok + ai * kDecodeMaxT;
@@ -722,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             o[8 + g] = v1;
           }
         }
-        dcur = dnxt;
+        if (!dn_staged) dcur = dnxt;
       }
       __syncthreads();
       // add this round's partials into the y accumulators, items in order
@@ -789,7 +853,9 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, uint32_t* smem_bytes)
 
 template <int T>
 int launch_decode_t(const DecodeArgs& a, uint32_t smem, const DeviceInfo& di, cudaStream_t s) {
-  const Smem L = smem_plan(T, a.d, a.I, a.E, a.k, di.sm_count);
+  Smem L = smem_plan(T, a.d, a.I, a.E, a.k, di.sm_count);
+  stage_down_units(L, a.I, di.smem_optin);
+  smem = L.total;
   MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
   int per_sm = 0;
   MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, kThreads, smem));
