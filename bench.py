@@ -51,6 +51,12 @@ def parse():
     ap.add_argument("--sets", type=int, default=None, help="weight sets cycled (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--oracle-1core-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--lmhead", action="store_true",
+                    help="time the FP8 LM-head GEMV (V=157184, d=2560) instead of the MoE layer")
+    ap.add_argument("--lm-tokens", type=int, default=1)
+    ap.add_argument("--act", choices=["bf16", "mxfp8"], default="bf16",
+                    help="mxfp8: the 8-bit-activation layer (moe_forward_w4a8)")
     ap.add_argument("--profile", action="store_true",
                     help="short run for profilers: no clocks, e2e or CPU baseline")
     return ap.parse_args()
@@ -164,6 +170,7 @@ def stage_bytes(w, stage, D, slots):
         "topk": T * E * 4 + T * w.k * 8,
         "sort": T * w.k * 4 * 4,
         "decode_fused": wl.weight_bytes(w, D) + T * d * 4,
+        "layer": wl.weight_bytes(w, D) + T * d * 4,
         "routed_gateup": D * per_gu + slots * I * 4,
         "act_split_h": slots * I * 4 + slots * (I // 32) * 130,
         "routed_down": D * per_dn + slots * d * 4,
@@ -257,6 +264,28 @@ def time_oracle(w, n_calls, device, budget_s=25.0):
     return dt / done * 1e6, done, dt
 
 
+def time_oracle_1core(w, budget_s=8.0):
+    """The same oracle layer call on one host core: a child process pinned to
+    one CPU with single-threaded BLAS (inputs drawn on the CPU: same shapes
+    and distributions; only the timing is used)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-1core-child", "--workload", w.name]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 6 + 120)
+        j = json.loads(r.stdout.strip().splitlines()[-1])
+        return j["us"], j["calls"], j["s"]
+    except Exception as e:   # pragma: no cover - reported, not fatal
+        return None, 0, str(e)
+
+
+def oracle_1core_child(w):
+    cpus = sorted(os.sched_getaffinity(0))
+    os.sched_setaffinity(0, {cpus[0]})
+    us, n, dt = time_oracle(w, 16, "cpu", budget_s=8.0)
+    print(json.dumps({"us": us, "calls": n, "s": dt}), flush=True)
+
+
 # ---------------------------------------------------------------------------
 
 def run_reference(args, w):
@@ -330,8 +359,9 @@ def run_ours(args, w):
                 mx.moe_forward_profiled(layers[s], xs[s], events[s], biases[s], y=ys[s], workspace=work[s],
                                         idx_out=idxs[s], dev_status=status, stream=stream)
             else:
-                mx.moe_forward(layers[s], xs[s], biases[s], y=ys[s], workspace=work[s], idx_out=idxs[s],
-                               dev_status=status, stream=stream)
+                fwd = mx.moe_forward_w4a8 if args.act == "mxfp8" else mx.moe_forward
+                fwd(layers[s], xs[s], biases[s], y=ys[s], workspace=work[s], idx_out=idxs[s],
+                    dev_status=status, stream=stream)
             if copies is not None:
                 copies[1][s].copy_(ys[s], non_blocking=True)
 
@@ -400,6 +430,19 @@ def run_ours(args, w):
         for i, n in enumerate(stages):
             stage_us[n].append(events[s][i].elapsed_time(events[s][i + 1]) * 1e3)
     stage_mean = {n: float(np.mean(v)) for n, v in stage_us.items()}
+    per_D = None
+    if len(stages) == 1 and len(set(D_sets)) > 1:
+        # one launch per layer: its duration per distinct-expert count, from the
+        # profiling graph (events between layers, so launches do not overlap there)
+        per_D = {}
+        for D, t in zip(D_sets, stage_us[stages[0]]):
+            per_D.setdefault(int(D), []).append(t)
+        per_D = {str(D): {"us": float(np.mean(v)), "sets": len(v),
+                          "weight_gbs": weight_bytes_per_call(w, D) / (np.mean(v) * 1e-6) / 1e9}
+                 for D, v in sorted(per_D.items())}
+    if args.act == "mxfp8":
+        # the profiling hook runs the bf16-activation call: report the layer as a whole
+        stage_mean = {"layer": us_per_layer}
     dom = max(stage_mean, key=stage_mean.get)
     D_mean = float(np.mean(D_sets))
     slots = w.T * w.k
@@ -408,7 +451,7 @@ def run_ours(args, w):
     # one launch per layer on the single-launch path: its duration is the timed
     # region's time per layer (launches overlap there, so an event pair around
     # one launch would count the previous layer's tail)
-    dom_us = us_per_layer if stages == ["decode_fused"] else stage_mean[dom]
+    dom_us = us_per_layer if stages == ["decode_fused"] or dom == "layer" else stage_mean[dom]
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
     kernel_src = os.path.join(ROOT, "mxfp4_expert_gb300", "csrc",
                               "decode.cu" if dom == "decode_fused" else
@@ -440,7 +483,23 @@ def run_ours(args, w):
         e1.synchronize()
         ms2 = max_over_ranks(e0.elapsed_time(e1), ws, dev)
         e2e = {"value": ms2 * 1e3 / (calls * ws), "unit": "us/layer",
-               "h2d_bytes_per_step": n_sets * w.T * w.d * 2, "d2h_bytes_per_step": n_sets * w.T * w.d * 2}
+               "h2d_bytes_per_step": n_sets * w.T * w.d * 2, "d2h_bytes_per_step": n_sets * w.T * w.d * 2,
+               "how": "graph replay of (pinned x -> device, moe_forward, y -> pinned) per layer"}
+        # the same through the plain public call every step (no graph): host
+        # clock around the steps, which include every host-side cost of the call
+        e_steps = min(steps, 200)
+        with torch.cuda.stream(stream):
+            one_cycle(False, (hx, hy))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(e_steps):
+                one_cycle(False, (hx, hy))
+        torch.cuda.synchronize()
+        dt_e = time.perf_counter() - t0
+        dt_e = max_over_ranks(dt_e, ws, dev)
+        e2e["eager"] = {"value": dt_e * 1e6 / (e_steps * n_sets * ws), "unit": "us/layer", "steps": e_steps,
+                        "how": "moe_forward called from Python per layer, host clock, pinned copies each step"}
 
     launches_per_call = {"decode_fused": 1, "act_split_x": 1, "router_shared_gateup": 1, "topk": 1, "sort": 3,
                          "quant_x": 1, "routed_gateup": 1, "quant_h": 1, "routed_down": 1, "combine": 1}
@@ -452,6 +511,10 @@ def run_ours(args, w):
         cpu = {"value": us_cpu, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{n_done} single-token layer calls of {w.name} in {dt:.1f} s "
                          f"(numpy fp64; experts dequantised from MXFP4 inside each call)"}
+        us1, n1, dt1 = time_oracle_1core(w)
+        cpu["one_core"] = {"value": us1, "unit": "us/layer", "cores": 1,
+                           "sample": f"{n1} single-token layer calls in a child pinned to one CPU, "
+                                     f"single-threaded BLAS ({dt1 if isinstance(dt1, str) else round(dt1, 1)} s)"}
 
     if rank != 0:
         return
@@ -459,12 +522,15 @@ def run_ours(args, w):
         "metric": METRIC, "value": us_per_layer, "unit": "us/layer", "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("e2m1 (as e4m3) x e4m3 2-term activations, e8m0 block scales (tcgen05 mxf8f6f4 routed experts), "
+        "dtype": ("e2m1 (as e4m3) x mxfp8 e4m3 activations, e8m0 block scales (tcgen05 mxf8f6f4 routed experts), "
+                  "bf16 router/shared (mma.sync), f32 accumulate" if args.act == "mxfp8" else
+                  "e2m1 (as e4m3) x e4m3 2-term activations, e8m0 block scales (tcgen05 mxf8f6f4 routed experts), "
                   "bf16 router/shared (mma.sync), f32 accumulate"
                   if path == mx.MOE_PATH_PREFILL_TC else
                   "e2m1xe4m3->f32 (mma.sync), bf16 router/shared, f32 accumulate"),
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, E={w.E}, k={w.k}, I={w.I}, shared=1",
+        "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, E={w.E}, k={w.k}, I={w.I}, shared=1"
+                               + (", activations MXFP8 (W4A8)" if args.act == "mxfp8" else ""),
                    "weight_sets_cycled": n_sets, "layers_per_step": n_sets,
                    "l2": f"defeated by cycling {n_sets} weight sets "
                          f"({n_sets * algo_bytes / 1e9:.2f} GB of weights read per step; L2 129 MB)",
@@ -473,6 +539,7 @@ def run_ours(args, w):
         "pct_of_hbm_peak": 100.0 * eff_gbs / peak,
         "algorithmic_bytes_per_layer": algo_bytes,
         "stage_us": stage_mean,
+        "isolated_call_us_by_distinct_experts": per_D,
         "step_us_per_layer": step_pct,   # this rank's per-step spread (each step = n_sets layer calls)
         "roofline": {"bound": "hbm", "kernel": dom, "kernel_us": dom_us, "achieved": achieved, "peak": peak,
                      "unit": "GB/s",
@@ -486,8 +553,77 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_lmhead(args):
+    """The FP8 LM-head GEMV: logits [T, 157184] of bf16 x [T, 2560]; the FP8
+    head (402 MB) is larger than L2, so every call streams it from HBM."""
+    rank, ws = dist_setup("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import mxfp4_expert_gb300 as mx
+    V, d, T = 157184, 2560, args.lm_tokens
+    g = torch.Generator(device=dev).manual_seed(7)
+    w = (torch.randn((V, d), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    codes, scales = mx.moe_lmhead_pack_fp8(w)
+    del w
+    x = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
+    logits = torch.empty((T, V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    calls_per_step = 16
+    with torch.cuda.stream(stream):
+        for _ in range(calls_per_step):
+            mx.moe_lmhead_fp8(codes, scales, x, logits, stream=stream)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for _ in range(calls_per_step):
+            mx.moe_lmhead_fp8(codes, scales, x, logits, stream=stream)
+    steps = args.steps or 50
+    for _ in range(args.warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            gr.replay()
+        e1.record(stream)
+    e1.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    us = job_us_per_layer(ms, steps * calls_per_step, ws)
+    bytes_ = V * d + V * 4 + T * d * 2 + T * V * 4
+    peak, peak_kind = measured_peaks()
+    gbs = bytes_ / (us * 1e-6) / 1e9
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": "us per FP8 LM-head call (2560 -> 157184) and effective HBM GB/s", "value": us, "unit": "us/call",
+        "n_gpus": ws, "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 weights (fp32 row scales) x bf16 activations, f32 acc",
+        "data": "synthetic",
+        "config": {"workload": f"lmhead: T={T}, V={V}, d={d}", "calls_per_step": calls_per_step,
+                   "l2": "the 402 MB head exceeds L2 (129 MB)"},
+        "effective_gbs": gbs,
+        "roofline": {"bound": "hbm", "kernel": "lm_gemv_kernel", "kernel_us": us, "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": bytes_},
+        "gpu_launches": 2 * steps * calls_per_step, "clocks": clocks}), flush=True)
+
+
 def main():
     args = parse()
+    if args.oracle_1core_child:
+        oracle_1core_child(wl.get(args.workload))
+        return
+    if args.lmhead and args.impl == "ours":
+        run_lmhead(args)
+        return
     w = wl.get(args.workload)
     if args.impl == "reference":
         run_reference(args, w)

@@ -310,6 +310,31 @@ int moe_forward_w4a8(const moe_layer* L, const void* x_dev, int T, void* y_dev,
 int moe_quant_mxfp8(const void* src_dev, int src_is_bf16, int rows, int K, uint8_t* codes_dev,
                     uint8_t* scales_dev, moe_stream_t stream);
 
+/* ---- FP8 LM head ------------------------------------------------------------ */
+
+/* Quantise a bf16 LM head to FP8 once (online, at load time): per output row
+ * v, s_v = fp32(amax_v / 448) (1 for a zero row) and codes = E4M3 round to
+ * nearest even of fp32(w / s_v), saturating at 448.
+ * Source: page "3 ways to speed up MoE inference on NVIDIA DGX Spark", §4 (the
+ * BF16 LM head, 2,560 -> 157,184, is quantised to FP8 when it is built, which
+ * halves the bytes each decode step reads); the pages do not give the FP8
+ * recipe, and this per-row scale is the reading.
+ *   w_dev       bf16 [V][d] (device)
+ *   codes_dev   uint8 [V][d] E4M3 (device, 2-B aligned); scales_dev fp32 [V]
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE (d odd). */
+int moe_lmhead_pack_fp8(const void* w_dev, int V, int d, uint8_t* codes_dev, float* scales_dev,
+                        moe_stream_t stream);
+
+/* logits[t][v] = s_v * sum_j x[t][j] * codes[v][j] for T <= 8 tokens; the
+ * codes are read once from HBM, the activations enter exactly (bf16 split into
+ * e4m3 terms), fp32 accumulation. Same source as moe_lmhead_pack_fp8.
+ *   codes_dev, scales_dev  as written by moe_lmhead_pack_fp8 (device, 8-B aligned codes)
+ *   x_dev       bf16 [T][d] (device, 16-B aligned)
+ *   logits_dev  fp32 [T][V] (device); overwritten (zeroed on `stream` first)
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE (V % 16, d % 64, T > 8). */
+int moe_lmhead_fp8(const uint8_t* codes_dev, const float* scales_dev, int V, int d, const void* x_dev, int T,
+                   float* logits_dev, moe_stream_t stream);
+
 /* Size in bytes of the scratch array inside the library that
  * moe_forward_static_scratch uses instead of a caller's workspace. */
 #define MOE_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)

@@ -19,7 +19,7 @@ __all__ = [
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
     "moe_route_topk", "moe_sort_workspace_bytes", "moe_sort_by_expert",
-    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_profiled", "moe_forward_w4a8", "moe_quant_mxfp8", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
+    "moe_workspace_bytes", "moe_query_path", "moe_stage_names", "moe_forward", "moe_forward_profiled", "moe_forward_w4a8", "moe_quant_mxfp8", "moe_lmhead_pack_fp8", "moe_lmhead_fp8", "moe_forward_static_scratch", "STATIC_SCRATCH_BYTES", "moe_selftest_bounded_wait", "moe_status_string", "moe_version",
 ]
 
 # The in-tree build, and only it: there is no way to point the binding at
@@ -80,6 +80,8 @@ def _load():
         "moe_workspace_bytes": (sz, [ctypes.POINTER(moe_shape), i32]),
         "moe_query_path": (i32, [ctypes.POINTER(moe_shape), i32]),
         "moe_forward": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]),
+        "moe_lmhead_pack_fp8": (i32, [vp, i32, i32, vp, vp, vp]),
+        "moe_lmhead_fp8": (i32, [vp, vp, i32, i32, vp, i32, vp, vp]),
         "moe_quant_mxfp8": (i32, [vp, i32, i32, i32, vp, vp, vp]),
         "moe_forward_w4a8": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]),
         "moe_forward_profiled": (i32, [ctypes.POINTER(moe_layer), vp, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp,
@@ -344,6 +346,35 @@ def moe_quant_mxfp8(src: torch.Tensor, stream=None):
     _check(lib.moe_quant_mxfp8(_p(src), 1 if src.dtype == torch.bfloat16 else 0, rows, K, _p(codes), _p(scales),
                                _s(stream)), "moe_quant_mxfp8")
     return codes, scales
+
+
+def moe_lmhead_pack_fp8(w: torch.Tensor, stream=None):
+    """bf16 LM head [V, d] -> (E4M3 codes uint8 [V, d], fp32 row scales [V])."""
+    _cuda(w, torch.bfloat16, "w")
+    V, d = w.shape
+    codes = torch.empty((V, d), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(V, dtype=torch.float32, device=w.device)
+    _check(lib.moe_lmhead_pack_fp8(_p(w), V, d, _p(codes), _p(scales), _s(stream)), "moe_lmhead_pack_fp8")
+    return codes, scales
+
+
+def moe_lmhead_fp8(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, logits: torch.Tensor | None = None,
+                   stream=None):
+    """fp32 logits [T, V] of bf16 x [T, d] against the FP8 head (codes, scales)."""
+    _cuda(codes, torch.uint8, "codes")
+    _cuda(scales, torch.float32, "scales")
+    _cuda(x, torch.bfloat16, "x")
+    V, d = codes.shape
+    if x.dim() != 2 or x.shape[1] != d or scales.numel() != V:
+        raise ValueError("x must be [T, d] and scales [V] for codes [V, d]")
+    T = x.shape[0]
+    if logits is None:
+        logits = torch.empty((T, V), dtype=torch.float32, device=x.device)
+    _cuda(logits, torch.float32, "logits")
+    if logits.numel() < T * V:
+        raise ValueError("logits needs T * V elements")
+    _check(lib.moe_lmhead_fp8(_p(codes), _p(scales), V, d, _p(x), T, _p(logits), _s(stream)), "moe_lmhead_fp8")
+    return logits
 
 
 def moe_forward_profiled(layer: Layer, x: torch.Tensor, stage_events, bias: torch.Tensor | None = None,

@@ -497,6 +497,27 @@ extern "C" int moe_quant_mxfp8(const void* src_dev, int src_is_bf16, int rows, i
                           (cudaStream_t)stream);
 }
 
+extern "C" int moe_lmhead_pack_fp8(const void* w_dev, int V, int d, uint8_t* codes_dev, float* scales_dev,
+                                   moe_stream_t stream) {
+  MOE_CHECK_ARG(w_dev && codes_dev && scales_dev && V > 0 && d > 0, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(d % 2 == 0 && aligned(codes_dev, 2), MOE_ERR_UNSUPPORTED_SHAPE);
+  DeviceInfo di;
+  const int st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return launch_lm_pack(w_dev, V, d, codes_dev, scales_dev, (cudaStream_t)stream);
+}
+
+extern "C" int moe_lmhead_fp8(const uint8_t* codes_dev, const float* scales_dev, int V, int d, const void* x_dev,
+                              int T, float* logits_dev, moe_stream_t stream) {
+  MOE_CHECK_ARG(codes_dev && scales_dev && x_dev && logits_dev && V > 0 && d > 0 && T >= 1, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(V % 16 == 0 && d % 64 == 0 && T <= 8, MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK_ARG(aligned(codes_dev, 8) && aligned(x_dev, 16), MOE_ERR_INVALID_ARG);
+  DeviceInfo di;
+  const int st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return launch_lm_gemv(codes_dev, scales_dev, V, d, x_dev, T, logits_dev, di, (cudaStream_t)stream);
+}
+
 extern "C" const char* moe_stage_names(int path) {
   if (path == MOE_PATH_DECODE_FUSED) return "decode_fused";
   if (path == MOE_PATH_DECODE_MMA)

@@ -1,41 +1,39 @@
 // Single-launch decode path (T <= 4 tokens): the whole layer in one kernel
 // launch, one CTA per SM, 16 warps per CTA.
 //
-// Weights are read straight from global memory into registers (16-byte and
-// 8-byte non-caching loads) by the warp that uses them. Before a phase starts,
-// one thread of the CTA issues bulk L2 prefetches for every weight byte the
-// phase will read, so HBM streams the phase's bytes at full depth while the
-// warps' own loads mostly hit L2. Shared memory holds only activations,
-// partial sums and routing tables, which leaves most of the SM's L1 for loads
-// in flight.
-//
 // Phases of one CTA c of G:
-//   0. launch_dependents, L2 prefetch of this CTA's router rows, shared
-//      gate/up rows and shared-down rows (routing-independent), then
-//      griddepcontrol.wait: under programmatic dependent launch the next
-//      layer's prefetches overlap the end of this one.
+//   0. griddepcontrol.launch_dependents, then L2 prefetch of this CTA's
+//      router rows, shared gate/up rows and shared-down rows (routing-
+//      independent; one prefetch per warp), then griddepcontrol.wait: under
+//      programmatic dependent launch the next layer's prefetches overlap the
+//      end of the previous one, and nothing written by the previous kernel is
+//      read before the wait.
 //   1. x -> shared memory; router rows [c E/G, (c+1) E/G) and shared gate/up
-//      features [c I/G, (c+1) I/G), one bf16 row per warp, fp32 FMAs; logits
-//      and h_sh to global memory, one release increment each.
-//   2. x -> e4m3 terms (B operand of the routed MMAs) while the other CTAs
-//      finish; wait for every CTA's logits; top-k in every CTA (best k of each
-//      32-expert chunk on all warps, then a k-way merge per token); active
-//      experts with their slots.
-//   3. Routed gate/up: this CTA's contiguous range of the D x (2I/16) packed
-//      tiles (balanced by bytes against each CTA's down and shared-down
-//      work), prefetched into L2 together with its down units. Work items are
-//      (tile, K-range) pairs; a warp loads 8 units (272 B: 16 rows x 32 K,
-//      E2M1 codes + E8M0 scales) at a time and multiplies them on the e4m3
-//      warp MMA against the 3-term e4m3 split of x. Partials of a tile are
-//      added in a fixed order, SwiGLU is applied, and h is published as 2 e4m3
-//      terms per feature with one factor per 8 features (routing weight
-//      folded in), followed by one release increment.
-//   4. Shared down rows of this CTA's 16-row output tiles (needs every CTA's
-//      h_sh), fp32 FMAs.
+//      features [c I/G, (c+1) I/G), one bf16 row per warp (16-byte loads of
+//      the whole row in flight, fp32 FMAs); logits and h_sh to global memory,
+//      then one release increment.
+//   2. x -> 3 e4m3 terms per 32-block (B operand of the routed MMAs) while the
+//      other CTAs finish; wait for every CTA's logits; top-k in every CTA (the
+//      best k of each 32-expert chunk on all warps, then a k-way merge per
+//      token); the active experts with their slots (one warp, shuffles); this
+//      CTA's contiguous range of gate/up tiles, balanced by bytes against its
+//      down and shared-down work. One L2 prefetch per gate/up tile and per
+//      active expert's down units.
+//   3. Routed gate/up: items (16-row tile, 8 units of 272 B = 16 rows x 32 K
+//      of E2M1 codes + E8M0 scales), item j on warp j % 16. Each warp keeps 4
+//      items in flight, copied with cp.async into its own shared-memory
+//      buffers, and multiplies them on the e4m3 warp MMA (m16n8k32) against
+//      the x terms. The warp that finishes a tile's last item adds the tile's
+//      partials in K order, applies SwiGLU and writes the tile's 8 features of
+//      h as 2 e4m3 terms per feature with one factor per 8 features (routing
+//      weight folded in); then one release increment per CTA.
+//   4. Shared down rows of this CTA's 16-row output tiles (every CTA's h_sh is
+//      in since the routing barrier), fp32 FMAs, while the down items are
+//      already being copied (cp.async, from L2) into the warps' buffers.
 //   5. Routed down: after every CTA's h is in, the h terms of all slots go to
-//      shared memory; work items are (output tile, active expert, K-range)
-//      MMAs into per-item partials, added in a fixed order into y (bf16).
-//      Each CTA owns whole output tiles, so y needs no cross-CTA reduction.
+//      shared memory; items (output tile, active expert, 8 units) into
+//      per-item partials, added in a fixed order into y (bf16). Each CTA owns
+//      whole output tiles, so y needs no cross-CTA reduction.
 //
 // The counters live at the head of the workspace and must be zero before the
 // first call; the last CTA of a call resets them. Every wait is bounded
@@ -58,6 +56,10 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kU = 8;                // MXFP4 units a warp loads together
 constexpr int kRowVec = 10;          // 16-byte vectors of a bf16 row a lane loads together
 constexpr int kMaxGuItems = 96;      // gate/up (tile, K-range) items per round
+// items a warp keeps in flight (cp.async into its own shared-memory buffers):
+// 4 for one or two tokens, 2 when the activations need more shared memory
+__host__ __device__ constexpr int stage_items(int T) { return T <= 2 ? 4 : 2; }
+constexpr uint32_t kItemBytes = kU * kUnitBytes;   // one item: kU units of a 16-row tile
 constexpr int kMaxDnItems = 64;      // down (tile, expert, K-range) items per round
 constexpr int kMergeChunks = 16;     // top-k: E <= 16 chunks of 32 experts
 constexpr int kHTermBytes = 64;      // h of one (slot, K-block): 2 e4m3 terms x 32 features
@@ -96,21 +98,19 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ldg_nc_u16(const void* p) {
-  unsigned short v;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ uint2 ldg_nc_stream_u2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
 // L2 prefetch of [p, p + bytes) (16-byte aligned, multiple of 16) in 32 KB pieces.
 __device__ __noinline__ void prefetch_range(const void* p, uint32_t bytes) {
   const uint8_t* b = static_cast<const uint8_t*>(p);
   for (uint32_t o = 0; o < bytes; o += 32768u) prefetch_l2(b + o, min(32768u, bytes - o));
 }
+
+// 16-byte asynchronous global -> shared copy through L2 (no L1 allocation).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Weight scale bytes (row g in the low byte, row g+8 in the high byte) ->
 // 2^(s-127) as fp32 (s = 0 gives 0).
@@ -123,29 +123,12 @@ __device__ __forceinline__ float scale_hi(uint32_t sc16) { return __uint_as_floa
 // factor is w x 2^(e+6) (0 for an all-zero block).
 __device__ __forceinline__ float act_factor(int e, float w) { return e == kActZeroExp ? 0.0f : scale2(w, e + 6); }
 
-// Weights of up to kU consecutive 272-byte units of one packed tile, in
-// registers: this lane's 8 code bytes and the scale pair of its rows.
-struct UnitBatch {
-  uint2 w[kU];
-  uint32_t s[kU];
-};
-// Loads units [kb, kb + n) of the tile at `base` (n <= kU; the lanes of units
-// past n load unit kb again and are never used).
-__device__ __forceinline__ void load_batch(UnitBatch& b, const uint8_t* base, int kb, int n, int lane) {
-#pragma unroll
-  for (int u = 0; u < kU; ++u) {
-    const uint8_t* unit = base + (size_t)(kb + (u < n ? u : 0)) * kUnitBytes;
-    b.w[u] = ldg_nc_stream_u2(unit + lane * 8);
-    b.s[u] = ldg_nc_u16(unit + kUnitCodeBytes + 2 * (lane >> 2));
-  }
-}
-
 // Shared-memory carve-up (byte offsets), identical on host and device.
 // Region ov holds x, its e4m3 terms and factors (phases 1-3) and later the h
 // terms of every slot (phase 5); region cg holds the gate/up partials.
 struct Smem {
   uint32_t ov, xs, xb, xfa, hbs, hfa, gpart, rpart, hsh, dpart, yacc, sel_e, sel_w, act, act_n, act_slot, act_tok,
-      first, gtab, dtab, misc, dnbar, dnw, dnw_bytes, total;
+      tcnt, gtab, dtab, misc, wbuf, total;
 };
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -184,32 +167,19 @@ __host__ __device__ inline Smem smem_plan(int T, int d, int I, int E, int k, int
   s.act_n = take(kDecodeMaxT * 32 * 4, 4);
   s.act_slot = take(kDecodeMaxT * 32 * kDecodeMaxT * 4, 4);
   s.act_tok = take(kDecodeMaxT * 32 * kDecodeMaxT * 4, 4);
-  s.first = take(kDecodeMaxT * 32 * 4, 4);
+  s.tcnt = take(kMaxGuItems * 4, 4);
   s.gtab = take(kMaxGuItems * 8, 8);
   s.dtab = take(kMaxDnItems * 8, 8);
   s.misc = take(16 * 4, 8);
-  s.dnbar = take(8, 8);
-  s.dnw = align_up(at, 128);
-  s.dnw_bytes = 0;   // set on the host when the down units fit (stage_down_units)
+  s.wbuf = take(uint32_t(kWarps * stage_items(T)) * kItemBytes, 128);
   s.total = at;
   return s;
 }
-// Room for the down units of up to 16 (output tile, expert) pairs of a CTA in
-// shared memory, if the device has it: then they are bulk-copied there during
-// the gate/up phase.
-inline void stage_down_units(Smem& s, int I, size_t smem_optin) {
-  const uint32_t bytes = 16u * uint32_t(I / kMxBlock) * kUnitBytes;
-  if (size_t(s.dnw) + bytes + 1024 <= smem_optin) {
-    s.dnw_bytes = bytes;
-    s.total = s.dnw + bytes;
-  }
-}
-
 template <int T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem L) {
   extern __shared__ __align__(128) uint8_t sm[];
   constexpr int kPairs = (T + 1) / 2;
-  constexpr int kPL = (32 * kMergeChunks) / 32;   // logits per lane in the top-k (E <= 512)
+  constexpr int kStageItems = stage_items(T);
   const int d = a.d, I = a.I, E = a.E, k = a.k;
   const int KBd = d / kMxBlock, KBi = I / kMxBlock;
   const int NTd = d / kTileRows, NTg = 2 * I / kTileRows;
@@ -238,12 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   int* act_n = reinterpret_cast<int*>(sm + L.act_n);
   int* act_slot = reinterpret_cast<int*>(sm + L.act_slot);
   int* act_tok = reinterpret_cast<int*>(sm + L.act_tok);
-  int* first = reinterpret_cast<int*>(sm + L.first);
+  int* tcnt = reinterpret_cast<int*>(sm + L.tcnt);
   int2* gtab = reinterpret_cast<int2*>(sm + L.gtab);
+  uint8_t* wb = sm + L.wbuf + (size_t)warp * kStageItems * kItemBytes;   // this warp's item buffers
   int2* dtab = reinterpret_cast<int2*>(sm + L.dtab);
   int* misc = reinterpret_cast<int*>(sm + L.misc);
-  uint64_t* dnbar = reinterpret_cast<uint64_t*>(sm + L.dnbar);
-  uint8_t* dnw = sm + L.dnw;
+
   DecodeState* st = a.state;
 
   // ---- 0. next launch, routing-independent prefetch, previous kernel ---------
@@ -262,10 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  if (tid == 0) {
-    mbar_init(dnbar, 1);
-    mbar_fence_init();
-  }
+
 
   // ---- 1. x; router rows and shared gate/up rows ------------------------------
   #pragma unroll 1
@@ -492,31 +459,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   __syncthreads();
   const int D = misc[0], i0 = misc[1], i1 = misc[2] > misc[1] ? misc[2] : misc[1];
 
-  // this CTA's gate/up tiles into L2 (one prefetch per tile, spread over the
-  // warps); the down units of its output tiles for every active expert into
-  // shared memory when they fit (bulk copies, one per expert, by the last
-  // warp; read after the h exchange), else into L2
-  const bool dn_staged = L.dnw_bytes > 0 && uint32_t(D * ntl) * U_dn <= L.dnw_bytes && ntl > 0;
+  // this CTA's gate/up tiles (one prefetch per tile) and the down units of its
+  // output tiles for every active expert (one prefetch per expert) into L2,
+  // spread over the warps
   if (lane == 0) {
 #pragma unroll 1
     for (int gt = i0 + warp; gt < i1; gt += kWarps) {
       const int ai = gt / NTg;
       prefetch_l2(a.gate_up + (size_t)act[ai] * a.gu_mat + (size_t)(gt - ai * NTg) * U_gu, U_gu);
     }
-    if (ntl > 0 && !dn_staged)
+    if (ntl > 0)
 #pragma unroll 1
-      for (int ai = warp; ai < D; ai += kWarps)
+      for (int ai = kWarps - 1 - warp; ai < D; ai += kWarps)
         prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
-    if (dn_staged && warp == kWarps - 1) {
-      mbar_arrive_expect_tx(dnbar, uint32_t(D * ntl) * U_dn);
-#pragma unroll 1
-      for (int ai = 0; ai < D; ++ai)
-        bulk_g2s(dnw + (size_t)ai * ntl * U_dn, a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn,
-                 uint32_t(ntl) * U_dn, dnbar);
-    }
   }
-
-  // ---- 3. routed gate/up: items (tile, K-range of kU units) --------------------
+  // ---- 3. routed gate/up: items (tile, K-range of kU units), item j of a round
+  // on warp j % kWarps; every warp keeps kStageItems items in flight, copied
+  // with cp.async into its own shared-memory buffers. The warp that finishes a
+  // tile's last item adds the tile's partials in order, applies SwiGLU and
+  // writes the tile's 8 features of h as 2 e4m3 terms per feature with one
+  // factor per 8 features.
   {
     uint8_t* hT = a.h;
     float* hF = reinterpret_cast<float*>(a.h + (size_t)T * k * KBi * kHTermBytes);
@@ -527,26 +489,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     for (int rb = 0; rb < n_tiles; rb += tiles_per_round) {
       const int nt_round = min(tiles_per_round, n_tiles - rb);
       const int n_items = nt_round * KP;
-      // item j: tile rb + j / KP of this CTA's range, units [kU (j % KP), ...):
-      // byte offset of its first unit, and (expert rank << 12 | kb0 << 4 | n)
       if (rb > 0) __syncthreads();
-      #pragma unroll 1
+      // item j: byte offset of its first unit, and (expert rank << 12 | kb0 << 4 | n)
+#pragma unroll 1
       for (int j = tid; j < n_items; j += kThreads) {
         const int tl = j / KP, gt = i0 + rb + tl, ai = gt / NTg, kb = (j - tl * KP) * kU;
         gtab[j] = make_int2(int(act[ai] * a.gu_mat + (uint64_t)(gt - ai * NTg) * U_gu + (uint64_t)kb * kUnitBytes),
                             (ai << 12) | (kb << 4) | min(kU, KBd - kb));
       }
+      for (int j = tid; j < nt_round; j += kThreads) tcnt[j] = 0;
       __syncthreads();
-      UnitBatch cur, nxt;
-      if (warp < n_items) load_batch(cur, a.gate_up + uint32_t(gtab[warp].x), 0, gtab[warp].y & 15, lane);
+      auto issue = [&](int m) {   // this warp's m-th item of the round -> buffer m % kStageItems
+        const int it = warp + m * kWarps;
+        if (it < n_items) {
+          const int2 e = gtab[it];
+          const uint8_t* src = a.gate_up + uint32_t(e.x);
+          uint8_t* dst = wb + (size_t)(m % kStageItems) * kItemBytes;
+          const int n16 = (e.y & 15) * (kUnitBytes / 16);
 #pragma unroll 1
-      for (int it = warp; it < n_items; it += kWarps) {
-        if (it + kWarps < n_items) {
-          const int2 nx = gtab[it + kWarps];
-          load_batch(nxt, a.gate_up + uint32_t(nx.x), 0, nx.y & 15, lane);
+          for (int c = lane; c < n16; c += 32) cp_async16(dst + c * 16, src + c * 16);
         }
+        cp_async_commit();   // one group per item (empty past the end)
+      };
+#pragma unroll
+      for (int m = 0; m < kStageItems; ++m) issue(m);
+#pragma unroll 1
+      for (int m = 0, it = warp; it < n_items; ++m, it += kWarps) {
+        cp_async_wait<kStageItems - 1>();
+        __syncwarp();
+        const uint8_t* base = wb + (size_t)(m % kStageItems) * kItemBytes;
         const int meta = gtab[it].y;
         const int kb0 = (meta >> 4) & 255, n = meta & 15, ai = meta >> 12;
+        const int tl = it / KP;
         const int nt = act_n[ai];
         const int* toks = act_tok + ai * kDecodeMaxT;
         int boff[kPairs], foff[kPairs];
@@ -561,10 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           if (u < n) {
+            const uint8_t* unit = base + (size_t)u * kUnitBytes;
+            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
             const int kb = kb0 + u;
-            const float fwl = scale_lo(cur.s[u]), fwh = scale_hi(cur.s[u]);
-            const uint32_t a0 = decode_rowlo(cur.w[u].x), a1 = decode_rowhi(cur.w[u].x);
-            const uint32_t a2 = decode_rowlo(cur.w[u].y), a3 = decode_rowhi(cur.w[u].y);
+            const float fwl = scale_lo(sc), fwh = scale_hi(sc);
+            const uint32_t a0 = decode_rowlo(wv.x), a1 = decode_rowhi(wv.x);
+            const uint32_t a2 = decode_rowlo(wv.y), a3 = decode_rowhi(wv.y);
 #pragma unroll
             for (int p = 0; p < kPairs; ++p) {
               const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kb * kActRowKbBytes)
@@ -577,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             }
           }
         }
+        __syncwarp();   // every lane is done with the buffer before it is refilled
+        issue(m + kStageItems);
         // the term pairs of a token sit in lanes q and q^1
 #pragma unroll
         for (int p = 0; p < kPairs; ++p) {
@@ -588,64 +567,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             o[16 + g * 2 + (q >> 1)] = v1;   // up row g
           }
         }
-        cur = nxt;
-      }
-      __syncthreads();
-      // epilogue, one warp per tile: K-range partials in order, SwiGLU, h as
-      // 2 e4m3 terms per feature with one factor per 8 features
-#pragma unroll 1
-      for (int tl = warp; tl < nt_round; tl += kWarps) {
-        const int gt = i0 + rb + tl, ai = gt / NTg, tt = gt - ai * NTg;
-        const int nt = act_n[ai];
-        const int* slots = act_slot + ai * kDecodeMaxT;
-        const int kbh = tt >> 2, grp = tt & 3;
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          last = atomicAdd(&tcnt[tl], 1) == KP - 1;
+        }
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (last) {
+          // this warp finished the tile's last item: partials in K order, SwiGLU, h
+          __threadfence_block();
+          const int gt = i0 + rb + tl, tt = gt - ai * NTg, kbh = tt >> 2, grp = tt & 3;
+          const int* slots = act_slot + ai * kDecodeMaxT;
 #pragma unroll
-        for (int p = 0; p < kPairs; ++p) {
-          if (2 * p < nt) {
-            float v = 0.0f;
+          for (int p = 0; p < kPairs; ++p) {
+            if (2 * p < nt) {
+              float v = 0.0f;
 #pragma unroll 1
-            for (int kp = 0; kp < KP; ++kp) v += gpart[(size_t)((tl * KP + kp) * kPairs + p) * 32 + lane];
-            const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
-            const float hv = lane < 16 ? silu_f(v) * up : 0.0f;   // feature lane>>1, token column lane&1
-            float am = fabsf(hv);
-            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
-            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 8));
-            int ex = kActZeroExp;
-            uint32_t e0 = 0u, e1 = 0u;
-            if (am > 0.0f) {
-              ex = floor_log2(am) - 7;
-              const float sv = scale2(hv, -ex);
-              e0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
-              e1 = f32x2_to_e4m3x2(sv - e4m3_to_f32_hw(e0), 0.0f) & 0xFFu;
-            }
-            const int scol = 2 * p + (lane & 1);
-            if (lane < 16 && scol < nt) {
-              const int sl = slots[scol];
-              const size_t base = ((size_t)sl * KBi + kbh) * kHTermBytes + grp * 8 + (lane >> 1);
-              hT[base] = uint8_t(e0);
-              hT[base + 32] = uint8_t(e1);
-              if ((lane >> 1) == 0) hF[((size_t)sl * KBi + kbh) * kHGroups + grp] = act_factor(ex, sel_w[sl]);
+              for (int kp = 0; kp < KP; ++kp) v += gpart[(size_t)((tl * KP + kp) * kPairs + p) * 32 + lane];
+              const float up = __shfl_down_sync(0xFFFFFFFFu, v, 16);
+              const float hv = lane < 16 ? silu_f(v) * up : 0.0f;   // feature lane>>1, token column lane&1
+              float am = fabsf(hv);
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+              am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 8));
+              int ex = kActZeroExp;
+              uint32_t e0 = 0u, e1 = 0u;
+              if (am > 0.0f) {
+                ex = floor_log2(am) - 7;
+                const float sv = scale2(hv, -ex);
+                e0 = f32x2_to_e4m3x2(sv, 0.0f) & 0xFFu;
+                e1 = f32x2_to_e4m3x2(sv - e4m3_to_f32_hw(e0), 0.0f) & 0xFFu;
+              }
+              const int scol = 2 * p + (lane & 1);
+              if (lane < 16 && scol < nt) {
+                const int slx = slots[scol];
+                const size_t base_h = ((size_t)slx * KBi + kbh) * kHTermBytes + grp * 8 + (lane >> 1);
+                hT[base_h] = uint8_t(e0);
+                hT[base_h + 32] = uint8_t(e1);
+                if ((lane >> 1) == 0) hF[((size_t)slx * KBi + kbh) * kHGroups + grp] = act_factor(ex, sel_w[slx]);
+              }
             }
           }
         }
       }
+      cp_async_wait<0>();
       __syncthreads();
     }
   }
   // this CTA's h is written: publish (the last warp; the others go on)
   if (warp == kWarps - 1 && lane == 0) red_release_add(&st->gudone, 1u);
 
-  // ---- 4./5. down: items (output tile, active expert, K-range of kU units);
-  // this warp's first item is requested before the waits, and the shared-down
-  // rows run while the other CTAs finish their gate/up ------------------------------
+  // ---- 4./5. down: items (output tile, active expert, K-range of kU units),
+  // item j of a round on warp j % kWarps, copied from L2 (prefetched during
+  // gate/up) into the warp's buffers before the wait for every CTA's h; the
+  // shared-down rows run while the other CTAs finish their gate/up -------------------
   const int KPD = ceil_div(KBi, kU);
   const int per_tile = D * KPD;
   const int n_dn = ntl * per_tile;
-  // item j: output tile j / per_tile, expert rank (j % per_tile) / KPD, units
-  // [kU (j % KPD), ...): byte offset of its first unit, (rank << 12 | kb0 << 4 | n)
+  // item j: byte offset of its first unit, (expert rank << 12 | kb0 << 4 | n)
   auto dn_table = [&](int rb) {
-    #pragma unroll 1
+#pragma unroll 1
     for (int j = tid; j < min(kMaxDnItems, n_dn - rb); j += kThreads) {
       const int it = rb + j, tl = it / per_tile, rem = it - tl * per_tile, ai = rem / KPD;
       const int kb = (rem - ai * KPD) * kU;
@@ -653,11 +635,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
                           (ai << 12) | (kb << 4) | min(kU, KBi - kb));
     }
   };
+  auto dn_issue = [&](int rb, int m) {   // this warp's m-th item of the round starting at rb
+    const int it = rb + warp + m * kWarps;
+    if (it < min(n_dn, rb + kMaxDnItems)) {
+      const int2 e = dtab[it - rb];
+      const uint8_t* src = a.down + uint32_t(e.x);
+      uint8_t* dst = wb + (size_t)(m % kStageItems) * kItemBytes;
+      const int n16 = (e.y & 15) * (kUnitBytes / 16);
+#pragma unroll 1
+      for (int c = lane; c < n16; c += 32) cp_async16(dst + c * 16, src + c * 16);
+    }
+    cp_async_commit();
+  };
   dn_table(0);
   __syncthreads();
-  UnitBatch dcur, dnxt;
-  if (!dn_staged && warp < min(n_dn, kMaxDnItems))
-    load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
+#pragma unroll
+  for (int m = 0; m < kStageItems; ++m) dn_issue(0, m);
 
   if (a.has_shared && ntl > 0) {
     #pragma unroll 1
@@ -700,12 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     __syncthreads();
     // every slot's h terms and group factors (contiguous in the workspace and
     // in shared memory); x and its terms are dead now
-    const int n16 = T * k * KBi * (kHTermBytes + kHGroups * 4) / 16;
-    #pragma unroll 1
-    for (int j = tid; j < n16; j += kThreads)
+    const int n16h = T * k * KBi * (kHTermBytes + kHGroups * 4) / 16;
+#pragma unroll 1
+    for (int j = tid; j < n16h; j += kThreads)
       reinterpret_cast<uint4*>(hbs)[j] = __ldcg(reinterpret_cast<const uint4*>(a.h) + j);
     __syncthreads();
-    if (dn_staged) mbar_wait(dnbar, 0u, a.status);   // the down units are in shared memory
     // B columns of a down MMA: 4 groups of 8 features x 2 terms; lane (g, q)
     // holds the C columns of group q, so the quad sum adds the groups
     const int grp = g >> 1;
@@ -714,28 +706,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     for (int rb = 0; rb < n_dn; rb += kMaxDnItems) {
       const int round_end = min(n_dn, rb + kMaxDnItems);
       if (rb > 0) {
+        __syncthreads();
         dn_table(rb);
         __syncthreads();
-        if (!dn_staged && rb + warp < round_end)
-          load_batch(dcur, a.down + uint32_t(dtab[warp].x), 0, dtab[warp].y & 15, lane);
+#pragma unroll
+        for (int m = 0; m < kStageItems; ++m) dn_issue(rb, m);
       }
 #pragma unroll 1
-      for (int it = rb + warp; it < round_end; it += kWarps) {
+      for (int m = 0, it = rb + warp; it < round_end; ++m, it += kWarps) {
+        cp_async_wait<kStageItems - 1>();
+        __syncwarp();
+        const uint8_t* base = wb + (size_t)(m % kStageItems) * kItemBytes;
         const int meta = dtab[it - rb].y;
         const int kb0 = (meta >> 4) & 255, n = meta & 15, ai = meta >> 12;
-        if (dn_staged) {
-          // this item's units from shared memory: expert rank ai, tile it / per_tile
-          const uint8_t* base = dnw + (size_t)(ai * ntl + it / per_tile) * U_dn + (size_t)kb0 * kUnitBytes;
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const uint8_t* unit = base + (size_t)(u < n ? u : 0) * kUnitBytes;
-            dcur.w[u] = *reinterpret_cast<const uint2*>(unit + lane * 8);
-            dcur.s[u] = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          }
-        } else if (it + kWarps < round_end) {
-          const int2 nx = dtab[it + kWarps - rb];
-          load_batch(dnxt, a.down + uint32_t(nx.x), 0, nx.y & 15, lane);
-        }
         const int nt = act_n[ai];
         const int* slots = act_slot + ai * kDecodeMaxT;
         const int* toks = act_tok + ai * kDecodeMaxT;
@@ -752,10 +735,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           if (u < n) {
+            const uint8_t* unit = base + (size_t)u * kUnitBytes;
+            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
             const int kb = kb0 + u;
-            const float fwl = scale_lo(dcur.s[u]), fwh = scale_hi(dcur.s[u]);
-            const uint32_t a0 = decode_rowlo(dcur.w[u].x), a1 = decode_rowhi(dcur.w[u].x);
-            const uint32_t a2 = decode_rowlo(dcur.w[u].y), a3 = decode_rowhi(dcur.w[u].y);
+            const float fwl = scale_lo(sc), fwh = scale_hi(sc);
+            const uint32_t a0 = decode_rowlo(wv.x), a1 = decode_rowhi(wv.x);
+            const uint32_t a2 = decode_rowlo(wv.y), a3 = decode_rowhi(wv.y);
 #pragma unroll
             for (int si = 0; si < T; ++si) {
               if (T > 1 && si >= nt) continue;
@@ -773,6 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             }
           }
         }
+        __syncwarp();
+        dn_issue(rb, m + kStageItems);
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           float v0 = dacc[t][0], v1 = dacc[t][1];
@@ -786,26 +774,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
             o[8 + g] = v1;
           }
         }
-        if (!dn_staged) dcur = dnxt;
       }
+      cp_async_wait<0>();
       __syncthreads();
       // add this round's partials into the y accumulators, items in order
-      #pragma unroll 1
+#pragma unroll 1
       for (int j = tid; j < T * ntl * kTileRows; j += kThreads) {
         const int t = j / (ntl * kTileRows), r = j - t * (ntl * kTileRows);
         const int tl = r / kTileRows, rr = r - tl * kTileRows;
         const int lo = max(rb, tl * per_tile), hi = min(round_end, (tl + 1) * per_tile);
         float v = yacc[t * kYStride + r];
-        #pragma unroll 1
+#pragma unroll 1
         for (int it = lo; it < hi; ++it) v += dpart[(size_t)((it - rb) * T + t) * kTileRows + rr];
         yacc[t * kYStride + r] = v;
       }
-      __syncthreads();
     }
+    __syncthreads();
   } else {
+    cp_async_wait<0>();
     __syncthreads();
   }
-  #pragma unroll 1
+#pragma unroll 1
   for (int j = tid; j < T * ntl * kTileRows; j += kThreads) {
     const int t = j / (ntl * kTileRows), r = j - t * (ntl * kTileRows);
     a.y[(size_t)t * d + t0 * kTileRows + r] = __float2bfloat16_rn(yacc[t * kYStride + r]);
@@ -853,9 +842,7 @@ int decode_plan(const DecodeArgs& a, const DeviceInfo& di, uint32_t* smem_bytes)
 
 template <int T>
 int launch_decode_t(const DecodeArgs& a, uint32_t smem, const DeviceInfo& di, cudaStream_t s) {
-  Smem L = smem_plan(T, a.d, a.I, a.E, a.k, di.sm_count);
-  stage_down_units(L, a.I, di.smem_optin);
-  smem = L.total;
+  const Smem L = smem_plan(T, a.d, a.I, a.E, a.k, di.sm_count);
   MOE_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
   int per_sm = 0;
   MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T>, kThreads, smem));

@@ -30,6 +30,11 @@ enum QuantMode { kQuantMxfp8 = 0, kQuantSplit2 = 1 };
 int launch_act_quant(const void* src, bool src_bf16, int rows, int K, int mode, uint8_t* q, uint8_t* scales,
                      cudaStream_t s);
 
+// lmhead.cu: FP8 LM head (E4M3 rows with an fp32 scale per row)
+int launch_lm_pack(const void* w_bf16, int V, int d, uint8_t* codes, float* scales, cudaStream_t s);
+int launch_lm_gemv(const uint8_t* codes, const float* scales, int V, int d, const void* x_bf16, int T,
+                   float* logits, const DeviceInfo& di, cudaStream_t s);
+
 enum RoutedMode { kModeGateUp = 0, kModeDown = 1 };
 
 struct RoutedArgs {

@@ -11,9 +11,10 @@ Contents
   mxfp4  — E2M1/E8M0 decode and the MX quantisation rule (pack oracle)
   moe    — router logits, top-k + renormalised softmax, expert SwiGLU,
            shared expert, layer output, and the token->expert sort
-  mxfp8  — E4M3 activation quantisation for the W4A8 prefill mode
+  mxfp8  — E4M3 activation quantisation for the W4A8 mode
+  lmhead — the FP8 (per-row scale) LM-head GEMV
 
 Pin status of every function is listed in the module docstrings; none is
 "parity unpinned".
 """
-from . import mxfp4, moe, mxfp8  # noqa: F401
+from . import lmhead, mxfp4, moe, mxfp8  # noqa: F401
