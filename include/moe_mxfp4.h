@@ -370,7 +370,7 @@ int moe_lmhead_fp8(const uint8_t* codes_dev, const float* scales_dev, int V, int
  *     one stream or order them with events.
  *   - Returns MOE_ERR_WORKSPACE_TOO_SMALL, with nothing enqueued, when
  *     moe_workspace_bytes(&L->shape, T) > MOE_STATIC_SCRATCH_BYTES (at
- *     d = 2560, I = 768, E = 512, k = 8 that is T > 30). Larger calls need
+ *     d = 2560, I = 768, E = 512, k = 8 that is T > 26). Larger calls need
  *     moe_forward with a workspace of their own. */
 int moe_forward_static_scratch(const moe_layer* L, const void* x_dev, int T, void* y_dev,
                                const float* bias_dev, int bias_row_stride,

@@ -51,14 +51,14 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 32;
 constexpr int kThreads = kWarps * 32;
 constexpr int kU = 8;                // MXFP4 units a warp loads together
 constexpr int kRowVec = 10;          // 16-byte vectors of a bf16 row a lane loads together
 constexpr int kMaxGuItems = 96;      // gate/up (tile, K-range) items per round
 // items a warp keeps in flight (cp.async into its own shared-memory buffers):
 // 4 for one or two tokens, 2 when the activations need more shared memory
-__host__ __device__ constexpr int stage_items(int T) { return T <= 2 ? 4 : 2; }
+__host__ __device__ constexpr int stage_items(int T) { return T <= 2 ? 2 : 1; }
 constexpr uint32_t kItemBytes = kU * kUnitBytes;   // one item: kU units of a 16-row tile
 constexpr int kMaxDnItems = 64;      // down (tile, expert, K-range) items per round
 constexpr int kMergeChunks = 16;     // top-k: E <= 16 chunks of 32 experts
@@ -374,8 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   // ---- active experts (ascending) with their slots, and this CTA's gate/up
   // range, by warp 0 alone -----------------------------------------------------------
   if (warp == 0) {
-    // slot j = lane + 32 m holds expert ev[m]; every slot is compared with
-    // every other through shuffles (no shared-memory round trips)
+    // slot j = lane + 32 m holds expert ev[m]. Up to 32 slots (every decode
+    // shape with k <= 8): match_any gives each slot its expert's slot set
+    // (first occurrence, count, place), and one pass over the first
+    // occurrences gives the rank; larger T * k compares through shuffles.
     const int n = T * k;
     int ev[4], fst[4], rank[4], pos[4], cnt[4];
 #pragma unroll
@@ -385,38 +387,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       fst[m] = j < n ? 1 : 0;
       rank[m] = pos[m] = cnt[m] = 0;
     }
-    auto slot_e = [&](int i) {
-      const int a0 = __shfl_sync(0xFFFFFFFFu, ev[0], i & 31), a1 = __shfl_sync(0xFFFFFFFFu, ev[1], i & 31);
-      const int a2 = __shfl_sync(0xFFFFFFFFu, ev[2], i & 31), a3 = __shfl_sync(0xFFFFFFFFu, ev[3], i & 31);
-      return i < 32 ? a0 : (i < 64 ? a1 : (i < 96 ? a2 : a3));
-    };
+    int D = 0;
+    if (n <= 32) {
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, ev[0]);
+      const unsigned lt = (1u << lane) - 1u;
+      fst[0] = (lane < n && (peers & lt) == 0u) ? 1 : 0;
+      cnt[0] = __popc(peers);
+      pos[0] = __popc(peers & lt);
+      const unsigned firsts = __ballot_sync(0xFFFFFFFFu, fst[0] != 0);
+      D = __popc(firsts);
 #pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-      const int ei = slot_e(i);
+      for (unsigned f = firsts; f; f &= f - 1u) {
+        const int i = __ffs(f) - 1;
+        rank[0] += __shfl_sync(0xFFFFFFFFu, ev[0], i) < ev[0] ? 1 : 0;
+      }
+    } else {
+      auto slot_e = [&](int i) {
+        const int a0 = __shfl_sync(0xFFFFFFFFu, ev[0], i & 31), a1 = __shfl_sync(0xFFFFFFFFu, ev[1], i & 31);
+        const int a2 = __shfl_sync(0xFFFFFFFFu, ev[2], i & 31), a3 = __shfl_sync(0xFFFFFFFFu, ev[3], i & 31);
+        return i < 32 ? a0 : (i < 64 ? a1 : (i < 96 ? a2 : a3));
+      };
+#pragma unroll 1
+      for (int i = 0; i < n; ++i) {
+        const int ei = slot_e(i);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int j = lane + 32 * m;
-        if (ei == ev[m]) {
-          ++cnt[m];
-          if (i < j) {
-            ++pos[m];
-            fst[m] = 0;
+        for (int m = 0; m < 4; ++m) {
+          const int j = lane + 32 * m;
+          if (ei == ev[m]) {
+            ++cnt[m];
+            if (i < j) {
+              ++pos[m];
+              fst[m] = 0;
+            }
           }
         }
       }
-    }
-    // rank of an expert among the distinct ones: first occurrences of smaller ids
-    int D = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) D += __popc(__ballot_sync(0xFFFFFFFFu, fst[m] != 0));
+      for (int m = 0; m < 4; ++m) D += __popc(__ballot_sync(0xFFFFFFFFu, fst[m] != 0));
 #pragma unroll 1
-    for (int i = 0; i < n; ++i) {
-      const int ei = slot_e(i);
-      const int f0_ = __shfl_sync(0xFFFFFFFFu, fst[0], i & 31), f1_ = __shfl_sync(0xFFFFFFFFu, fst[1], i & 31);
-      const int f2_ = __shfl_sync(0xFFFFFFFFu, fst[2], i & 31), f3_ = __shfl_sync(0xFFFFFFFFu, fst[3], i & 31);
-      const int fi = i < 32 ? f0_ : (i < 64 ? f1_ : (i < 96 ? f2_ : f3_));
+      for (int i = 0; i < n; ++i) {
+        const int ei = slot_e(i);
+        const int f0_ = __shfl_sync(0xFFFFFFFFu, fst[0], i & 31), f1_ = __shfl_sync(0xFFFFFFFFu, fst[1], i & 31);
+        const int f2_ = __shfl_sync(0xFFFFFFFFu, fst[2], i & 31), f3_ = __shfl_sync(0xFFFFFFFFu, fst[3], i & 31);
+        const int fi = i < 32 ? f0_ : (i < 64 ? f1_ : (i < 96 ? f2_ : f3_));
 #pragma unroll
-      for (int m = 0; m < 4; ++m) rank[m] += (fi && ei < ev[m]) ? 1 : 0;
+        for (int m = 0; m < 4; ++m) rank[m] += (fi && ei < ev[m]) ? 1 : 0;
+      }
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {

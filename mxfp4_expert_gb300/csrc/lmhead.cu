@@ -25,7 +25,6 @@ namespace {
 
 constexpr int kLWarps = 16;
 constexpr int kLThreads = kLWarps * 32;
-constexpr int kLMaxT = 8;      // tokens per call
 constexpr int kLBatch = 8;     // K-blocks a lane loads together (16 bytes each)
 
 // per-row fp32 scale and E4M3 codes (quantisation of one bf16 row per block)

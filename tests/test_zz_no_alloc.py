@@ -70,16 +70,16 @@ def test_static_scratch_matches_moe_forward_twice(mx, name, T):
 
 
 def test_static_scratch_ling_limit(mx):
-    """At the Ling shape the 4 MiB array holds the workspace of up to 30
-    tokens: T = 30 runs (and matches moe_forward), T = 31 is refused with
+    """At the Ling shape the 4 MiB array holds the workspace of up to 26
+    tokens: T = 26 runs (and matches moe_forward), T = 27 is refused with
     MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued."""
     from mxfp4_expert_gb300 import synthetic
     w = wl.WORKLOADS["ling_t1"]
     layer = synthetic.build_layer(w, 0)
-    assert mx.moe_workspace_bytes(layer.shape, 30) <= mx.STATIC_SCRATCH_BYTES
-    assert mx.moe_workspace_bytes(layer.shape, 31) > mx.STATIC_SCRATCH_BYTES
-    _compare(mx, layer, _x(w, 0, 30), None, w)
-    x = _x(w, 1, 31)
+    assert mx.moe_workspace_bytes(layer.shape, 26) <= mx.STATIC_SCRATCH_BYTES
+    assert mx.moe_workspace_bytes(layer.shape, 27) > mx.STATIC_SCRATCH_BYTES
+    _compare(mx, layer, _x(w, 0, 26), None, w)
+    x = _x(w, 1, 27)
     y = torch.full_like(x, 7.0)
     with pytest.raises(mx.MoeError) as ei:
         mx.moe_forward_static_scratch(layer, x, y)
