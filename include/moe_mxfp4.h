@@ -70,30 +70,32 @@ typedef enum moe_dev_status {
 
 /* Packed layouts (byte formats of moe_pack_mxfp4's output).
  *
- * MOE_LAYOUT_MMA16: matrix W [N][K] (N % 16 == 0, K % 32 == 0) is cut into
+ * MOE_LAYOUT_TILE16: matrix W [N][K] (N % 16 == 0, K % 32 == 0) is cut into
  *   row tiles of 16 rows. For tile r (rows 16r..16r+15) and K-block b
  *   (columns 32b..32b+31) a 272-byte unit sits at byte (r*K/32 + b) * 272:
- *     bytes [0, 256): the 512 E2M1 codes, 8 bytes per lane l = 4g + q
- *       (g = l/4, q = l%4): word 0 holds rows g and g+8 at columns
- *       32b + 4q + (0..3), word 1 the same rows at columns 32b + 16 + 4q + (0..3).
- *       In byte j of a word, row g's code sits at bits {2: m, 3: e0, 4: e1,
- *       7: sign} and row g+8's at bits {0: m, 1: e0, 6: e1, 5: sign}; masking
- *       the first with 0x9C, or shifting the second into place, gives the
- *       code as an E4M3 byte worth 2^-6 times the E2M1 value.
- *     bytes [256, 272): scale bytes, row g at 256 + 2g, row g+8 at 257 + 2g.
+ *     bytes [0, 256): the 512 E2M1 codes, row-major: bytes [16i, 16i+16)
+ *       hold row 16r+i, columns 32b..32b+31, column 32b+2j in the low nibble
+ *       of byte j and 32b+2j+1 in its high nibble (the canonical MXFP4 byte
+ *       order). Each 8-byte half-row (16 codes) is the low half of one
+ *       16-byte chunk of the tensor cores' E2M1 operand form, and the
+ *       even/odd nibbles of a 4-byte word re-encode with two logic
+ *       operations as E4M3 bytes worth 2^-6 times the E2M1 value.
+ *     bytes [256, 272): scale bytes, row g at 256 + 2g, row g+8 at 257 + 2g
+ *       (g = 0..7).
+ *   A tile's units over all K are contiguous, and a matrix's tiles too.
  *   Bytes per matrix: N*K/2 + N*K/32 (exactly the MXFP4 payload).
- * MOE_LAYOUT_MMA16_GATEUP: the input matrix is a fused [2I][K] gate/up
+ * MOE_LAYOUT_TILE16_GATEUP: the input matrix is a fused [2I][K] gate/up
  *   projection (rows 0..I-1 gate, I..2I-1 up, I % 8 == 0). Packed tile r
  *   holds gate rows 8r..8r+7 as its rows 0..7 and up rows 8r..8r+7 as its
- *   rows 8..15; otherwise as MOE_LAYOUT_MMA16.
+ *   rows 8..15; otherwise as MOE_LAYOUT_TILE16.
  */
 typedef enum moe_layout {
-  MOE_LAYOUT_MMA16 = 1,
-  MOE_LAYOUT_MMA16_GATEUP = 2
+  MOE_LAYOUT_TILE16 = 1,
+  MOE_LAYOUT_TILE16_GATEUP = 2
 } moe_layout;
 
 #define MOE_PACK_MAGIC 0x3446584Du /* "MXF4" */
-#define MOE_PACK_VERSION 1u
+#define MOE_PACK_VERSION 2u
 
 /* Host-side descriptor of a packed weight buffer. moe_pack_mxfp4 fills it;
  * moe_forward refuses buffers whose descriptor does not match the layer
@@ -120,9 +122,9 @@ typedef struct moe_shape {
 typedef struct moe_layer {
   moe_shape shape;
   const void* router_w;        /* bf16 [E][d] row-major */
-  const void* gate_up;         /* packed, MOE_LAYOUT_MMA16_GATEUP, n_mat=E, N=2I, K=d */
+  const void* gate_up;         /* packed, MOE_LAYOUT_TILE16_GATEUP, n_mat=E, N=2I, K=d */
   moe_packed_desc gate_up_desc;
-  const void* down;            /* packed, MOE_LAYOUT_MMA16, n_mat=E, N=d, K=I */
+  const void* down;            /* packed, MOE_LAYOUT_TILE16, n_mat=E, N=d, K=I */
   moe_packed_desc down_desc;
   const void* shared_gate;     /* bf16 [I][d]  (unused if has_shared == 0) */
   const void* shared_up;       /* bf16 [I][d] */
@@ -392,7 +394,7 @@ int moe_selftest_bounded_wait(const uint32_t* flag_dev, uint32_t want, long long
 /* Static text for a moe_status value. */
 const char* moe_status_string(int status);
 
-/* Library version, e.g. "moe_mxfp4 1.1 sm_103a". */
+/* Library version, e.g. "moe_mxfp4 1.2 sm_103a". */
 const char* moe_version(void);
 
 #ifdef __cplusplus

@@ -14,7 +14,7 @@ import os
 import torch
 
 __all__ = [
-    "MoeError", "LIB_PATH", "lib", "MOE_LAYOUT_MMA16", "MOE_LAYOUT_MMA16_GATEUP",
+    "MoeError", "LIB_PATH", "lib", "MOE_LAYOUT_TILE16", "MOE_LAYOUT_TILE16_GATEUP",
     "MOE_PATH_DECODE_MMA", "MOE_PATH_DECODE_FUSED", "MOE_PATH_PREFILL_TC", "DEV_NONFINITE_INPUT", "DEV_SCALE_RANGE", "DEV_INDEX_OOB", "DEV_TIMEOUT",
     "moe_packed_desc", "moe_shape", "moe_layer", "Layer",
     "moe_packed_bytes", "moe_describe_packed", "moe_pack_mxfp4", "moe_unpack_mxfp4",
@@ -26,10 +26,10 @@ __all__ = [
 # another library.
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxfp4.so")
 # Version string the library must report (moe_version); anything else is refused.
-EXPECTED_VERSION = "moe_mxfp4 1.1 sm_103a"
+EXPECTED_VERSION = "moe_mxfp4 1.2 sm_103a"
 
-MOE_LAYOUT_MMA16 = 1
-MOE_LAYOUT_MMA16_GATEUP = 2
+MOE_LAYOUT_TILE16 = 1
+MOE_LAYOUT_TILE16_GATEUP = 2
 MOE_PATH_DECODE_MMA = 1
 MOE_PATH_DECODE_FUSED = 2
 MOE_PATH_PREFILL_TC = 3
@@ -237,8 +237,8 @@ def moe_stage_names(path: int) -> list[str]:
 class Layer:
     """Device weights of one layer plus the moe_layer struct the C ABI takes.
 
-    router_w bf16 [E, d]; gate_up packed (layout MMA16_GATEUP, n_mat=E, N=2I,
-    K=d); down packed (layout MMA16, n_mat=E, N=d, K=I); shared_* bf16 or None.
+    router_w bf16 [E, d]; gate_up packed (layout TILE16_GATEUP, n_mat=E, N=2I,
+    K=d); down packed (layout TILE16, n_mat=E, N=d, K=I); shared_* bf16 or None.
     """
 
     def __init__(self, router_w, gate_up, gate_up_desc, down, down_desc,
@@ -258,8 +258,8 @@ class Layer:
     @classmethod
     def from_fp32(cls, router_w, gate_up_f32, down_f32, shared=None, top_k=8, stream=None):
         """Pack fp32 expert weights (gate_up [E, 2I, d], down [E, d, I]) with moe_pack_mxfp4."""
-        gu, gud = moe_pack_mxfp4(gate_up_f32, MOE_LAYOUT_MMA16_GATEUP, stream=stream)
-        dn, dnd = moe_pack_mxfp4(down_f32, MOE_LAYOUT_MMA16, stream=stream)
+        gu, gud = moe_pack_mxfp4(gate_up_f32, MOE_LAYOUT_TILE16_GATEUP, stream=stream)
+        dn, dnd = moe_pack_mxfp4(down_f32, MOE_LAYOUT_TILE16, stream=stream)
         sg, su, sd = shared if shared is not None else (None, None, None)
         return cls(router_w, gu, gud, dn, dnd, sg, su, sd, top_k=top_k)
 

@@ -157,8 +157,8 @@ int validate_forward(const moe_layer* L, const void* x_dev, int T, const void* y
   MOE_CHECK_ARG(!sh.has_shared || (L->shared_gate && L->shared_up && L->shared_down), MOE_ERR_INVALID_ARG);
   MOE_CHECK_ARG(bias_row_stride == 0 || bias_row_stride >= E, MOE_ERR_INVALID_ARG);
   MOE_CHECK_ARG(x_dev != y_dev, MOE_ERR_INVALID_ARG);
-  MOE_CHECK_ARG(desc_matches(L->gate_up_desc, MOE_LAYOUT_MMA16_GATEUP, E, 2 * I, d), MOE_ERR_BAD_DESCRIPTOR);
-  MOE_CHECK_ARG(desc_matches(L->down_desc, MOE_LAYOUT_MMA16, E, d, I), MOE_ERR_BAD_DESCRIPTOR);
+  MOE_CHECK_ARG(desc_matches(L->gate_up_desc, MOE_LAYOUT_TILE16_GATEUP, E, 2 * I, d), MOE_ERR_BAD_DESCRIPTOR);
+  MOE_CHECK_ARG(desc_matches(L->down_desc, MOE_LAYOUT_TILE16, E, d, I), MOE_ERR_BAD_DESCRIPTOR);
   MOE_CHECK_ARG(aligned(L->gate_up, 16) && aligned(L->down, 16) && aligned(L->router_w, 16) &&
                     aligned(x_dev, 16) && aligned(workspace_dev, 256),
                 MOE_ERR_INVALID_ARG);
@@ -541,7 +541,7 @@ extern "C" const char* moe_status_string(int status) {
   }
 }
 
-extern "C" const char* moe_version(void) { return "moe_mxfp4 1.1 sm_103a"; }
+extern "C" const char* moe_version(void) { return "moe_mxfp4 1.2 sm_103a"; }
 
 namespace moe {
 namespace {

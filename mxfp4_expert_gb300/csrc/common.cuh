@@ -108,13 +108,33 @@ __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// Packed code word -> two e4m3x4 registers (each byte = 2^-6 * E2M1 value).
-// Row-g codes sit at bits {2,3,4,7} of every byte, row-(g+8) codes at
-// {0,1,6,5} (m, e0, e1, sign); see the layout in moe_mxfp4.h.
-__device__ __forceinline__ uint32_t decode_rowlo(uint32_t w) { return w & 0x9C9C9C9Cu; }
-__device__ __forceinline__ uint32_t decode_rowhi(uint32_t w) {
-  return ((w << 2) & 0x8C8C8C8Cu) | ((w >> 2) & 0x10101010u);
+// A 4-byte word of a packed unit row (8 E2M1 codes, code 2j in the low nibble
+// of byte j) -> two e4m3x4 registers, each byte worth 2^-6 times the E2M1
+// value (sign to bit 7, the 3 exponent/mantissa bits to bits 2..4; the E2M1
+// subnormal lands on the E4M3 subnormal). dec_even: codes 0, 2, 4, 6 of the
+// word; dec_odd: codes 1, 3, 5, 7.
+__device__ __forceinline__ uint32_t dec_even(uint32_t w) {
+  return ((w << 4) & 0x80808080u) | ((w << 2) & 0x1C1C1C1Cu);
 }
+__device__ __forceinline__ uint32_t dec_odd(uint32_t w) { return (w & 0x80808080u) | ((w >> 2) & 0x1C1C1C1Cu); }
+
+// The warp MMA's A fragment from packed unit rows. Lane (g, q) reads bytes
+// [4q, 4q+4) of rows g and g+8 (codes 8q..8q+7) and hands the even codes to MMA
+// K positions 4q..4q+3 and the odd ones to 16+4q..16+4q+3. K is thereby
+// permuted inside each 32-block: MMA position 4q+j <-> code 8q+2j and
+// 16+4q+j <-> 8q+2j+1. B operands are stored in the same permuted order
+// (bfrag_pos), so every product pairs the right elements.
+struct AFrag {
+  uint32_t a0, a1, a2, a3;
+};
+__device__ __forceinline__ AFrag load_afrag(const uint8_t* unit, int g, int q) {
+  const uint32_t w0 = *reinterpret_cast<const uint32_t*>(unit + g * 16 + 4 * q);
+  const uint32_t w1 = *reinterpret_cast<const uint32_t*>(unit + (g + 8) * 16 + 4 * q);
+  return AFrag{dec_even(w0), dec_even(w1), dec_odd(w0), dec_odd(w1)};
+}
+// Byte position of element e (0..31) of a 32-element B column block, so that
+// lane q of a quad reads its fragment (b0, b1) as bytes [8q, 8q+8).
+__device__ __forceinline__ int bfrag_pos(int e) { return (e & 24) + ((e & 1) << 2) + ((e >> 1) & 3); }
 
 // fp32 pair -> e4m3x2 (round to nearest even, saturating to +-448); low byte = lo.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {

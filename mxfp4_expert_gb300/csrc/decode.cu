@@ -371,6 +371,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     }
   }
   __syncthreads();
+  // ---- gate/up matrices of the selected experts into L2 at once: the
+  // concatenation of the distinct experts' matrices (first-occurrence order)
+  // cut into G equal slices, slice c prefetched by this CTA, lane r taking
+  // its part of the r-th matrix (up to 32 selections; larger T * k leaves the
+  // prefetch to the per-tile one below)
+  const bool early_pf = T * k <= 32;
+  if (warp == 1 && early_pf) {
+    const int n = T * k;
+    const int ev = lane < n ? sel_e[lane] : -1 - lane;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, ev);
+    const bool first = lane < n && (peers & ((1u << lane) - 1u)) == 0u;
+    const unsigned firsts = __ballot_sync(0xFFFFFFFFu, first);
+    if (first) {
+      const uint64_t m = a.gu_mat, S = (uint64_t)__popc(firsts) * m;
+      const uint64_t lo = (S * (uint64_t)c / (uint64_t)G) & ~uint64_t(15);
+      const uint64_t hi = c + 1 == G ? S : (S * (uint64_t)(c + 1) / (uint64_t)G) & ~uint64_t(15);
+      const uint64_t r0m = (uint64_t)__popc(firsts & ((1u << lane) - 1u)) * m;
+      const uint64_t b0 = lo > r0m ? lo : r0m, b1 = hi < r0m + m ? hi : r0m + m;
+      if (b1 > b0) prefetch_range(a.gate_up + (size_t)ev * m + (b0 - r0m), uint32_t(b1 - b0));
+    }
+  }
   // ---- active experts (ascending) with their slots, and this CTA's gate/up
   // range, by warp 0 alone -----------------------------------------------------------
   if (warp == 0) {
@@ -475,12 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   __syncthreads();
   const int D = misc[0], i0 = misc[1], i1 = misc[2] > misc[1] ? misc[2] : misc[1];
 
-  // this CTA's gate/up tiles (one prefetch per tile) and the down units of its
-  // output tiles for every active expert (one prefetch per expert) into L2,
-  // spread over the warps
+  // this CTA's gate/up tiles (one prefetch per tile, unless the slices above
+  // covered them) and the down units of its output tiles for every active
+  // expert (one prefetch per expert) into L2, spread over the warps
   if (lane == 0) {
 #pragma unroll 1
-    for (int gt = i0 + warp; gt < i1; gt += kWarps) {
+    for (int gt = i0 + warp; !early_pf && gt < i1; gt += kWarps) {
       const int ai = gt / NTg;
       prefetch_l2(a.gate_up + (size_t)act[ai] * a.gu_mat + (size_t)(gt - ai * NTg) * U_gu, U_gu);
     }
@@ -489,6 +510,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       for (int ai = kWarps - 1 - warp; ai < D; ai += kWarps)
         prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
   }
+  // down items (output tile, active expert, K-range of kU units), in rounds
+  // of kMaxDnItems; the first round's table is built now, its copies are
+  // issued as soon as this CTA's gate/up is done
+  // units per item: up to kU, fewer when that gives every warp one item
+  const int uD = D * ntl > 0 ? min(kU, ceil_div(KBi, max(1, kWarps / (D * ntl)))) : kU;
+  const int KPD = ceil_div(KBi, uD);
+  const int per_tile = D * KPD;
+  const int n_dn = ntl * per_tile;
+  // item j: byte offset of its first unit, (expert rank << 12 | kb0 << 4 | n)
+  auto dn_table = [&](int rb) {
+#pragma unroll 1
+    for (int j = tid; j < min(kMaxDnItems, n_dn - rb); j += kThreads) {
+      const int it = rb + j, tl = it / per_tile, rem = it - tl * per_tile, ai = rem / KPD;
+      const int kb = (rem - ai * KPD) * uD;
+      dtab[j] = make_int2(int(act[ai] * a.dn_mat + (uint64_t)(t0 + tl) * U_dn + (uint64_t)kb * kUnitBytes),
+                          (ai << 12) | (kb << 4) | min(uD, KBi - kb));
+    }
+  };
+  auto dn_issue = [&](int rb, int m) {   // this warp's m-th item of the round starting at rb
+    const int it = rb + warp + m * kWarps;
+    if (it < min(n_dn, rb + kMaxDnItems)) {
+      const int2 e = dtab[it - rb];
+      const uint8_t* src = a.down + uint32_t(e.x);
+      uint8_t* dst = wb + (size_t)(m % kStageItems) * kItemBytes;
+      const int n16 = (e.y & 15) * (kUnitBytes / 16);
+#pragma unroll 1
+      for (int c = lane; c < n16; c += 32) cp_async16(dst + c * 16, src + c * 16);
+    }
+    cp_async_commit();
+  };
+  dn_table(0);
+  if (i1 == i0) __syncthreads();   // otherwise the gate/up round barrier orders it
+
   // ---- 3. routed gate/up: items (tile, K-range of kU units), item j of a round
   // on warp j % kWarps; every warp keeps kStageItems items in flight, copied
   // with cp.async into its own shared-memory buffers. The warp that finishes a
@@ -552,19 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
         for (int u = 0; u < kU; ++u) {
           if (u < n) {
             const uint8_t* unit = base + (size_t)u * kUnitBytes;
-            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const AFrag af = load_afrag(unit, g, q);
             const uint32_t sc = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
             const int kb = kb0 + u;
             const float fwl = scale_lo(sc), fwh = scale_hi(sc);
-            const uint32_t a0 = decode_rowlo(wv.x), a1 = decode_rowhi(wv.x);
-            const uint32_t a2 = decode_rowlo(wv.y), a3 = decode_rowhi(wv.y);
 #pragma unroll
             for (int p = 0; p < kPairs; ++p) {
               const uint2 bv = boff[p] >= 0 ? *reinterpret_cast<const uint2*>(xb + boff[p] + kb * kActRowKbBytes)
                                             : make_uint2(0u, 0u);
               const float fa = foff[p] >= 0 ? xfa[foff[p] + kb] : 0.0f;
               float dd[4];
-              mma_e4m3(dd, a0, a1, a2, a3, bv.x, bv.y);
+              mma_e4m3(dd, af.a0, af.a1, af.a2, af.a3, bv.x, bv.y);
               acc[p][0] = fmaf((dd[0] + dd[1]) * fa, fwl, acc[p][0]);
               acc[p][1] = fmaf((dd[2] + dd[3]) * fa, fwh, acc[p][1]);
             }
@@ -618,7 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
               const int scol = 2 * p + (lane & 1);
               if (lane < 16 && scol < nt) {
                 const int slx = slots[scol];
-                const size_t base_h = ((size_t)slx * KBi + kbh) * kHTermBytes + grp * 8 + (lane >> 1);
+                // feature 8 grp + (lane >> 1) of K-block kbh, at its B-fragment position
+                const size_t base_h = ((size_t)slx * KBi + kbh) * kHTermBytes + bfrag_pos(grp * 8 + (lane >> 1));
                 hT[base_h] = uint8_t(e0);
                 hT[base_h + 32] = uint8_t(e1);
                 if ((lane >> 1) == 0) hF[((size_t)slx * KBi + kbh) * kHGroups + grp] = act_factor(ex, sel_w[slx]);
@@ -631,45 +684,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       __syncthreads();
     }
   }
-  // this CTA's h is written: publish (the last warp; the others go on)
-  if (warp == kWarps - 1 && lane == 0) red_release_add(&st->gudone, 1u);
-
-  // ---- 4./5. down: items (output tile, active expert, K-range of kU units),
-  // item j of a round on warp j % kWarps, copied from L2 (prefetched during
-  // gate/up) into the warp's buffers before the wait for every CTA's h; the
-  // shared-down rows run while the other CTAs finish their gate/up -------------------
-  const int KPD = ceil_div(KBi, kU);
-  const int per_tile = D * KPD;
-  const int n_dn = ntl * per_tile;
-  // item j: byte offset of its first unit, (expert rank << 12 | kb0 << 4 | n)
-  auto dn_table = [&](int rb) {
-#pragma unroll 1
-    for (int j = tid; j < min(kMaxDnItems, n_dn - rb); j += kThreads) {
-      const int it = rb + j, tl = it / per_tile, rem = it - tl * per_tile, ai = rem / KPD;
-      const int kb = (rem - ai * KPD) * kU;
-      dtab[j] = make_int2(int(act[ai] * a.dn_mat + (uint64_t)(t0 + tl) * U_dn + (uint64_t)kb * kUnitBytes),
-                          (ai << 12) | (kb << 4) | min(kU, KBi - kb));
-    }
-  };
-  auto dn_issue = [&](int rb, int m) {   // this warp's m-th item of the round starting at rb
-    const int it = rb + warp + m * kWarps;
-    if (it < min(n_dn, rb + kMaxDnItems)) {
-      const int2 e = dtab[it - rb];
-      const uint8_t* src = a.down + uint32_t(e.x);
-      uint8_t* dst = wb + (size_t)(m % kStageItems) * kItemBytes;
-      const int n16 = (e.y & 15) * (kUnitBytes / 16);
-#pragma unroll 1
-      for (int c = lane; c < n16; c += 32) cp_async16(dst + c * 16, src + c * 16);
-    }
-    cp_async_commit();
-  };
-  dn_table(0);
-  __syncthreads();
+  // the first down items into each warp's (now free) buffers, then this CTA's
+  // h is written: publish (the last warp; the others go on)
 #pragma unroll
   for (int m = 0; m < kStageItems; ++m) dn_issue(0, m);
+  if (warp == kWarps - 1 && lane == 0) red_release_add(&st->gudone, 1u);
 
+  // ---- 4. shared-down rows of this CTA's output tiles while the other CTAs
+  // finish their gate/up
   if (a.has_shared && ntl > 0) {
-    #pragma unroll 1
+#pragma unroll 1
     for (int j = tid; j < T * I; j += kThreads) hsh[j] = __ldcg(a.h_sh + j);
     __syncthreads();
     const int n8 = I / 8;
@@ -704,6 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     }
   }
 
+  // ---- 5. down: item j of a round on warp j % kWarps, copied from L2
+  // (prefetched during gate/up) into the warp's buffers before the wait for
+  // every CTA's h -----------------------------------------------------------------------
+
   if (n_dn > 0) {
     if (tid == 0) wait_geq_u32(&st->gudone, uint32_t(G), a.status);
     __syncthreads();
@@ -714,10 +742,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
     for (int j = tid; j < n16h; j += kThreads)
       reinterpret_cast<uint4*>(hbs)[j] = __ldcg(reinterpret_cast<const uint4*>(a.h) + j);
     __syncthreads();
-    // B columns of a down MMA: 4 groups of 8 features x 2 terms; lane (g, q)
-    // holds the C columns of group q, so the quad sum adds the groups
-    const int grp = g >> 1;
-    const bool lo_ok = grp == (q >> 1), hi_ok = grp == 2 + (q >> 1);
+    // B columns of a down MMA: 4 groups of 8 features x 2 terms (column g =
+    // group g / 2, term g % 2). Lane (g, q) supplies MMA K positions whose
+    // elements (8q + 0..7, see load_afrag) all lie in group q, so its B words
+    // are nonzero only for column group q; it holds the C columns of group q,
+    // and the quad sum adds the groups.
+    const bool grp_ok = (g >> 1) == q;
 #pragma unroll 1
     for (int rb = 0; rb < n_dn; rb += kMaxDnItems) {
       const int round_end = min(n_dn, rb + kMaxDnItems);
@@ -743,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
 #pragma unroll
         for (int si = 0; si < T; ++si) {
           const int sl = si < nt ? slots[si] : 0;
-          hbo[si] = sl * KBi * kHTermBytes + (g & 1) * 32 + 4 * q + (grp == (q >> 1) ? 0 : 16);
+          hbo[si] = sl * KBi * kHTermBytes + (g & 1) * 32 + 8 * q;
           hfo[si] = sl * KBi * kHGroups + q;
           tok[si] = si < nt ? toks[si] : -1;
           dacc[si][0] = dacc[si][1] = 0.0f;
@@ -752,19 +782,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
         for (int u = 0; u < kU; ++u) {
           if (u < n) {
             const uint8_t* unit = base + (size_t)u * kUnitBytes;
-            const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+            const AFrag af = load_afrag(unit, g, q);
             const uint32_t sc = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
             const int kb = kb0 + u;
             const float fwl = scale_lo(sc), fwh = scale_hi(sc);
-            const uint32_t a0 = decode_rowlo(wv.x), a1 = decode_rowhi(wv.x);
-            const uint32_t a2 = decode_rowlo(wv.y), a3 = decode_rowhi(wv.y);
 #pragma unroll
             for (int si = 0; si < T; ++si) {
               if (T > 1 && si >= nt) continue;
-              const uint32_t bw = *reinterpret_cast<const uint32_t*>(hbs + hbo[si] + kb * kHTermBytes);
+              const uint2 bw = grp_ok ? *reinterpret_cast<const uint2*>(hbs + hbo[si] + kb * kHTermBytes)
+                                      : make_uint2(0u, 0u);
               const float fa = hfa[hfo[si] + kb * kHGroups];
               float dd[4];
-              mma_e4m3(dd, a0, a1, a2, a3, lo_ok ? bw : 0u, hi_ok ? bw : 0u);
+              mma_e4m3(dd, af.a0, af.a1, af.a2, af.a3, bw.x, bw.y);
               const float vlo = (dd[0] + dd[1]) * fa * fwl;
               const float vhi = (dd[2] + dd[3]) * fa * fwh;
 #pragma unroll
@@ -793,16 +822,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       }
       cp_async_wait<0>();
       __syncthreads();
-      // add this round's partials into the y accumulators, items in order
+      // add this round's partials into the y accumulators: one warp per
+      // output, lane i taking items i, i + 32 (fixed order, tree sum)
 #pragma unroll 1
-      for (int j = tid; j < T * ntl * kTileRows; j += kThreads) {
+      for (int j = warp; j < T * ntl * kTileRows; j += kWarps) {
         const int t = j / (ntl * kTileRows), r = j - t * (ntl * kTileRows);
         const int tl = r / kTileRows, rr = r - tl * kTileRows;
         const int lo = max(rb, tl * per_tile), hi = min(round_end, (tl + 1) * per_tile);
-        float v = yacc[t * kYStride + r];
+        float v = 0.0f;
 #pragma unroll 1
-        for (int it = lo; it < hi; ++it) v += dpart[(size_t)((it - rb) * T + t) * kTileRows + rr];
-        yacc[t * kYStride + r] = v;
+        for (int it = lo + lane; it < hi; it += 32) v += dpart[(size_t)((it - rb) * T + t) * kTileRows + rr];
+        v = warp_sum(v);
+        if (lane == 0) yacc[t * kYStride + r] += v;
       }
     }
     __syncthreads();

@@ -17,7 +17,7 @@
 // one is multiplied.
 //
 // In the first kernel the shared gate and up rows are interleaved 8 + 8 per
-// 16-row tile (the MMA16_GATEUP idea), so one lane holds gate and up of the
+// 16-row tile (as the TILE16_GATEUP weight layout does), so one lane holds gate and up of the
 // same feature for the SwiGLU. The shared down projection reads h_sh (fp32)
 // as two bf16 terms, hi = bf16(h) and lo = bf16(h - hi), about 16 significant
 // bits, with one MMA per term.

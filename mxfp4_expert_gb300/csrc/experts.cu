@@ -117,7 +117,7 @@ __device__ __forceinline__ void routed_tile(const uint8_t* st, const uint8_t* bs
       const bool in = kb < KB;
       const int kc = in ? kb : KB - 1;
       const uint8_t* unit = st + (size_t)kc * kUnitBytes;
-      const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
+      const AFrag af = load_afrag(unit, g, q);
       const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
       const float fwl = in ? wscale_lo(sc16) : 0.0f, fwh = in ? wscale_hi(sc16) : 0.0f;
 #pragma unroll
@@ -126,7 +126,7 @@ __device__ __forceinline__ void routed_tile(const uint8_t* st, const uint8_t* bs
                                       : make_uint2(0u, 0u);
         const float fa = est[erow[p] + kc];
         float d[4];
-        mma_e4m3(d, decode_rowlo(wv.x), decode_rowhi(wv.x), decode_rowlo(wv.y), decode_rowhi(wv.y), bv.x, bv.y);
+        mma_e4m3(d, af.a0, af.a1, af.a2, af.a3, bv.x, bv.y);
         acc[p][0] = fmaf((d[0] + d[1]) * fa, fwl, acc[p][0]);
         acc[p][1] = fmaf((d[2] + d[3]) * fa, fwh, acc[p][1]);
       }

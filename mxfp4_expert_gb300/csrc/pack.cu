@@ -1,4 +1,4 @@
-// MXFP4 packing: fp32 weights -> E2M1 codes + E8M0 scales in the MMA16 tile
+// MXFP4 packing: fp32 weights -> E2M1 codes + E8M0 scales in the TILE16
 // layout (include/moe_mxfp4.h), and the inverse permutation to the canonical
 // layout for tests.
 //
@@ -15,23 +15,11 @@ namespace {
 
 // Source row of packed row r (0..15) of tile `tile`.
 __device__ __forceinline__ int source_row(int layout, int tile, int r, int N) {
-  if (layout == MOE_LAYOUT_MMA16_GATEUP) {
+  if (layout == MOE_LAYOUT_TILE16_GATEUP) {
     const int I = N / 2;
     return r < 8 ? tile * 8 + r : I + tile * 8 + (r - 8);
   }
   return tile * kTileRows + r;
-}
-
-// E2M1 code bits (m, e0, e1, sign) -> position in a packed byte.
-__device__ __forceinline__ uint32_t place_rowlo(uint32_t c) {   // bits 2,3,4,7
-  return ((c & 7u) << 2) | ((c & 8u) << 4);
-}
-__device__ __forceinline__ uint32_t place_rowhi(uint32_t c) {   // bits 0,1,6,5
-  return (c & 3u) | ((c & 4u) << 4) | ((c & 8u) << 2);
-}
-__device__ __forceinline__ uint32_t take_rowlo(uint32_t b) { return ((b >> 2) & 7u) | ((b >> 4) & 8u); }
-__device__ __forceinline__ uint32_t take_rowhi(uint32_t b) {
-  return (b & 3u) | ((b >> 4) & 4u) | ((b >> 2) & 8u);
 }
 
 // Nearest E2M1 magnitude code for |q| < 8, ties to even (codes 0, 2, 4, 6
@@ -46,10 +34,10 @@ constexpr int kPackWarps = 8;
 __global__ void __launch_bounds__(kPackWarps * 32)
 pack_kernel(const float* __restrict__ w, uint8_t* __restrict__ packed, int n_mat, int N, int K,
             int layout, int* status) {
-  __shared__ uint8_t codes_sm[kPackWarps][kTileRows][kMxBlock];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KB = K / kMxBlock, NT = N / kTileRows;
   const long long units = (long long)n_mat * NT * KB;
+  // lane = 2 r + hh: row r of the unit, elements 16 hh .. 16 hh + 15 of its K-block
   const int r = lane >> 1, hh = lane & 1;
   for (long long u = (long long)blockIdx.x * kPackWarps + warp; u < units;
        u += (long long)gridDim.x * kPackWarps) {
@@ -80,43 +68,33 @@ pack_kernel(const float* __restrict__ w, uint8_t* __restrict__ packed, int n_mat
     const uint32_t ebits = __float_as_uint(amax) >> 23;
     int s = amax == 0.0f ? 0 : max(int(ebits) - 2, 0);
     const float inv_x = exp2i(127 - s);   // exact power of two
+    uint32_t wd[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const bool fin = isfinite(v[i]);
       const float q = fin ? v[i] * inv_x : 0.0f;
       uint32_t c = e2m1_magnitude(fabsf(q));
       c |= (fin && signbit(v[i])) ? 8u : 0u;
-      codes_sm[warp][r][hh * 16 + i] = uint8_t(c);
+      wd[i >> 3] |= c << (4 * (i & 7));   // element 2j in the low nibble of byte j
     }
     if (bad && hh == 0 && status) atomicOr(status, MOE_DEV_NONFINITE_INPUT);
     if (!bad && s > 248 && hh == 0 && status) atomicOr(status, MOE_DEV_SCALE_RANGE);
-    __syncwarp();
-    // assemble this lane's 8 packed bytes: lane = 4g + q
-    const int g = lane >> 2, q = lane & 3;
-    uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int k0 = 4 * q + j, k1 = 16 + 4 * q + j;
-      w0 |= (place_rowlo(codes_sm[warp][g][k0]) | place_rowhi(codes_sm[warp][g + 8][k0])) << (8 * j);
-      w1 |= (place_rowlo(codes_sm[warp][g][k1]) | place_rowhi(codes_sm[warp][g + 8][k1])) << (8 * j);
-    }
     uint8_t* unit = packed + ((long long)mat * NT * KB + (long long)tile * KB + kb) * kUnitBytes;
-    reinterpret_cast<uint2*>(unit)[lane] = make_uint2(w0, w1);
+    *reinterpret_cast<uint2*>(unit + r * 16 + hh * 8) = make_uint2(wd[0], wd[1]);
     if (hh == 0) {
       const int pos = r < 8 ? 2 * r : 2 * (r - 8) + 1;
       unit[kUnitCodeBytes + pos] = bad ? uint8_t(255) : uint8_t(s);
     }
-    __syncwarp();
   }
 }
 
 __global__ void __launch_bounds__(kPackWarps * 32)
 unpack_kernel(const uint8_t* __restrict__ packed, uint8_t* __restrict__ codes,
               uint8_t* __restrict__ scales, int n_mat, int N, int K, int layout) {
-  __shared__ uint8_t codes_sm[kPackWarps][kTileRows][kMxBlock];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int KB = K / kMxBlock, NT = N / kTileRows;
   const long long units = (long long)n_mat * NT * KB;
+  const int r = lane >> 1, half = lane & 1;
   for (long long u = (long long)blockIdx.x * kPackWarps + warp; u < units;
        u += (long long)gridDim.x * kPackWarps) {
     const int kb = int(u % KB);
@@ -124,38 +102,26 @@ unpack_kernel(const uint8_t* __restrict__ packed, uint8_t* __restrict__ codes,
     const int tile = int(mt % NT);
     const int mat = int(mt / NT);
     const uint8_t* unit = packed + ((long long)mat * NT * KB + (long long)tile * KB + kb) * kUnitBytes;
-    const uint2 wv = reinterpret_cast<const uint2*>(unit)[lane];
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t b0 = (wv.x >> (8 * j)) & 0xFFu, b1 = (wv.y >> (8 * j)) & 0xFFu;
-      codes_sm[warp][g][4 * q + j] = uint8_t(take_rowlo(b0));
-      codes_sm[warp][g + 8][4 * q + j] = uint8_t(take_rowhi(b0));
-      codes_sm[warp][g][16 + 4 * q + j] = uint8_t(take_rowlo(b1));
-      codes_sm[warp][g + 8][16 + 4 * q + j] = uint8_t(take_rowhi(b1));
-    }
-    __syncwarp();
-    // canonical: row r, 16 bytes per K-block, element 2j in the low nibble
-    const int r = lane >> 1, half = lane & 1;
+    // a unit row is the canonical row's 16 bytes of this K-block
     const int srow = source_row(layout, tile, r, N);
+    const uint2 v = *reinterpret_cast<const uint2*>(unit + r * 16 + half * 8);
     uint8_t* dst = codes + ((long long)mat * N + srow) * (K / 2) + (long long)kb * 16 + half * 8;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = half * 16 + 2 * j;
-      dst[j] = uint8_t(codes_sm[warp][r][e] | (codes_sm[warp][r][e + 1] << 4));
+    for (int j = 0; j < 4; ++j) {
+      dst[j] = uint8_t(v.x >> (8 * j));
+      dst[4 + j] = uint8_t(v.y >> (8 * j));
     }
     if (half == 0) {
       const int pos = r < 8 ? 2 * r : 2 * (r - 8) + 1;
       scales[((long long)mat * N + srow) * KB + kb] = unit[kUnitCodeBytes + pos];
     }
-    __syncwarp();
   }
 }
 
 bool shape_ok(int n_mat, int N, int K, int layout) {
   if (n_mat < 1 || N < kTileRows || K < kMxBlock) return false;
   if (N % kTileRows || K % kMxBlock) return false;
-  if (layout != MOE_LAYOUT_MMA16 && layout != MOE_LAYOUT_MMA16_GATEUP) return false;
+  if (layout != MOE_LAYOUT_TILE16 && layout != MOE_LAYOUT_TILE16_GATEUP) return false;
   return true;
 }
 
@@ -193,7 +159,7 @@ extern "C" int moe_pack_mxfp4(const float* w_dev, int n_mat, int N, int K, int l
                               void* packed_dev, size_t packed_bytes, moe_packed_desc* desc_out,
                               int* dev_status, moe_stream_t stream) {
   MOE_CHECK_ARG(w_dev && packed_dev, MOE_ERR_INVALID_ARG);
-  MOE_CHECK_ARG(layout == MOE_LAYOUT_MMA16 || layout == MOE_LAYOUT_MMA16_GATEUP, MOE_ERR_INVALID_ARG);
+  MOE_CHECK_ARG(layout == MOE_LAYOUT_TILE16 || layout == MOE_LAYOUT_TILE16_GATEUP, MOE_ERR_INVALID_ARG);
   MOE_CHECK_ARG(shape_ok(n_mat, N, K, layout), MOE_ERR_UNSUPPORTED_SHAPE);
   MOE_CHECK_ARG(aligned(w_dev, 16) && aligned(packed_dev, 16), MOE_ERR_INVALID_ARG);
   moe_packed_desc d;

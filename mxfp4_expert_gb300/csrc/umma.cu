@@ -3,26 +3,28 @@
 // and down.
 //
 // Every MMA is tcgen05.mma.kind::mxf8f6f4.block_scale: A = 128 weight rows x
-// K 32 as E4M3 codes, B = activation rows x K 32 as E4M3 codes, each with one
+// K 32 as E2M1 codes, B = activation rows x K 32 as E4M3 codes, each with one
 // E8M0 scale per row and 32-wide K-block, read by the tensor core from tensor
-// memory; fp32 accumulation in tensor memory. The MXFP4 weights enter exactly:
-// an E2M1 code re-encoded as E4M3 is 2^-6 times its value (E2M1's subnormal
-// maps onto E4M3's), so the A scale byte is the block's E8M0 scale + 6. The
-// activations arrive pre-quantised (quant.cu): MXFP8 for the 8-bit-activation
-// call, or two E4M3 terms sharing one E8M0 scale (bf16 precision), which the
-// MMA reads as separate B rows and the epilogue adds.
+// memory; fp32 accumulation in tensor memory. The MXFP4 weights enter as they
+// are stored: the tensor cores read E2M1 from 16-byte chunks whose low 8 bytes
+// hold 16 codes (the packed layout's half-rows), and the A scale bytes are the
+// packed E8M0 bytes. The activations arrive pre-quantised (quant.cu): MXFP8
+// for the 8-bit-activation call, or two E4M3 terms sharing one E8M0 scale
+// (bf16 precision), which the MMA reads as separate B rows and the epilogue
+// adds.
 //
 // Work items are (active expert, block of 128 weight rows = 8 packed 16-row
 // tiles, block of up to 128 B rows of that expert's tokens / slots), split
 // into contiguous ranges per CTA (one CTA per SM, persistent). Along K an
-// item goes in slices of four 32-wide K-blocks (one 128-byte swizzle row of
-// E4M3). The CTA is a pipeline of warp roles that meet only at mbarriers:
+// item goes in slices of four 32-wide K-blocks (one 128-byte swizzle row).
+// The CTA is a pipeline of warp roles that meet only at mbarriers:
 //   * producer (one thread): 1-D bulk copies of the packed MXFP4 bytes of a
 //     chunk of 2 slices (one copy per tile) into a ring of raw slots; whole
 //     items are also prefetched into L2 about 8 chunks ahead;
-//   * 16 decode warps (two per tile): raw slot -> E4M3 codes (two logic
-//     operations per 4 codes) in the K-major 128-byte-swizzled layout the MMA
-//     reads, and the A scale bytes in the layout tcgen05.cp copies;
+//   * 16 placement warps (two per tile): raw slot -> the half-rows of codes
+//     in the K-major 128-byte-swizzled layout the MMA reads (one 8-byte load
+//     and store per lane and unit, no arithmetic), and the A scale bytes in
+//     the layout tcgen05.cp copies;
 //   * 4 loader warps: the slice of the activation rows (x gathered by token,
 //     or h by slot; each term a block of B rows) copied with cp.async, and
 //     their B scale bytes; a loader announces slice p once its copies have
@@ -49,8 +51,8 @@ namespace moe {
 namespace {
 
 constexpr int kURows = 128;                  // weight rows per item (MMA M)
-constexpr int kUTiles = kURows / kTileRows;  // packed tiles per item (one per decode warp pair)
-constexpr int kUSliceKb = 4;                 // 32-wide K-blocks per slice: one 128-byte row of E4M3
+constexpr int kUTiles = kURows / kTileRows;  // packed tiles per item (one per placement warp pair)
+constexpr int kUSliceKb = 4;                 // 32-wide K-blocks per slice: one 128-byte swizzle row
 constexpr int kUSliceK = kUSliceKb * kMxBlock;
 constexpr int kUStages = 4;                  // operand stages (weights + activations + scales)
 constexpr int kUChunk = 2;                   // slices per raw weight copy
@@ -66,7 +68,7 @@ constexpr int kUMaxActive = 1024;
 constexpr int kUTable = 256;                 // items per CTA with a precomputed table entry
 constexpr uint32_t kUTileChunk = kUChunk * kUSliceKb * kUnitBytes;   // one tile's part of a chunk
 constexpr uint32_t kURawBytes = kUTiles * kUTileChunk;                  // one chunk of packed weights
-constexpr uint32_t kUABytes = kURows * kUSliceK;                     // one slice of E4M3 weights
+constexpr uint32_t kUABytes = kURows * kUSliceK;                     // one slice of weights (E2M1 chunks)
 constexpr uint32_t kUBBytes = kUCols * kUSliceK;                     // one slice of E4M3 activations
 constexpr uint32_t kUSfBytes = 512;                                  // scales of 128 rows x 4 K-blocks
 
@@ -125,7 +127,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // mbarrier.try_wait with an explicit suspend-time limit: the thread sleeps in
 // hardware until the phase completes or about `ns` nanoseconds pass, instead
-// of spinning (a spinning warp takes issue slots from the decode warps)
+// of spinning (a spinning warp takes issue slots from the working warps)
 __device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
   uint32_t ok;
   asm volatile(
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           tmem_cp_sf(sfb, umma_desc_sf(smem_addr(sfbbuf + (size_t)st * kUSfBytes)));
           for (int kb = 0; kb < nkb; ++kb)   // K = 32 steps: 32 bytes into the swizzle rows
             umma_mx(d, umma_desc_sw128(as + 32 * kb), umma_desc_sw128(bs + 32 * kb),
-                    umma_idesc_mx_e4m3(kURows, f.nmma, kb, kb), sfa, sfb, sl > 0 || kb > 0);
+                    umma_idesc_mx(kURows, f.nmma, kFmtE2M1, kb, kb), sfa, sfb, sl > 0 || kb > 0);
           umma_commit(&op_empty[st]);
           last = &op_empty[st];
           last_par = par;
@@ -492,10 +494,13 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
     }
   } else {
-    // ---- raw ring -> E4M3 weights and A scales (decode warp dw: tile dw % 8 of
-    // the item, the slice's 32-wide K-blocks u = dw / 8, dw / 8 + 2) ---------------
+    // ---- raw ring -> the tensor cores' E2M1 operand form and A scales
+    // (placement warp dw: tile dw % 8 of the item, the slice's 32-wide
+    // K-blocks u = dw / 8, dw / 8 + 2). Lane l moves half-row l % 2 of row
+    // l / 2 of a unit (16 codes, 8 bytes) into the low half of its 16-byte
+    // chunk of the swizzled A slice; the high half is never read.
     const int dw = warp - kWDec, t = dw % kUTiles;
-    const int g = lane >> 2, q = lane & 3;
+    const int rr = lane >> 1, hh = lane & 1;
     int tile = 0;
     for (int p = 0; p < n_stream; ++p) {
       const int j = p / ns, sl = p - j * ns, st = p % kUStages;
@@ -511,27 +516,13 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       uint8_t* sa = sfabuf + (size_t)st * kUSfBytes;
 #pragma unroll
       for (int u = dw / kUTiles; u < kUSliceKb; u += kDecPerTile) {
-        const int r0 = t * kTileRows + g, r1 = r0 + 8;
-        uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 0u, slo = 0u, shi = 0u;
-        if (u < nkb && tile < a.n_tiles) {
-          const uint8_t* unit = raw + (size_t)u * kUnitBytes;
-          const uint2 wv = *reinterpret_cast<const uint2*>(unit + lane * 8);
-          const uint32_t sc16 = *reinterpret_cast<const uint16_t*>(unit + kUnitCodeBytes + 2 * g);
-          c0 = decode_rowlo(wv.x);   // row g,   k 4q .. 4q+3: E4M3 = 2^-6 x the E2M1 value
-          c1 = decode_rowhi(wv.x);   // row g+8
-          c2 = decode_rowlo(wv.y);   // row g,   k 16+4q ..
-          c3 = decode_rowhi(wv.y);   // row g+8
-          slo = min((sc16 & 0xFFu) + 6u, 255u);   // A scale: 2^(s-127) x 2^6
-          shi = min((sc16 >> 8) + 6u, 255u);
-        }
-        const int k0 = u * kMxBlock + 4 * q;
-        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r0, k0)) = c0;
-        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r1, k0)) = c1;
-        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r0, k0 + 16)) = c2;
-        *reinterpret_cast<uint32_t*>(ab + sw128_off8(r1, k0 + 16)) = c3;
-        if (q == 0) {
-          sa[sf_off(r0, u)] = uint8_t(slo);
-          sa[sf_off(r1, u)] = uint8_t(shi);
+        const bool ok = u < nkb && tile < a.n_tiles;
+        const uint8_t* unit = raw + (size_t)u * kUnitBytes;
+        const uint2 v = ok ? *reinterpret_cast<const uint2*>(unit + rr * 16 + hh * 8) : make_uint2(0u, 0u);
+        *reinterpret_cast<uint2*>(ab + sw128_off8(t * kTileRows + rr, u * kMxBlock + hh * 16)) = v;
+        if (lane < 16) {   // scale byte 2g + h is row g + 8h
+          const uint8_t sc = ok ? unit[kUnitCodeBytes + lane] : uint8_t(0);
+          sa[sf_off(t * kTileRows + (lane >> 1) + 8 * (lane & 1), u)] = sc;
         }
       }
       fence_async_smem();

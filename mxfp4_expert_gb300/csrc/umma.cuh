@@ -1,8 +1,8 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05): tensor
 // memory (TMEM) allocation, shared-memory matrix descriptors, the instruction
-// descriptor of a block-scaled E4M3 x E4M3 -> fp32 MMA, the MMA itself, the
-// copy of scale factors into TMEM, the completion signal, and TMEM -> register
-// loads.
+// descriptor of a block-scaled (E2M1 or E4M3) x E4M3 -> fp32 MMA, the MMA
+// itself, the copy of scale factors into TMEM, the completion signal, and
+// TMEM -> register loads.
 #pragma once
 
 #include "common.cuh"
@@ -59,13 +59,18 @@ __device__ __forceinline__ uint64_t umma_desc_sf(uint32_t saddr) {
   d |= (uint64_t)1 << 46;
   return d;
 }
+// Operand formats of kind::mxf8f6f4.
+constexpr int kFmtE4M3 = 0, kFmtE2M1 = 5;
 // Instruction descriptor of a block-scaled MMA (kind::mxf8f6f4): fp32
-// accumulator, E4M3 A and B (format 0), both K-major, E8M0 scales (bit 23),
-// M x N, and which byte of the 32-bit scale words the A and B scales of this
-// K-block are (sf_a at bits 29-30, sf_b at bits 4-5).
-__host__ __device__ constexpr uint32_t umma_idesc_mx_e4m3(int M, int N, int sf_a, int sf_b) {
-  return ((uint32_t)(sf_b & 3) << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
-         ((uint32_t)(sf_a & 3) << 29);
+// accumulator, A of format a_fmt (bits 7-9) and E4M3 B (bits 10-12 zero), both
+// K-major, E8M0 scales (bit 23), M x N, and which byte of the 32-bit scale
+// words the A and B scales of this K-block are (sf_a at bits 29-30, sf_b at
+// bits 4-5). An E2M1 operand sits in shared memory as 16-byte chunks whose low
+// 8 bytes hold 16 codes (code 2j in the low nibble of byte j); the high 8
+// bytes are not read.
+__host__ __device__ constexpr uint32_t umma_idesc_mx(int M, int N, int a_fmt, int sf_a, int sf_b) {
+  return ((uint32_t)(sf_b & 3) << 4) | ((uint32_t)(a_fmt & 7) << 7) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sf_a & 3) << 29);
 }
 
 // ---- MMA ----------------------------------------------------------------------

@@ -10,7 +10,7 @@ import torch
 
 import workloads as wl
 
-from . import (MOE_LAYOUT_MMA16, MOE_LAYOUT_MMA16_GATEUP, Layer, moe_describe_packed,
+from . import (MOE_LAYOUT_TILE16, MOE_LAYOUT_TILE16_GATEUP, Layer, moe_describe_packed,
                moe_pack_mxfp4)
 
 
@@ -19,16 +19,16 @@ def build_layer(w: wl.Workload, set_idx: int = 0, device="cuda", chunk: int = 32
     """Draw set `set_idx` of workload `w` on `device` and pack its experts."""
     router = wl.gen_router(w, set_idx, device)
     shared = wl.gen_shared(w, set_idx, device)
-    gu_desc = moe_describe_packed(w.E, 2 * w.I, w.d, MOE_LAYOUT_MMA16_GATEUP)
-    dn_desc = moe_describe_packed(w.E, w.d, w.I, MOE_LAYOUT_MMA16)
+    gu_desc = moe_describe_packed(w.E, 2 * w.I, w.d, MOE_LAYOUT_TILE16_GATEUP)
+    dn_desc = moe_describe_packed(w.E, w.d, w.I, MOE_LAYOUT_TILE16)
     gu = torch.empty(gu_desc.total_bytes, dtype=torch.uint8, device=device)
     dn = torch.empty(dn_desc.total_bytes, dtype=torch.uint8, device=device)
     bg, bd = gu_desc.bytes_per_mat, dn_desc.bytes_per_mat
     for e0 in range(0, w.E, chunk):
         n = min(chunk, w.E - e0)
         gu_f, dn_f = wl.gen_experts(w, set_idx, e0, n, device)
-        moe_pack_mxfp4(gu_f, MOE_LAYOUT_MMA16_GATEUP, out=gu[e0 * bg:(e0 + n) * bg], dev_status=dev_status)
-        moe_pack_mxfp4(dn_f, MOE_LAYOUT_MMA16, out=dn[e0 * bd:(e0 + n) * bd], dev_status=dev_status)
+        moe_pack_mxfp4(gu_f, MOE_LAYOUT_TILE16_GATEUP, out=gu[e0 * bg:(e0 + n) * bg], dev_status=dev_status)
+        moe_pack_mxfp4(dn_f, MOE_LAYOUT_TILE16, out=dn[e0 * bd:(e0 + n) * bd], dev_status=dev_status)
         del gu_f, dn_f
     return Layer(router, gu, gu_desc, dn, dn_desc, *shared, top_k=w.k)
 

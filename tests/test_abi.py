@@ -46,13 +46,13 @@ def test_status_strings_and_version(mx):
 
 
 def test_packed_bytes_and_descriptor(mx):
-    assert mx.moe_packed_bytes(512, 1536, 2560, mx.MOE_LAYOUT_MMA16_GATEUP) == 512 * (1536 * 2560 // 2 + 1536 * 2560 // 32)
-    assert mx.moe_packed_bytes(1, 2560, 768, mx.MOE_LAYOUT_MMA16) == 983040 + 61440
+    assert mx.moe_packed_bytes(512, 1536, 2560, mx.MOE_LAYOUT_TILE16_GATEUP) == 512 * (1536 * 2560 // 2 + 1536 * 2560 // 32)
+    assert mx.moe_packed_bytes(1, 2560, 768, mx.MOE_LAYOUT_TILE16) == 983040 + 61440
     assert mx.moe_packed_bytes(1, 24, 64, 1) == 0          # N not a multiple of 16
     assert mx.moe_packed_bytes(1, 32, 48, 1) == 0          # K not a multiple of 32
     assert mx.moe_packed_bytes(1, 32, 64, 7) == 0          # unknown layout
     d = mx.moe_describe_packed(3, 32, 64, 1)
-    assert (d.magic, d.version, d.n_mat, d.N, d.K) == (0x3446584D, 1, 3, 32, 64)
+    assert (d.magic, d.version, d.n_mat, d.N, d.K) == (0x3446584D, 2, 3, 32, 64)
     assert d.total_bytes == 3 * (32 * 64 // 2 + 32 * 64 // 32)
     with pytest.raises(mx.MoeError):
         mx.moe_describe_packed(1, 20, 64, 1)
