@@ -52,6 +52,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// mbarrier.try_wait with an explicit suspend-time limit: the thread sleeps in
+// hardware until the phase completes or about `ns` nanoseconds pass, instead
+// of spinning (a spinning warp takes issue slots from the working warps)
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false (and sets MOE_DEV_TIMEOUT) if the phase never
 // completes within kSpinBudget cycles. Between polls the thread sleeps for
 // sleep_ns, so waiting warps leave the issue slots to the working ones.

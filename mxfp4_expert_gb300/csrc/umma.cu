@@ -125,19 +125,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// mbarrier.try_wait with an explicit suspend-time limit: the thread sleeps in
-// hardware until the phase completes or about `ns` nanoseconds pass, instead
-// of spinning (a spinning warp takes issue slots from the working warps)
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded mbarrier wait that also gives up when another role of the CTA has
 // timed out (*abort set; seen within one suspend period).
 __device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
