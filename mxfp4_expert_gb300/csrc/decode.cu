@@ -1,5 +1,5 @@
 // Single-launch decode path (T <= 4 tokens): the whole layer in one kernel
-// launch, one CTA per SM, 16 warps per CTA.
+// launch, one CTA per SM, 32 warps per CTA.
 //
 // Phases of one CTA c of G:
 //   0. griddepcontrol.launch_dependents, then L2 prefetch of this CTA's
@@ -12,15 +12,17 @@
 //      features [c I/G, (c+1) I/G), one bf16 row per warp (16-byte loads of
 //      the whole row in flight, fp32 FMAs); logits and h_sh to global memory,
 //      then one release increment.
-//   2. x -> 3 e4m3 terms per 32-block (B operand of the routed MMAs) while the
-//      other CTAs finish; wait for every CTA's logits; top-k in every CTA (the
-//      best k of each 32-expert chunk on all warps, then a k-way merge per
-//      token); the active experts with their slots (one warp, shuffles); this
-//      CTA's contiguous range of gate/up tiles, balanced by bytes against its
-//      down and shared-down work. One L2 prefetch per gate/up tile and per
-//      active expert's down units.
+//   2. x -> 3 e4m3 terms per 32-block (B operand of the routed MMAs, in the
+//      K order of the A fragments) while the other CTAs finish; wait for
+//      every CTA's logits; top-k in every CTA (the best k of each 32-expert
+//      chunk on all warps, then a k-way merge per token). The selected
+//      experts' gate/up matrices go into L2 at once, cut into G slices (one
+//      per CTA). The active experts with their slots (one warp, match_any);
+//      this CTA's contiguous range of gate/up tiles, balanced by bytes against
+//      its down and shared-down work; one L2 prefetch per active expert's down
+//      units of this CTA's output tiles; the first round of down items.
 //   3. Routed gate/up: items (16-row tile, 8 units of 272 B = 16 rows x 32 K
-//      of E2M1 codes + E8M0 scales), item j on warp j % 16. Each warp keeps 4
+//      of E2M1 codes + E8M0 scales), item j on warp j % 32. Each warp keeps 1-2
 //      items in flight, copied with cp.async into its own shared-memory
 //      buffers, and multiplies them on the e4m3 warp MMA (m16n8k32) against
 //      the x terms. The warp that finishes a tile's last item adds the tile's
@@ -28,12 +30,13 @@
 //      h as 2 e4m3 terms per feature with one factor per 8 features (routing
 //      weight folded in); then one release increment per CTA.
 //   4. Shared down rows of this CTA's 16-row output tiles (every CTA's h_sh is
-//      in since the routing barrier), fp32 FMAs, while the down items are
+//      in since the routing barrier), fp32 FMAs, while the first down items are
 //      already being copied (cp.async, from L2) into the warps' buffers.
 //   5. Routed down: after every CTA's h is in, the h terms of all slots go to
-//      shared memory; items (output tile, active expert, 8 units) into
-//      per-item partials, added in a fixed order into y (bf16). Each CTA owns
-//      whole output tiles, so y needs no cross-CTA reduction.
+//      shared memory; items (output tile, active expert, up to 8 units, sized
+//      so every warp gets one) into per-item partials, added in a fixed order
+//      (one warp per output, a fixed tree) into y (bf16). Each CTA owns whole
+//      output tiles, so y needs no cross-CTA reduction.
 //
 // The counters live at the head of the workspace and must be zero before the
 // first call; the last CTA of a call resets them. Every wait is bounded
@@ -57,7 +60,7 @@ constexpr int kU = 8;                // MXFP4 units a warp loads together
 constexpr int kRowVec = 10;          // 16-byte vectors of a bf16 row a lane loads together
 constexpr int kMaxGuItems = 96;      // gate/up (tile, K-range) items per round
 // items a warp keeps in flight (cp.async into its own shared-memory buffers):
-// 4 for one or two tokens, 2 when the activations need more shared memory
+// 2 for one or two tokens, 1 when the activations need more shared memory
 __host__ __device__ constexpr int stage_items(int T) { return T <= 2 ? 2 : 1; }
 constexpr uint32_t kItemBytes = kU * kUnitBytes;   // one item: kU units of a 16-row tile
 constexpr int kMaxDnItems = 64;      // down (tile, expert, K-range) items per round

@@ -14,8 +14,9 @@
 // adds.
 //
 // Work items are (active expert, block of 128 weight rows = 8 packed 16-row
-// tiles, block of up to 128 B rows of that expert's tokens / slots), split
-// into contiguous ranges per CTA (one CTA per SM, persistent). Along K an
+// tiles, block of up to 128 B rows of that expert's tokens / slots), ordered
+// by row block then token block, split into contiguous ranges per CTA (one
+// CTA per SM, persistent). Along K an
 // item goes in slices of four 32-wide K-blocks (one 128-byte swizzle row).
 // The CTA is a pipeline of warp roles that meet only at mbarriers:
 //   * producer (one thread): 1-D bulk copies of the packed MXFP4 bytes of a
@@ -238,10 +239,13 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   auto item_slow = [&](int j) {
     Item f;
     const int it = lo + j, ai = expert_of(it), rem = it - iofs[ai];
-    const int tb = rem / nrb;
     f.e = a.active[ai];
     const int n_e = a.offsets[f.e + 1] - a.offsets[f.e];
-    f.rb = rem - tb * nrb;
+    // row block major, token block minor: the token blocks of one row block
+    // follow each other, so the second one reads the weights from L2
+    const int ntb = (n_e + kNTok - 1) / kNTok;
+    f.rb = rem / ntb;
+    const int tb = rem - f.rb * ntb;
     f.pos0 = a.offsets[f.e] + tb * kNTok;
     f.ntok = min(kNTok, n_e - tb * kNTok);
     geometry(f);
