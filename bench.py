@@ -189,15 +189,16 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel_src, kernel):
-    """dram bytes per launch from profiles/dram_traffic.txt if the kernel source is unchanged."""
+def profiled_traffic(kernel_src, kernel, workload):
+    """dram bytes per launch of `kernel` on `workload` from profiles/dram_traffic.txt,
+    if the kernel source is unchanged since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
     for ln in open(p):
         f = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("src_sha") == sha:
+        if f.get("kernel") == kernel and f.get("src_sha") == sha and f.get("workload") == workload:
             return int(float(f["bytes_per_launch"]))
     return None
 
@@ -457,7 +458,7 @@ def run_ours(args, w):
                               "decode.cu" if dom == "decode_fused" else
                               ("umma.cu" if "routed_down" in stage_mean and "act_split_h" not in stage_mean
                                else "experts.cu") if dom.startswith("routed") else "dense.cu")
-    traffic = profiled_traffic(kernel_src, dom)
+    traffic = profiled_traffic(kernel_src, dom, w.name + ("_mxfp8" if args.act == "mxfp8" else ""))
     algo_bytes = float(np.mean([weight_bytes_per_call(w, D) for D in D_sets]))
     eff_gbs = algo_bytes * calls * ws / (ms * 1e-3) / 1e9     # whole-job weight bytes per second
 
@@ -611,7 +612,10 @@ def run_lmhead(args):
                    "l2": "the 402 MB head exceeds L2 (129 MB)"},
         "effective_gbs": gbs,
         "roofline": {"bound": "hbm", "kernel": "lm_gemv_kernel", "kernel_us": us, "achieved": gbs, "peak": peak,
-                     "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_source": peak_kind,
+                     "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": profiled_traffic(os.path.join(ROOT, "mxfp4_expert_gb300", "csrc", "lmhead.cu"),
+                                                 "lm_gemv", f"lmhead_t{T}"),
+                     "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": bytes_},
         "gpu_launches": 2 * steps * calls_per_step, "clocks": clocks}), flush=True)
 
