@@ -28,11 +28,12 @@
 //     the layout tcgen05.cp copies;
 //   * 4 loader warps: the slice of the activation rows (x gathered by token,
 //     or h by slot; each term a block of B rows) copied with cp.async, and
-//     their B scale bytes; a loader announces slice p once its copies have
-//     landed (it waits for them two slices later) and it has made them
-//     visible to the async proxy;
-//   * MMA (one thread): tcgen05.cp of the slice's A and B scales into tensor
-//     memory, then one MMA per K-block (M = 128, N = the item's B rows) into
+//     their B scale bytes; every loader thread's copies arrive on the stage
+//     barrier by themselves when they land (cp.async.mbarrier.arrive.noinc),
+//     so a loader never waits for its own copies;
+//   * MMA (one thread): after the stage's barriers, a proxy fence (the
+//     loaders' copies and scale bytes are generic-proxy writes), tcgen05.cp of
+//     the slice's A and B scales into tensor memory, then one MMA per K-block (M = 128, N = the item's B rows) into
 //     one of two accumulators; each slice's work is committed to the barrier
 //     that frees its stage, the item's last slice also to the accumulator's;
 //   * 4 epilogue warps (one per 32-lane quarter of tensor memory): tcgen05.ld,
@@ -59,8 +60,6 @@ constexpr int kUStages = 4;                  // operand stages (weights + activa
 constexpr int kUChunk = 2;                   // slices per raw weight copy
 constexpr int kURing = 3;                    // raw weight chunks in flight
 constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about this many chunks ahead
-constexpr int kULag = 2;                     // activation slices a loader keeps in flight
-static_assert(kUStages > kULag, "a loader announces slice p - kULag only after it has claimed slice p's stage");
 constexpr int kUAcc = 2;                     // accumulators in tensor memory
 constexpr int kUCols = 128;                  // B rows per item = largest MMA N
 constexpr int kUSfCols = 8;                  // tensor-memory columns of one stage's scales (A: 4, B: 4)
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     }
     for (int i = 0; i < kUStages; ++i) {
       mbar_init(&a_full[i], kNDec);
-      mbar_init(&b_full[i], kNLoad);
+      mbar_init(&b_full[i], kNLoad * 32);
       mbar_init(&op_empty[i], 1);
     }
     for (int i = 0; i < kUAcc; ++i) {
@@ -347,6 +346,7 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
             ok = false;
             break;
           }
+          fence_async_smem();
           tc_fence_after();
           const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
           const uint32_t as = smem_addr(abuf + (size_t)st * kUABytes);
@@ -422,7 +422,6 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
     constexpr int kRows = kUCols / 16;   // B rows per thread
     int b_src[kRows], nb_src[kRows];     // (activation row * nterms + term), or -1 for padding
     int s_src = -1, ns_src = -1;         // activation row of B row lt, or -1
-    int pend = 0;                        // first slice not yet announced
     Item f{};
     // rows of item j (requested one item ahead, so the loads are in flight meanwhile)
     auto rows_of = [&](int j, int (&src)[kRows], int& ssrc) {
@@ -467,23 +466,10 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
 #pragma unroll
       for (int i = 0; i < kUSliceKb; ++i)
         sb[sf_off(lt, i)] = (s_src >= 0 && i < nkb) ? a.act_s[(size_t)s_src * KB + kb0 + i] : uint8_t(127);
-      cp_async_commit();
-      // announce slice p - kULag once its copies (not the later ones) have landed
-      if (p - pend >= kULag) {
-        cp_async_wait<kULag>();
-        fence_async_smem();   // generic-proxy writes -> visible to the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
-        ++pend;
-      }
+      // this thread's arrival on the stage barrier, made when its copies land
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&b_full[st])) : "memory");
     }
     cp_async_wait<0>();   // nothing lands after the CTA's shared memory goes away
-    if (!*abort) {
-      fence_async_smem();
-      __syncwarp();
-      for (; pend < n_stream; ++pend)
-        if (lane == 0) mbar_arrive(&b_full[pend % kUStages]);
-    }
   } else {
     // ---- raw ring -> the tensor cores' E2M1 operand form and A scales
     // (placement warp dw: tile dw % 8 of the item, the slice's 32-wide
