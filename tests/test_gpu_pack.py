@@ -105,3 +105,49 @@ def test_pack_rejects_bad_arguments(mx):
     small = torch.empty(10, dtype=torch.uint8, device="cuda")
     with pytest.raises(mx.MoeError):
         mx.moe_pack_mxfp4(w, 1, out=small)             # buffer too small
+
+
+def packed_reference(codes, scales, layout):
+    """The packed bytes as include/moe_mxfp4.h documents them, built from the
+    oracle's canonical codes [n_mat][N][K/2] and scales [n_mat][N][K/32]:
+    unit (tile r, block b) at (r*K/32 + b)*272; bytes [16i, 16i+16) = packed row
+    i's canonical bytes of block b; byte 256 + 2g + h = scale of row g + 8h.
+    GATEUP: packed row i of tile r is gate row 8r + i (i < 8) or up row
+    I + 8r + i - 8."""
+    n_mat, N, KH = codes.shape
+    KB = KH // 16
+    out = np.zeros(n_mat * N * KB * 272 // 16, dtype=np.uint8)
+    o = 0
+    for m in range(n_mat):
+        for r in range(N // 16):
+            for b in range(KB):
+                unit = np.zeros(272, dtype=np.uint8)
+                for i in range(16):
+                    if layout == 2:
+                        src = 8 * r + i if i < 8 else N // 2 + 8 * r + i - 8
+                    else:
+                        src = 16 * r + i
+                    unit[16 * i:16 * i + 16] = codes[m, src, 16 * b:16 * b + 16]
+                    g, h = (i, 0) if i < 8 else (i - 8, 1)
+                    unit[256 + 2 * g + h] = scales[m, src, b]
+                out[o:o + 272] = unit
+                o += 272
+    return out
+
+
+@pytest.mark.parametrize("n_mat,N,K,layout", [(2, 32, 96, 1), (1, 48, 64, 2), (1, 64, 256, 2)])
+def test_pack_bytes_match_documented_layout(mx, n_mat, N, K, layout):
+    """The raw packed bytes (not their unpacking) against the header's layout
+    formula applied to the oracle's quantisation."""
+    g = torch.Generator().manual_seed(N + K + layout)
+    w = torch.randn((n_mat, N, K), generator=g) * 0.02
+    w = w * torch.exp2(torch.randint(-8, 8, (n_mat, N, 1), generator=g).float())
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    packed, _ = mx.moe_pack_mxfp4(w.cuda().contiguous(), layout, dev_status=st)
+    torch.cuda.synchronize()
+    rc, rs, _ = mxfp4.quantize(w.numpy())
+    ref = packed_reference(rc, rs, layout)
+    got = packed.cpu().numpy().view(np.uint8).ravel()
+    assert got.size == ref.size
+    assert np.array_equal(got, ref)
+    assert int(st.item()) == 0
