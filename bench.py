@@ -454,10 +454,11 @@ def run_ours(args, w):
     # one launch would count the previous layer's tail)
     dom_us = us_per_layer if stages == ["decode_fused"] or dom == "layer" else stage_mean[dom]
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    tc_path = "routed_down" in stage_mean and "act_split_h" not in stage_mean
     kernel_src = os.path.join(ROOT, "mxfp4_expert_gb300", "csrc",
                               "decode.cu" if dom == "decode_fused" else
-                              ("umma.cu" if "routed_down" in stage_mean and "act_split_h" not in stage_mean
-                               else "experts.cu") if dom.startswith("routed") else "dense.cu")
+                              ("umma.cu" if tc_path else "experts.cu") if dom.startswith("routed") else
+                              ("tcdense.cu" if tc_path else "dense.cu"))
     traffic = profiled_traffic(kernel_src, dom, w.name + ("_mxfp8" if args.act == "mxfp8" else ""))
     algo_bytes = float(np.mean([weight_bytes_per_call(w, D) for D in D_sets]))
     eff_gbs = algo_bytes * calls * ws / (ms * 1e-3) / 1e9     # whole-job weight bytes per second
@@ -524,9 +525,10 @@ def run_ours(args, w):
         "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None,
         "dtype": ("e2m1 (as e4m3) x mxfp8 e4m3 activations, e8m0 block scales (tcgen05 mxf8f6f4 routed experts), "
-                  "bf16 router/shared (mma.sync), f32 accumulate" if args.act == "mxfp8" else
+                  "bf16 router/shared (tcgen05 kind::f16), f32 accumulate" if args.act == "mxfp8" else
                   "e2m1 (as e4m3) x e4m3 2-term activations, e8m0 block scales (tcgen05 mxf8f6f4 routed experts), "
-                  "bf16 router/shared (mma.sync), f32 accumulate"
+                  "bf16 router/shared (tcgen05 kind::f16; mma.sync router/shared gate-up below 128 tokens), "
+                  "f32 accumulate"
                   if path == mx.MOE_PATH_PREFILL_TC else
                   "e2m1xe4m3->f32 (mma.sync), bf16 router/shared, f32 accumulate"),
         "data": "synthetic",

@@ -39,6 +39,11 @@ namespace {
 
 // Tokens from which the routed experts run as tcgen05 grouped GEMMs.
 constexpr int kPrefillMinT = 32;
+// Tensor-core path: tokens from which the combine (shared down + weighted
+// sum) runs as a tcgen05 GEMM, and from which the router + shared gate/up do
+// (below it their 10 or so 128-row blocks leave most SMs idle).
+constexpr int kDenseTcMinT = 32;
+constexpr int kFrontTcMinT = 128;
 
 // Workspace sections of one forward call (byte offsets from the base).
 struct Workspace {
@@ -247,7 +252,16 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
                sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_gate) : nullptr,
                sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_up) : nullptr, logits,
                at<float>(B, ws.h_sh)};
-  if ((st = launch_front(fa, di, s))) return st;
+  // tcgen05 dense stages: h_sh as bf16 hi and lo terms in the fp32 h_sh section
+  const bool tcd = tc && T >= kDenseTcMinT && tc_dense_supported(T, d, I, k, sh.has_shared != 0, di);
+  __nv_bfloat16* h_hi = at<__nv_bfloat16>(B, ws.h_sh);
+  __nv_bfloat16* h_lo = h_hi + (size_t)T * I;
+  if (tcd) {
+    fa.h_hi = h_hi;
+    fa.h_lo = h_lo;
+  }
+  if ((st = tcd && T >= kFrontTcMinT ? launch_tc_front(fa, h_hi, h_lo, status, di, s) : launch_front(fa, di, s)))
+    return st;
   if ((st = mark())) return st;
   // 3. top-k + weights, 4. sort by expert
   if ((st = launch_topk(logits, T, E, k, bias_dev, bias_row_stride, idx, w, s))) return st;
@@ -302,13 +316,14 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
     ud.act_s = at<uint8_t>(B, ws.hs);
     ud.out = at<float>(B, ws.part);
     ud.out_ld = d;
+    ud.out_by_pair = tcd ? 1 : 0;   // the tcgen05 combine reads part in (token, choice) order
     if ((st = launch_umma_routed(kModeDown, ud, di, s))) return st;
     if ((st = mark())) return st;
     CombineArgs ca{T, d, I, k,
                    sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_down) : nullptr,
                    at<float>(B, ws.h_sh), w, inv, at<float>(B, ws.part),
                    static_cast<__nv_bfloat16*>(y_dev)};
-    if ((st = launch_combine(ca, di, s))) return st;
+    if ((st = tcd ? launch_tc_combine(ca, h_hi, h_lo, status, di, s) : launch_combine(ca, di, s))) return st;
     return mark();
   }
   // 5. routed gate/up + SwiGLU -> h [slots][I]

@@ -18,7 +18,8 @@
 //
 // In the first kernel the shared gate and up rows are interleaved 8 + 8 per
 // 16-row tile (as the TILE16_GATEUP weight layout does), so one lane holds gate and up of the
-// same feature for the SwiGLU. The shared down projection reads h_sh (fp32)
+// same feature for the SwiGLU; h_sh goes out as fp32, or as the two bf16
+// terms the tcgen05 combine reads. The shared down projection reads h_sh (fp32)
 // as two bf16 terms, hi = bf16(h) and lo = bf16(h - hi), about 16 significant
 // bits, with one MMA per term.
 #include <cuda_runtime.h>
@@ -202,7 +203,16 @@ dense_kernel(P a, int Ep, int N, int K) {
         } else if (a.sh_gate) {
           const int s = m - Ep;   // gate row of feature f in c[u], its up row in c[2 + u]
           const int f = (s >> 4) * 8 + (s & 7);
-          if (f < a.I) a.h_sh[(size_t)t * a.I + f] = silu_f(acc[j][u]) * acc[j][2 + u];
+          if (f < a.I) {
+            const float h = silu_f(acc[j][u]) * acc[j][2 + u];
+            if (a.h_hi) {
+              const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+              a.h_hi[(size_t)t * a.I + f] = hi;
+              a.h_lo[(size_t)t * a.I + f] = __float2bfloat16_rn(h - __bfloat162float(hi));
+            } else {
+              a.h_sh[(size_t)t * a.I + f] = h;
+            }
+          }
         }
       } else {
 #pragma unroll

@@ -57,6 +57,7 @@ struct RoutedArgs {
   int max_items;            // upper bound on n_active * n_tiles (grid sizing)
   float* out;               // gate/up: h [slots][N/2]; down: part [slots][N]
   int out_ld;
+  int out_by_pair;          // tensor-core down pass: part row = perm[slot] (t k + j), not the slot
   int* status;
 };
 int launch_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);
@@ -75,6 +76,8 @@ struct FrontArgs {
   const __nv_bfloat16* sh_up;      // [I][d]
   float* logits;                   // [T][E]
   float* h_sh;                     // [T][I]
+  __nv_bfloat16* h_hi = nullptr;   // if set: h_sh goes out as two bf16 terms [T][I] here
+  __nv_bfloat16* h_lo = nullptr;   //   (hi = bf16(h), lo = bf16(h - hi)) instead of fp32
 };
 int launch_front(const FrontArgs& a, const DeviceInfo& di, cudaStream_t s);
 
@@ -88,5 +91,17 @@ struct CombineArgs {
   __nv_bfloat16* y;                // [T][d]
 };
 int launch_combine(const CombineArgs& a, const DeviceInfo& di, cudaStream_t s);
+
+// tcdense.cu: the same two dense stages on tcgen05 bf16 MMAs with TMA-tiled
+// operands (shared expert and k <= 8 required). h_sh passes between them as
+// two bf16 terms h_hi, h_lo [T][I] (hi = bf16(h), lo = bf16(h - hi)); a.h_sh
+// is unused by both (launch_front writes the same terms when a.h_hi is set).
+// The combine reads part in (token, choice) order: part row t k + j (a.inv
+// unused).
+bool tc_dense_supported(int T, int d, int I, int k, bool has_shared, const DeviceInfo& di);
+int launch_tc_front(const FrontArgs& a, __nv_bfloat16* h_hi, __nv_bfloat16* h_lo, int* status,
+                    const DeviceInfo& di, cudaStream_t s);
+int launch_tc_combine(const CombineArgs& a, const __nv_bfloat16* h_hi, const __nv_bfloat16* h_lo, int* status,
+                      const DeviceInfo& di, cudaStream_t s);
 
 }  // namespace moe

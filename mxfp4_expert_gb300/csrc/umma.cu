@@ -125,22 +125,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Bounded mbarrier wait that also gives up when another role of the CTA has
-// timed out (*abort set; seen within one suspend period).
-__device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_for(bar, parity, 100000u)) {
-    if (*abort) return false;
-    if (clock64() - t0 > kSpinBudget) {
-      *abort = 1;
-      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, UmmaSmem L) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -398,14 +382,20 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
         const int r = f.rb * kURows + row;   // output feature
         const bool st_ok = r < a.n_tiles * kTileRows;
         for (int c0 = 0; c0 < f.n16; c0 += 8) {
+          // output row of column c0 + l at lane l < 8: the sorted slot, or its
+          // (token, choice) pair t k + j
+          int orow = f.pos0 + c0 + (lane & 7);
+          if (a.out_by_pair && lane < 8 && c0 + lane < f.ntok) orow = __ldg(a.perm + orow);
           uint32_t vh[8], vl[8];
           tmem_ld8(trow + c0, vh);
           if (nterms == 2) tmem_ld8(trow + f.n16 + c0, vl);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
+          for (int jj = 0; jj < 8; ++jj) {
+            const int o = __shfl_sync(0xFFFFFFFFu, orow, jj);
             if (st_ok && c0 + jj < f.ntok)
-              a.out[(size_t)(f.pos0 + c0 + jj) * a.out_ld + r] =
+              a.out[(size_t)o * a.out_ld + r] =
                   __uint_as_float(vh[jj]) + (nterms == 2 ? __uint_as_float(vl[jj]) : 0.0f);
+          }
         }
       }
       tc_fence_before();

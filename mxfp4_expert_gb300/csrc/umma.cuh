@@ -1,8 +1,9 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05): tensor
 // memory (TMEM) allocation, shared-memory matrix descriptors, the instruction
-// descriptor of a block-scaled (E2M1 or E4M3) x E4M3 -> fp32 MMA, the MMA
-// itself, the copy of scale factors into TMEM, the completion signal, and
-// TMEM -> register loads.
+// descriptors of a block-scaled (E2M1 or E4M3) x E4M3 -> fp32 MMA and of a
+// bf16 x bf16 -> fp32 MMA, the MMAs themselves, the copy of scale factors
+// into TMEM, the completion signal, TMEM -> register loads, and the bounded
+// mbarrier wait of the warp-specialised kernels.
 #pragma once
 
 #include "common.cuh"
@@ -73,7 +74,23 @@ __host__ __device__ constexpr uint32_t umma_idesc_mx(int M, int N, int a_fmt, in
          ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sf_a & 3) << 29);
 }
 
+// Instruction descriptor of a dense MMA of kind::f16 with bf16 A and B (bits
+// 7-9 and 10-12 = 1), both K-major, fp32 accumulator (bits 4-5 = 1), M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // ---- MMA ----------------------------------------------------------------------
+// One thread: D[tmem] (+)= A * B^T for one K = 16 step of bf16 operands
+// (kind::f16, fp32 accumulator, cta_group::1).
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
 // One thread: D[tmem] (+)= (A x scale_A) * (B x scale_B)^T for one K = 32 step
 // (kind::mxf8f6f4, block_scale, one scale per 32 elements, cta_group::1).
 __device__ __forceinline__ void umma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -104,6 +121,58 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
                : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Whole warp: 4 consecutive columns of TMEM lane (taddr lane + t) to thread t.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+      : "r"(taddr)
+      : "memory");
+}
+// Whole warp: 16 consecutive columns of TMEM lane (taddr lane + t) to thread t.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Whole warp: two such loads (columns at ta and at tb) under one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%33];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// ---- bounded waits of a warp-specialised CTA ------------------------------------
+// mbarrier wait that gives up after kSpinBudget cycles (setting MOE_DEV_TIMEOUT
+// and *abort) or as soon as another role of the CTA has set *abort (seen
+// within one suspend period).
+__device__ __forceinline__ bool uwait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_for(bar, parity, 100000u)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kSpinBudget) {
+      *abort = 1;
+      if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 }  // namespace moe

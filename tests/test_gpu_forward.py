@@ -110,6 +110,10 @@ def build(mx, w, set_idx=0):
     ("tc_ragged", 33, 512, 96, 24, 5, "natural"),
     ("tc_wide_k", 32, 128, 32, 40, 32, "natural"),
     ("tc_many_rows", 300, 256, 64, 4, 2, "natural"),   # > 128 rows per expert: several token blocks
+    # T >= 128: router, shared expert and combine on tcgen05 too; ragged T, E,
+    # I and d against their 128-row blocks, K = d not a multiple of 64 (k3)
+    ("tc_dense_ragged", 257, 384, 96, 136, 8, "natural"),
+    ("tc_dense_k3", 200, 160, 224, 72, 3, "natural"),
 ])
 def test_small_layers(mx, name, T, d, I, E, k, routing):
     w = wl.Workload(name, T=T, d=d, I=I, E=E, k=k, sets=1, routing=routing, seed=3)
