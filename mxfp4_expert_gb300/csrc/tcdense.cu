@@ -43,11 +43,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "host_util.h"
 #include "kernels.h"
+#include "tma.cuh"
 #include "umma.cuh"
 
 namespace moe {
@@ -136,20 +135,6 @@ __host__ __device__ inline int tcd_item(const TcdSched& s, int b, int j) {
   if (j < n1) return s.n_big + (b - s.r) + j * s.nL;
   j -= n1;
   return s.n_big + s.n1 + b + j * s.G;
-}
-
-// 2-D tiled TMA load of box (x = innermost element, y = row) into shared
-// memory, completion counted on `bar`. x times the element size is a
-// multiple of 16 bytes (x = 64 i for bf16, 128 i for fp32).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // MODE 0: front; MODE 1: combine.
@@ -441,43 +426,15 @@ __global__ void __launch_bounds__(kTBlock, 1) tc_dense_kernel(const __grid_const
   }
 }
 
-// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
-// dependence on the driver library).
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(f);
-    (void)cudaGetLastError();
-  });
-  return fn;
-}
-
 // Tensor map of a row-major matrix [rows][cols] (row stride cols) of bf16
 // (box_rows x 64 boxes, 128-byte swizzle) or fp32 (box_rows x 128 boxes, no
 // swizzle); zero fill outside the matrix.
 int encode_map(CUtensorMap* m, const void* base, int rows, int cols, bool fp32, int box_rows) {
-  const EncodeTiled fn = encode_fn();
-  if (!fn) return MOE_ERR_CUDA;
-  const uint32_t es = fp32 ? 4 : 2;
-  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
-  const cuuint64_t strides[1] = {cuuint64_t(cols) * es};
-  const cuuint32_t box[2] = {cuuint32_t(fp32 ? kTM : kTK), cuuint32_t(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;
+  const uint64_t dims[2] = {uint64_t(cols), uint64_t(rows)};
+  const uint64_t strides[1] = {uint64_t(cols) * (fp32 ? 4 : 2)};
+  const uint32_t box[2] = {uint32_t(fp32 ? kTM : kTK), uint32_t(box_rows)};
+  return tma_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                    strides, box, fp32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int MODE>
@@ -496,7 +453,7 @@ int launch_tcd(const TcdParams& P, const DeviceInfo& di, cudaStream_t s) {
 
 bool tc_dense_supported(int T, int d, int I, int k, bool has_shared, const DeviceInfo& di) {
   return has_shared && T >= 1 && k >= 1 && k <= 8 && d % 8 == 0 && I % 8 == 0 &&
-         TcdPlan<0>::kTotal <= di.smem_optin && TcdPlan<1>::kTotal <= di.smem_optin && encode_fn() != nullptr;
+         TcdPlan<0>::kTotal <= di.smem_optin && TcdPlan<1>::kTotal <= di.smem_optin && tma_available();
 }
 
 int launch_tc_front(const FrontArgs& a, __nv_bfloat16* h_hi, __nv_bfloat16* h_lo, int* status,
