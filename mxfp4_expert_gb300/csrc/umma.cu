@@ -317,15 +317,26 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
       bool ok = true;
+      // One thread issues every tensor-core operation of the CTA, so its own
+      // instruction stream sets the pace: descriptors of stage st are the
+      // stage-0 ones plus a constant (the 14-bit address field is the byte
+      // address / 16 and never carries), the instruction descriptors are
+      // built once per item, and the K-blocks of a slice are unrolled.
+      const uint64_t a_desc0 = umma_desc_sw128(smem_addr(abuf)), b_desc0 = umma_desc_sw128(smem_addr(bbuf));
+      const uint64_t sfa_desc0 = umma_desc_sf(smem_addr(sfabuf)), sfb_desc0 = umma_desc_sf(smem_addr(sfbbuf));
+      const uint32_t sf_tmem0 = tmem + uint32_t(kUAcc * kUCols);
+      int st = 0;
+      uint32_t par = 0;
       for (int j = 0; j < n_mine && ok; ++j) {
         const Item f = item_of(j);
         const int ab = j % kUAcc;
         if (j >= kUAcc && !uwait(&acc_empty[ab], uint32_t(j / kUAcc - 1) & 1u, abort, a.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(ab * kUCols);
+        uint32_t idesc[kUSliceKb];
+#pragma unroll
+        for (int kb = 0; kb < kUSliceKb; ++kb) idesc[kb] = umma_idesc_mx(kURows, f.nmma, kFmtE2M1, kb, kb);
         for (int sl = 0; sl < ns; ++sl) {
-          const int p = j * ns + sl, st = p % kUStages;
-          const uint32_t par = uint32_t(p / kUStages) & 1u;
           if (!uwait(&a_full[st], par, abort, a.status) || !uwait(&b_full[st], par, abort, a.status)) {
             ok = false;
             break;
@@ -333,19 +344,22 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
           fence_async_smem();
           tc_fence_after();
           const int nkb = min(kUSliceKb, KB - sl * kUSliceKb);
-          const uint32_t as = smem_addr(abuf + (size_t)st * kUABytes);
-          const uint32_t bs = smem_addr(bbuf + (size_t)st * kUBBytes);
+          const uint64_t ad = a_desc0 + uint64_t(st * (kUABytes >> 4)), bd = b_desc0 + uint64_t(st * (kUBBytes >> 4));
           // this slice's scales into tensor memory (in issue order before its MMAs)
-          const uint32_t sfa = tmem + uint32_t(kUAcc * kUCols + st * kUSfCols), sfb = sfa + 4;
-          tmem_cp_sf(sfa, umma_desc_sf(smem_addr(sfabuf + (size_t)st * kUSfBytes)));
-          tmem_cp_sf(sfb, umma_desc_sf(smem_addr(sfbbuf + (size_t)st * kUSfBytes)));
-          for (int kb = 0; kb < nkb; ++kb)   // K = 32 steps: 32 bytes into the swizzle rows
-            umma_mx(d, umma_desc_sw128(as + 32 * kb), umma_desc_sw128(bs + 32 * kb),
-                    umma_idesc_mx(kURows, f.nmma, kFmtE2M1, kb, kb), sfa, sfb, sl > 0 || kb > 0);
+          const uint32_t sfa = sf_tmem0 + uint32_t(st * kUSfCols), sfb = sfa + 4;
+          tmem_cp_sf(sfa, sfa_desc0 + uint64_t(st * (kUSfBytes >> 4)));
+          tmem_cp_sf(sfb, sfb_desc0 + uint64_t(st * (kUSfBytes >> 4)));
+#pragma unroll
+          for (int kb = 0; kb < kUSliceKb; ++kb)   // K = 32 steps: 32 bytes into the swizzle rows
+            if (kb < nkb) umma_mx(d, ad + uint64_t(2 * kb), bd + uint64_t(2 * kb), idesc[kb], sfa, sfb, sl > 0 || kb > 0);
           umma_commit(&op_empty[st]);
           last = &op_empty[st];
           last_par = par;
           if (sl == ns - 1) umma_commit(&acc_full[ab]);
+          if (++st == kUStages) {
+            st = 0;
+            par ^= 1u;
+          }
         }
       }
       // every MMA has finished before tensor memory is freed
