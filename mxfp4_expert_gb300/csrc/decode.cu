@@ -19,8 +19,7 @@
 //      experts' gate/up matrices go into L2 at once, cut into G slices (one
 //      per CTA). The active experts with their slots (one warp, match_any);
 //      this CTA's contiguous range of gate/up tiles, balanced by bytes against
-//      its down and shared-down work; one L2 prefetch per active expert's down
-//      units of this CTA's output tiles; the first round of down items.
+//      its down and shared-down work; the first round of down items.
 //   3. Routed gate/up: items (16-row tile, 8 units of 272 B = 16 rows x 32 K
 //      of E2M1 codes + E8M0 scales), item j on warp j % 32. Each warp keeps 1-2
 //      items in flight, copied with cp.async into its own shared-memory
@@ -28,7 +27,9 @@
 //      the x terms. The warp that finishes a tile's last item adds the tile's
 //      partials in K order, applies SwiGLU and writes the tile's 8 features of
 //      h as 2 e4m3 terms per feature with one factor per 8 features (routing
-//      weight folded in); then one release increment per CTA.
+//      weight folded in); then (3-4 tokens) one L2 prefetch per active
+//      expert's down units of this CTA's output tiles, the first down items'
+//      copies, and one release increment per CTA.
 //   4. Shared down rows of this CTA's 16-row output tiles (every CTA's h_sh is
 //      in since the routing barrier), fp32 FMAs, while the first down items are
 //      already being copied (cp.async, from L2) into the warps' buffers.
@@ -499,19 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
   __syncthreads();
   const int D = misc[0], i0 = misc[1], i1 = misc[2] > misc[1] ? misc[2] : misc[1];
 
-  // this CTA's gate/up tiles (one prefetch per tile, unless the slices above
-  // covered them) and the down units of its output tiles for every active
-  // expert (one prefetch per expert) into L2, spread over the warps
+  // this CTA's gate/up tiles into L2 (one prefetch per tile, unless the
+  // slices above covered them), spread over the warps
   if (lane == 0) {
 #pragma unroll 1
     for (int gt = i0 + warp; !early_pf && gt < i1; gt += kWarps) {
       const int ai = gt / NTg;
       prefetch_l2(a.gate_up + (size_t)act[ai] * a.gu_mat + (size_t)(gt - ai * NTg) * U_gu, U_gu);
     }
-    if (ntl > 0)
-#pragma unroll 1
-      for (int ai = kWarps - 1 - warp; ai < D; ai += kWarps)
-        prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
   }
   // down items (output tile, active expert, K-range of kU units), in rounds
   // of kMaxDnItems; the first round's table is built now, its copies are
@@ -686,6 +682,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a, Smem 
       cp_async_wait<0>();
       __syncthreads();
     }
+  }
+  // 3-4 tokens: the down units of this CTA's output tiles for every active
+  // expert into L2 (one prefetch per expert), now that its gate/up weights
+  // are in (issued earlier they compete with them for DRAM); 1-2 tokens need
+  // none: the first down items below are copied during the h exchange
+  if constexpr (T >= 3) {
+    if (lane == 0 && ntl > 0)
+#pragma unroll 1
+      for (int ai = kWarps - 1 - warp; ai < D; ai += kWarps)
+        prefetch_range(a.down + (size_t)act[ai] * a.dn_mat + (size_t)t0 * U_dn, uint32_t(ntl) * U_dn);
   }
   // the first down items into each warp's (now free) buffers, then this CTA's
   // h is written: publish (the last warp; the others go on)
