@@ -263,17 +263,25 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
   if ((st = tcd && T >= kFrontTcMinT ? launch_tc_front(fa, h_hi, h_lo, status, di, s) : launch_front(fa, di, s)))
     return st;
   if ((st = mark())) return st;
-  // 3. top-k + weights, 4. sort by expert
-  if ((st = launch_topk(logits, T, E, k, bias_dev, bias_row_stride, idx, w, s))) return st;
-  if ((st = mark())) return st;
+  // 3. top-k + weights, 4. sort by expert (one launch for up to 32 tokens;
+  // the sort stage is then empty)
   int32_t* offsets = at<int32_t>(B, ws.offsets);
   int32_t* perm = at<int32_t>(B, ws.perm);
   int32_t* inv = at<int32_t>(B, ws.inv);
   int32_t* active = at<int32_t>(B, ws.active);
   int32_t* n_active = at<int32_t>(B, ws.n_active);
-  if ((st = launch_sort(idx, T, k, E, at<int32_t>(B, ws.counts), offsets, perm, inv, active, n_active,
-                        at<void>(B, ws.sort_ws), status, s)))
-    return st;
+  if (route_fused_ok(T, E, k)) {
+    if ((st = launch_route_fused(logits, T, E, k, bias_dev, bias_row_stride, idx, w, at<int32_t>(B, ws.counts),
+                                 offsets, perm, inv, active, n_active, status, s)))
+      return st;
+    if ((st = mark())) return st;
+  } else {
+    if ((st = launch_topk(logits, T, E, k, bias_dev, bias_row_stride, idx, w, s))) return st;
+    if ((st = mark())) return st;
+    if ((st = launch_sort(idx, T, k, E, at<int32_t>(B, ws.counts), offsets, perm, inv, active, n_active,
+                          at<void>(B, ws.sort_ws), status, s)))
+      return st;
+  }
   if ((st = mark())) return st;
   const int max_active = T * k < E ? T * k : E;
   if (tc) {

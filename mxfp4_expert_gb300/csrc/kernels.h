@@ -14,6 +14,11 @@ namespace moe {
 int launch_topk(const float* logits, int T, int E, int k, const float* bias, int bias_stride,
                 int32_t* idx, float* w, cudaStream_t s);
 size_t sort_workspace_bytes(int T, int E);
+// top-k and the sort in one launch (one block), for T <= 32 tokens
+bool route_fused_ok(int T, int E, int k);
+int launch_route_fused(const float* logits, int T, int E, int k, const float* bias, int bias_stride,
+                       int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       int32_t* active, int32_t* n_active, int* status, cudaStream_t s);
 int launch_sort(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_t* offsets,
                 int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* ws,
                 int* status, cudaStream_t s);

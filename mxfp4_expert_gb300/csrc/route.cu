@@ -22,13 +22,14 @@ __device__ __forceinline__ float rank_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Top-k of token t by one warp: the best k keys (logit + bias), equal keys to
+// the lower expert index, and their softmax weights; to idx/w (and, if sidx
+// is set, idx to sidx too). PL = 32-expert groups per lane.
 template <int PL>
-__global__ void __launch_bounds__(128)
-topk_kernel(const float* __restrict__ logits, int T, int E, int k, const float* __restrict__ bias,
-            int bias_stride, int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (t >= T) return;
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
+                                           const float* __restrict__ bias, int bias_stride, int lane,
+                                           int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                           int32_t* sidx) {
   const float* row = logits + (size_t)t * E;
   const float* brow = bias ? bias + (size_t)t * bias_stride : nullptr;
   uint32_t key[PL];
@@ -74,7 +75,18 @@ topk_kernel(const float* __restrict__ logits, int T, int E, int k, const float* 
   if (lane < k) {
     idx_out[(size_t)t * k + lane] = int32_t(my_e);
     w_out[(size_t)t * k + lane] = ex / sum;
+    if (sidx) sidx[t * k + lane] = int32_t(my_e);
   }
+}
+
+template <int PL>
+__global__ void __launch_bounds__(128)
+topk_kernel(const float* __restrict__ logits, int T, int E, int k, const float* __restrict__ bias,
+            int bias_stride, int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_token<PL>(logits, t, E, k, bias, bias_stride, lane, idx_out, w_out, nullptr);
 }
 
 // ---- stable sort by expert: counts per token chunk, scan, scatter ----------
@@ -191,6 +203,99 @@ sort_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
   }
 }
 
+// ---- top-k and sort in one block, for T <= 32 tokens ------------------------
+// The same steps as topk_kernel and the three sort kernels for one chunk:
+// warp w ranks tokens w, w + 32, ...; thread e < E then owns expert e for the
+// counts and the scans (offsets, active list); the scatter ranks each entry
+// among the chunk's tokens that chose its expert (bit masks). One launch
+// instead of four.
+template <int PL>
+__global__ void __launch_bounds__(1024)
+route_small_kernel(const float* __restrict__ logits, int T, int E, int k, const float* __restrict__ bias,
+                   int bias_stride, int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                   int32_t* __restrict__ active, int32_t* __restrict__ n_active, int* status) {
+  extern __shared__ uint32_t rs[];
+  int32_t* base = reinterpret_cast<int32_t*>(rs);        // [E]: counts, then first sorted slot
+  uint32_t* mask = rs + E;                               // [E][4]: tokens that chose e
+  int32_t* sidx = reinterpret_cast<int32_t*>(mask + 4 * E);   // [T k]
+  __shared__ int32_t warp_sum[2][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 5 * E; i += blockDim.x) rs[i] = 0u;
+  for (int t = warp; t < T; t += 32) topk_token<PL>(logits, t, E, k, bias, bias_stride, lane, idx, w, sidx);
+  __syncthreads();
+  const int n = T * k;
+  auto valid = [&](int t, int j) {   // in range, and the token's first entry of its expert
+    const int e = sidx[t * k + j];
+    if (e < 0 || e >= E) return false;
+    for (int jj = 0; jj < j; ++jj)
+      if (sidx[t * k + jj] == e) return false;
+    return true;
+  };
+  bool bad = false;
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int t = i / k, j = i - t * k;
+    if (valid(t, j)) {
+      const int e = sidx[i];
+      atomicAdd(&base[e], 1);
+      atomicOr(&mask[e * 4 + (t >> 5)], 1u << (t & 31));
+    } else {
+      bad = true;
+    }
+  }
+  if (bad && status) atomicOr(status, MOE_DEV_INDEX_OOB);
+  __syncthreads();
+  // exclusive scans of the counts (-> offsets) and of (count > 0) (-> active)
+  const int e = tid;
+  const int32_t total = e < E ? base[e] : 0;
+  int32_t a = total, b = total > 0 ? 1 : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t ya = __shfl_up_sync(0xFFFFFFFFu, a, o), yb = __shfl_up_sync(0xFFFFFFFFu, b, o);
+    if (lane >= o) { a += ya; b += yb; }
+  }
+  if (lane == 31) { warp_sum[0][warp] = a; warp_sum[1][warp] = b; }
+  __syncthreads();
+  if (warp == 0) {
+    int32_t sa = warp_sum[0][lane], sb = warp_sum[1][lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t ya = __shfl_up_sync(0xFFFFFFFFu, sa, o), yb = __shfl_up_sync(0xFFFFFFFFu, sb, o);
+      if (lane >= o) { sa += ya; sb += yb; }
+    }
+    warp_sum[0][lane] = sa;
+    warp_sum[1][lane] = sb;
+  }
+  __syncthreads();
+  const int32_t pa = (warp ? warp_sum[0][warp - 1] : 0) + a - total;
+  const int32_t pb = (warp ? warp_sum[1][warp - 1] : 0) + b - (total > 0 ? 1 : 0);
+  if (e < E) {
+    counts[e] = total;
+    offsets[e] = pa;
+    if (total > 0) active[pb] = e;
+    base[e] = pa;
+  }
+  if (e == E - 1) {
+    offsets[E] = pa + total;
+    *n_active = pb + (total > 0 ? 1 : 0);
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int t = i / k, j = i - t * k;
+    if (!valid(t, j)) {
+      inv[i] = -1;
+      continue;
+    }
+    const uint32_t* m = mask + sidx[i] * 4;
+    int rank = 0;
+    for (int wv = 0; wv < (t >> 5); ++wv) rank += __popc(m[wv]);
+    rank += __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+    const int pos = base[sidx[i]] + rank;
+    perm[pos] = i;
+    inv[i] = pos;
+  }
+}
+
 // ---- launchers --------------------------------------------------------------
 
 int launch_topk(const float* logits, int T, int E, int k, const float* bias, int bias_stride,
@@ -209,6 +314,32 @@ int launch_topk(const float* logits, int T, int E, int k, const float* bias, int
     default: MOE_TOPK_CASE(32)
   }
 #undef MOE_TOPK_CASE
+  return launch_status();
+}
+
+// One warp per token: beyond 32 tokens a warp would rank several in turn,
+// slower than the separate top-k kernel's one warp per token across the GPU.
+bool route_fused_ok(int T, int E, int k) { return T <= 32 && E <= 1024 && k <= 32; }
+
+int launch_route_fused(const float* logits, int T, int E, int k, const float* bias, int bias_stride,
+                       int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       int32_t* active, int32_t* n_active, int* status, cudaStream_t s) {
+  if (!route_fused_ok(T, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const size_t smem = (size_t)5 * E * 4 + (size_t)T * k * 4;
+  const int pl = (E + 31) / 32;
+#define MOE_ROUTE_CASE(P)                                                                                   \
+  route_small_kernel<P><<<1, 1024, smem, s>>>(logits, T, E, k, bias, bias_stride, idx, w, counts, offsets, \
+                                              perm, inv, active, n_active, status);                        \
+  break;
+  switch (pl <= 1 ? 1 : pl <= 2 ? 2 : pl <= 4 ? 4 : pl <= 8 ? 8 : pl <= 16 ? 16 : 32) {
+    case 1: MOE_ROUTE_CASE(1)
+    case 2: MOE_ROUTE_CASE(2)
+    case 4: MOE_ROUTE_CASE(4)
+    case 8: MOE_ROUTE_CASE(8)
+    case 16: MOE_ROUTE_CASE(16)
+    default: MOE_ROUTE_CASE(32)
+  }
+#undef MOE_ROUTE_CASE
   return launch_status();
 }
 
