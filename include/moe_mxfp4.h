@@ -133,13 +133,14 @@ typedef struct moe_layer {
 
 /* Kernel paths moe_forward can take (moe_query_path). */
 typedef enum moe_path {
-  MOE_PATH_DECODE_MMA = 1,   /* T < 32 where the single-launch kernel does not
-                                apply: per-stage kernels: router GEMV, top-k + sort,
-                                MXFP4 expert GEMVs on e4m3 mma.sync, combine */
+  MOE_PATH_DECODE_MMA = 1,   /* T <= 4 where the single-launch kernel does not
+                                apply (e.g. E > 512): per-stage kernels: router
+                                GEMV, top-k + sort, MXFP4 expert GEMVs on e4m3
+                                mma.sync, combine */
   MOE_PATH_DECODE_FUSED = 2, /* T <= 4: one cooperative persistent kernel per
                                 call (router, top-k, shared and routed experts,
                                 combine), one CTA per SM */
-  MOE_PATH_PREFILL_TC = 3    /* T >= 32: per-stage kernels with the routed
+  MOE_PATH_PREFILL_TC = 3    /* T >= 5: per-stage kernels with the routed
                                 experts as grouped GEMMs on block-scaled tcgen05
                                 MMAs (MXFP4 weights as E4M3 codes with E8M0
                                 scales, activations as E4M3 terms with E8M0

@@ -37,12 +37,13 @@ int current_device(DeviceInfo* out) {
 
 namespace {
 
-// Tokens from which the routed experts run as tcgen05 grouped GEMMs.
-constexpr int kPrefillMinT = 32;
-// Tensor-core path: tokens from which the combine (shared down + weighted
-// sum) runs as a tcgen05 GEMM, and from which the router + shared gate/up do
-// (below it their 10 or so 128-row blocks leave most SMs idle).
-constexpr int kDenseTcMinT = 32;
+// Tokens from which the routed experts run as tcgen05 grouped GEMMs (below
+// it, and only where the single-launch kernel cannot take the shape, they
+// run as warp-MMA GEMVs): measured faster than the warp-MMA path from 5.
+constexpr int kPrefillMinT = 5;
+// Tensor-core path: the combine (shared down + weighted sum) always runs as a
+// tcgen05 GEMM; the router + shared gate/up do from this many tokens (below
+// it their 10 or so 128-row blocks leave most SMs idle).
 constexpr int kFrontTcMinT = 128;
 
 // Workspace sections of one forward call (byte offsets from the base).
@@ -253,7 +254,7 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
                sh.has_shared ? static_cast<const __nv_bfloat16*>(L->shared_up) : nullptr, logits,
                at<float>(B, ws.h_sh)};
   // tcgen05 dense stages: h_sh as bf16 hi and lo terms in the fp32 h_sh section
-  const bool tcd = tc && T >= kDenseTcMinT && tc_dense_supported(T, d, I, k, sh.has_shared != 0, di);
+  const bool tcd = tc && tc_dense_supported(T, d, I, k, sh.has_shared != 0, di);
   __nv_bfloat16* h_hi = at<__nv_bfloat16>(B, ws.h_sh);
   __nv_bfloat16* h_lo = h_hi + (size_t)T * I;
   if (tcd) {

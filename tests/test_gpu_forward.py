@@ -103,6 +103,7 @@ def build(mx, w, set_idx=0):
     ("ragged", 17, 512, 96, 24, 5, "natural"),
     ("onehot", 3, 64, 32, 1, 1, "natural"),
     ("wide_k", 2, 128, 32, 40, 32, "natural"),
+    ("mma_e600", 3, 256, 64, 600, 4, "natural"),   # E > 512: warp-MMA per-stage path
     ("three", 3, 256, 64, 16, 3, "natural"),
     ("four_small", 4, 512, 128, 32, 4, "natural"),
     # T >= 32: routed experts on the tcgen05 grouped GEMMs
@@ -176,12 +177,13 @@ def test_mtp_t4(mx):
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("T", [8, 16])
-def test_ling_shape_per_stage_mma(mx, T):
-    """Ling shapes at 5 <= T < 32 (the per-stage e4m3 mma.sync path), every token."""
+@pytest.mark.parametrize("T", [5, 8, 16])
+def test_ling_shape_small_t_tensor_core(mx, T):
+    """Ling shapes at 5 <= T < 32 (the per-stage tcgen05 path with few tokens
+    per expert), every token."""
     w = dataclasses.replace(wl.WORKLOADS["ling_t1"], name=f"ling_t{T}", T=T, sets=1)
     layer, x, bias = build(mx, w, 0)
-    assert mx.moe_query_path(layer.shape, T) == mx.MOE_PATH_DECODE_MMA
+    assert mx.moe_query_path(layer.shape, T) == mx.MOE_PATH_PREFILL_TC
     out = run(mx, layer, x, bias, w.T, w.E, w.k)
     check_layer(w, 0, layer, x, bias, out, strict=True)
 
@@ -258,9 +260,11 @@ def test_paths(mx):
     s = mx.moe_shape(2560, 768, 512, 8, 1)
     assert mx.moe_query_path(s, 1) == mx.MOE_PATH_DECODE_FUSED
     assert mx.moe_query_path(s, 4) == mx.MOE_PATH_DECODE_FUSED
-    assert mx.moe_query_path(s, 5) == mx.MOE_PATH_DECODE_MMA
-    assert mx.moe_query_path(s, 31) == mx.MOE_PATH_DECODE_MMA
+    assert mx.moe_query_path(s, 5) == mx.MOE_PATH_PREFILL_TC
+    assert mx.moe_query_path(s, 31) == mx.MOE_PATH_PREFILL_TC
     assert mx.moe_query_path(s, 32) == mx.MOE_PATH_PREFILL_TC
+    # more than 512 experts do not fit the single-launch kernel: warp-MMA per-stage kernels
+    assert mx.moe_query_path(mx.moe_shape(256, 64, 600, 4, 1), 3) == mx.MOE_PATH_DECODE_MMA
     assert mx.moe_query_path(s, 4096) == mx.MOE_PATH_PREFILL_TC
     assert mx.moe_stage_names(mx.MOE_PATH_DECODE_FUSED) == ["decode_fused"]
     assert len(mx.moe_stage_names(mx.MOE_PATH_DECODE_MMA)) == 8
