@@ -45,6 +45,12 @@ constexpr int kPrefillMinT = 5;
 // tcgen05 GEMM; the router + shared gate/up do from this many tokens (below
 // it their 10 or so 128-row blocks leave most SMs idle).
 constexpr int kFrontTcMinT = 128;
+// Tensor-core routed GEMMs: items of up to 64 B rows (32 tokens with two
+// activation terms, 64 with one) while the mean tokens per expert, T k / E,
+// stays below 3/4 of that, else of up to 128 B rows. Graph-timed at the Ling
+// shape: 64-row items 896 against 968 us at T=1024, 128-row items 1,063
+// against 1,291 us at T=2048.
+constexpr int kNarrowRowsPerExpert = 48;   // T k terms < this x E: 64-row items
 
 // Workspace sections of one forward call (byte offsets from the base).
 struct Workspace {
@@ -307,6 +313,7 @@ int enqueue_forward(const moe_layer* L, const void* x_dev, int T, void* y_dev, c
     ua.act_q = at<uint8_t>(B, ws.xq);
     ua.act_s = at<uint8_t>(B, ws.xs);
     ua.act_terms = nterms;
+    ua.narrow = (int64_t)T * k * nterms < (int64_t)kNarrowRowsPerExpert * E ? 1 : 0;
     ua.out = at<float>(B, ws.h);
     ua.out_ld = I;
     ua.status = status;

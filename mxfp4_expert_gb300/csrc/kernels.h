@@ -63,6 +63,7 @@ struct RoutedArgs {
   float* out;               // gate/up: h [slots][N/2]; down: part [slots][N]
   int out_ld;
   int out_by_pair;          // tensor-core down pass: part row = perm[slot] (t k + j), not the slot
+  int narrow;               // tensor-core path: items of up to 64 B rows (few tokens per expert), else 128
   int* status;
 };
 int launch_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s);

@@ -58,10 +58,8 @@ constexpr int kUSliceKb = 4;                 // 32-wide K-blocks per slice: one 
 constexpr int kUSliceK = kUSliceKb * kMxBlock;
 constexpr int kUStages = 4;                  // operand stages (weights + activations + scales)
 constexpr int kUChunk = 2;                   // slices per raw weight copy
-constexpr int kURing = 3;                    // raw weight chunks in flight
 constexpr int kUPrefetchChunks = 8;          // weights prefetched into L2 about this many chunks ahead
 constexpr int kUAcc = 2;                     // accumulators in tensor memory
-constexpr int kUCols = 128;                  // B rows per item = largest MMA N
 constexpr int kUSfCols = 8;                  // tensor-memory columns of one stage's scales (A: 4, B: 4)
 constexpr uint32_t kUTmemCols = 512;         // 2 x 128 accumulator + 4 x 8 scale columns, as a power of two
 constexpr int kUMaxActive = 1024;
@@ -69,7 +67,6 @@ constexpr int kUTable = 256;                 // items per CTA with a precomputed
 constexpr uint32_t kUTileChunk = kUChunk * kUSliceKb * kUnitBytes;   // one tile's part of a chunk
 constexpr uint32_t kURawBytes = kUTiles * kUTileChunk;                  // one chunk of packed weights
 constexpr uint32_t kUABytes = kURows * kUSliceK;                     // one slice of weights (E2M1 chunks)
-constexpr uint32_t kUBBytes = kUCols * kUSliceK;                     // one slice of E4M3 activations
 constexpr uint32_t kUSfBytes = 512;                                  // scales of 128 rows x 4 K-blocks
 
 // warp roles
@@ -81,6 +78,13 @@ constexpr int kScanThreads = 256;
 struct UmmaSmem {
   uint32_t ring, a, b, sfa, sfb, iofs, itab, bars, misc, total;
 };
+// Two configurations (template arguments COLS, RING of the kernel and of its
+// shared-memory plan): wide items of up to 128 B rows with a 3-chunk raw
+// ring, for many tokens per expert; narrow items of up to 64 B rows, whose
+// smaller activation stages leave room for a 5-chunk raw ring (more weight
+// bytes in flight), for few tokens per expert.
+constexpr int kUColsWide = 128, kURingWide = 3, kUColsNarrow = 64, kURingNarrow = 5;
+template <int COLS, int RING>
 __host__ __device__ inline UmmaSmem umma_smem() {
   UmmaSmem m{};
   uint32_t at = 0;
@@ -90,14 +94,14 @@ __host__ __device__ inline UmmaSmem umma_smem() {
     at += bytes;
     return here;
   };
-  m.ring = take(kURing * kURawBytes, 128);
+  m.ring = take(RING * kURawBytes, 128);
   m.a = take(kUStages * kUABytes, 1024);
-  m.b = take(kUStages * kUBBytes, 1024);
+  m.b = take(kUStages * uint32_t(COLS) * kUSliceK, 1024);
   m.sfa = take(kUStages * kUSfBytes, 128);
   m.sfb = take(kUStages * kUSfBytes, 128);
   m.iofs = take((kUMaxActive + 1) * 4, 16);
   m.itab = take(kUTable * 16, 16);
-  m.bars = take((2 * kURing + 3 * kUStages + 2 * kUAcc) * 8, 8);
+  m.bars = take((2 * RING + 3 * kUStages + 2 * kUAcc) * 8, 8);
   m.misc = take(16, 16);   // tensor-memory address, abort flag
   m.total = at + 1024;     // slack: the swizzled buffers are aligned to 1024 in the shared window
   return m;
@@ -125,8 +129,11 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int MODE>
+template <int MODE, int COLS, int RING>
 __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, UmmaSmem L) {
+  constexpr int kUCols = COLS;                                    // B rows per item = largest MMA N
+  constexpr int kURing = RING;                                    // raw weight chunks in flight
+  constexpr uint32_t kUBBytes = uint32_t(kUCols) * kUSliceK;      // one slice of E4M3 activations
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the 128-byte swizzle is a function of the shared address: align the plan's base to 1024
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -524,22 +531,28 @@ __global__ void __launch_bounds__(kUBlock, 1) umma_routed_kernel(RoutedArgs a, U
   }
 }
 
-}  // namespace
-
-int launch_umma_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s) {
-  const UmmaSmem L = umma_smem();
+template <int COLS, int RING>
+int launch_umma_cfg(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s) {
+  const UmmaSmem L = umma_smem<COLS, RING>();
   if (L.total > di.smem_optin) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int grid = di.sm_count;
   if (mode == kModeGateUp) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      int(L.total)));
-    umma_routed_kernel<kModeGateUp><<<grid, kUBlock, L.total, s>>>(a, L);
+    MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeGateUp, COLS, RING>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total)));
+    umma_routed_kernel<kModeGateUp, COLS, RING><<<grid, kUBlock, L.total, s>>>(a, L);
   } else {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      int(L.total)));
-    umma_routed_kernel<kModeDown><<<grid, kUBlock, L.total, s>>>(a, L);
+    MOE_CUDA_TRY(cudaFuncSetAttribute(umma_routed_kernel<kModeDown, COLS, RING>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(L.total)));
+    umma_routed_kernel<kModeDown, COLS, RING><<<grid, kUBlock, L.total, s>>>(a, L);
   }
   return launch_status();
+}
+
+}  // namespace
+
+int launch_umma_routed(RoutedMode mode, const RoutedArgs& a, const DeviceInfo& di, cudaStream_t s) {
+  return a.narrow ? launch_umma_cfg<kUColsNarrow, kURingNarrow>(mode, a, di, s)
+                  : launch_umma_cfg<kUColsWide, kURingWide>(mode, a, di, s);
 }
 
 }  // namespace moe
