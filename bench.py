@@ -503,9 +503,10 @@ def run_ours(args, w):
         e2e["eager"] = {"value": dt_e * 1e6 / (e_steps * n_sets * ws), "unit": "us/layer", "steps": e_steps,
                         "how": "moe_forward called from Python per layer, host clock, pinned copies each step"}
 
-    # top-k and the sort are one launch up to 32 tokens
+    # top-k and the sort are one launch up to 32 tokens; the sort is one launch
+    # up to 128 (one chunk), else three
     launches_per_call = {"decode_fused": 1, "act_split_x": 1, "router_shared_gateup": 1, "topk": 1,
-                         "sort": 0 if w.T <= 32 else 3,
+                         "sort": 0 if w.T <= 32 else (1 if w.T <= 128 else 3),
                          "quant_x": 1, "routed_gateup": 1, "quant_h": 1, "routed_down": 1, "combine": 1}
     per_call = sum(launches_per_call.get(n, 1) for n in stages)
 

@@ -203,13 +203,15 @@ sort_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
   }
 }
 
-// ---- top-k and sort in one block, for T <= 32 tokens ------------------------
-// The same steps as topk_kernel and the three sort kernels for one chunk:
-// warp w ranks tokens w, w + 32, ...; thread e < E then owns expert e for the
-// counts and the scans (offsets, active list); the scatter ranks each entry
-// among the chunk's tokens that chose its expert (bit masks). One launch
-// instead of four.
-template <int PL>
+// ---- the sort of one chunk (T <= kSortChunk) in one block, with or without
+// the top-k before it ------------------------------------------------------------
+// The same steps as the three sort kernels for one chunk: thread e < E owns
+// expert e for the counts and the scans (offsets, active list); the scatter
+// ranks each entry among the chunk's tokens that chose its expert (bit
+// masks). With TOPK (T <= 32) warp w first ranks tokens w, w + 32, ... as
+// topk_kernel does: one launch instead of four; without it the entries come
+// from idx: one launch instead of three.
+template <int PL, bool TOPK>
 __global__ void __launch_bounds__(1024)
 route_small_kernel(const float* __restrict__ logits, int T, int E, int k, const float* __restrict__ bias,
                    int bias_stride, int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts,
@@ -222,7 +224,11 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, const 
   __shared__ int32_t warp_sum[2][32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 5 * E; i += blockDim.x) rs[i] = 0u;
-  for (int t = warp; t < T; t += 32) topk_token<PL>(logits, t, E, k, bias, bias_stride, lane, idx, w, sidx);
+  if constexpr (TOPK) {
+    for (int t = warp; t < T; t += 32) topk_token<PL>(logits, t, E, k, bias, bias_stride, lane, idx, w, sidx);
+  } else {
+    for (int i = tid; i < T * k; i += blockDim.x) sidx[i] = idx[i];
+  }
   __syncthreads();
   const int n = T * k;
   auto valid = [&](int t, int j) {   // in range, and the token's first entry of its expert
@@ -327,9 +333,9 @@ int launch_route_fused(const float* logits, int T, int E, int k, const float* bi
   if (!route_fused_ok(T, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const size_t smem = (size_t)5 * E * 4 + (size_t)T * k * 4;
   const int pl = (E + 31) / 32;
-#define MOE_ROUTE_CASE(P)                                                                                   \
-  route_small_kernel<P><<<1, 1024, smem, s>>>(logits, T, E, k, bias, bias_stride, idx, w, counts, offsets, \
-                                              perm, inv, active, n_active, status);                        \
+#define MOE_ROUTE_CASE(P)                                                                                         \
+  route_small_kernel<P, true><<<1, 1024, smem, s>>>(logits, T, E, k, bias, bias_stride, idx, w, counts, offsets, \
+                                                    perm, inv, active, n_active, status);                        \
   break;
   switch (pl <= 1 ? 1 : pl <= 2 ? 2 : pl <= 4 ? 4 : pl <= 8 ? 8 : pl <= 16 ? 16 : 32) {
     case 1: MOE_ROUTE_CASE(1)
@@ -352,6 +358,12 @@ int launch_sort(const int32_t* idx, int T, int k, int E, int32_t* counts, int32_
                 int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* ws,
                 int* status, cudaStream_t s) {
   const int chunks = (T + kSortChunk - 1) / kSortChunk;
+  if (chunks == 1 && E <= 1024 && k <= 32) {   // one chunk: one block, one launch
+    const size_t smem = (size_t)5 * E * 4 + (size_t)T * k * 4;
+    route_small_kernel<1, false><<<1, 1024, smem, s>>>(nullptr, T, E, k, nullptr, 0, const_cast<int32_t*>(idx),
+                                                       nullptr, counts, offsets, perm, inv, active, n_active, status);
+    return launch_status();
+  }
   int32_t* chunk_counts = static_cast<int32_t*>(ws);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) +
                                                    round_up((size_t)chunks * E * sizeof(int32_t), 256));
