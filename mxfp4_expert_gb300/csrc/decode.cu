@@ -1,5 +1,9 @@
 // Single-launch decode path (T <= 4 tokens): the whole layer in one kernel
-// launch, one CTA per SM, 32 warps per CTA.
+// launch, one CTA per SM, 32 warps per CTA. The layer is the mixture-of-
+// experts block of page "3 ways to speed up MoE inference on NVIDIA DGX
+// Spark": 512 routed experts, top-8, one shared expert (§2), expert
+// intermediate size 768 (§3); T = 1 is the single-token decode, T = 4 the
+// verify step of the 4-token speculative decoding in §5.
 //
 // Phases of one CTA c of G:
 //   0. griddepcontrol.launch_dependents, then L2 prefetch of this CTA's

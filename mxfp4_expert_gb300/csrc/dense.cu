@@ -1,5 +1,7 @@
 // bf16 GEMMs on the warp-level tensor-core MMA (m16n8k16, fp32 accumulate)
-// for the routing-independent dense parts of the per-stage path:
+// for the routing-independent dense parts of the per-stage path. The router
+// and the shared expert stay in bf16 (page "MoE-SpeQ ...", §2.1-§2.2: routing
+// is sensitive to quantisation, and the shared expert acts on every token):
 //   * the router and the shared expert's gate/up projections in one kernel
 //     (SwiGLU in the epilogue), and
 //   * the combine: the shared down projection plus the routing-weighted sum of

@@ -1,4 +1,7 @@
-// Routed-expert GEMVs over MXFP4 weights (gate/up with SwiGLU, and down).
+// Routed-expert GEMVs over MXFP4 weights (gate/up with SwiGLU, and down):
+// the W4 experts of page "3 ways to speed up MoE inference on NVIDIA DGX
+// Spark", §2-§3, each run once over the tokens sorted to it (page
+// "MoE-SpeQ ...", §4.2).
 //
 // Each work item is one 16-row tile of one active expert's matrix over the
 // whole K, for one chunk of at most 8 of that expert's activation rows. The

@@ -1,5 +1,7 @@
 // Dense bf16 GEMMs of the per-stage path on the 5th-generation tensor cores,
-// for many tokens:
+// for many tokens. The router and the shared expert stay in bf16 (page
+// "MoE-SpeQ ...", §2.1-§2.2: routing is sensitive to quantisation, and the
+// shared expert acts on every token):
 //   * front: the router logits and the shared expert's gate/up projections
 //     with SwiGLU, h_sh going out as two bf16 terms (hi = bf16(h), lo =
 //     bf16(h - hi));

@@ -1,6 +1,10 @@
 // Routed-expert GEMMs on the 5th-generation tensor cores (tcgen05) with
-// block-scaled MMAs, for large token counts (prefill): gate/up with SwiGLU,
-// and down.
+// block-scaled MMAs, from 5 tokens up to prefill: gate/up with SwiGLU, and
+// down. The experts are the MXFP4 (W4) experts of page "3 ways to speed up
+// MoE inference on NVIDIA DGX Spark", §2-§3, run with bf16 activations or, in
+// the W4A8 configuration of §2, 8-bit ones; each expert runs once over the
+// tokens that chose it, after they are sorted by expert (page "MoE-SpeQ ...",
+// §4.2).
 //
 // Every MMA is tcgen05.mma.kind::mxf8f6f4.block_scale: A = 128 weight rows x
 // K 32 as E2M1 codes, B = activation rows x K 32 as E4M3 codes, each with one
