@@ -189,16 +189,43 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_sha(path):
+    """sha256 prefix of a C/CUDA source's code: comments and blank lines
+    removed, so an edit to comments alone keeps the key of counters taken on
+    the same code (string and character literals are kept as they are)."""
+    src = open(path, encoding="utf-8").read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":   # literal: copy through the closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    code = "\n".join(ln.rstrip() for ln in "".join(out).splitlines() if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
 def profiled_traffic(kernel_src, kernel, workload):
     """dram bytes per launch of `kernel` on `workload` from profiles/dram_traffic.txt,
-    if the kernel source is unchanged since the counters were taken."""
+    if the kernel's code is unchanged since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    sha = code_sha(kernel_src)
     for ln in open(p):
         f = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
-        if f.get("kernel") == kernel and f.get("src_sha") == sha and f.get("workload") == workload:
+        if f.get("kernel") == kernel and f.get("code_sha") == sha and f.get("workload") == workload:
             return int(float(f["bytes_per_launch"]))
     return None
 
