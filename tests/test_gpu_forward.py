@@ -139,9 +139,13 @@ def test_tc_items_beyond_table(mx):
     check_layer(w, 0, layer, x, bias, out, tokens=range(0, w.T, 347))
 
 
-def test_no_shared_expert(mx):
+@pytest.mark.parametrize("T", [4, 40, 200])
+def test_no_shared_expert(mx, T):
+    """Without a shared expert: the single-launch kernel (T=4) and the
+    tensor-core path (T=40, 200), where the dense stages stay on the warp-MMA
+    kernels and the routed partials are combined by sorted slot."""
     from mxfp4_expert_gb300 import synthetic
-    w = wl.Workload("noshared", T=4, d=256, I=64, E=16, k=2, sets=1, routing="natural", seed=5)
+    w = wl.Workload("noshared", T=T, d=256, I=64, E=16, k=2, sets=1, routing="natural", seed=5)
     full = synthetic.build_layer(w, 0)
     layer = mx.Layer(full.router_w, full.gate_up, full.struct.gate_up_desc, full.down,
                      full.struct.down_desc, top_k=w.k)
